@@ -1,0 +1,192 @@
+/*
+ * moeroute.h -- C ABI of libmoeroute: MoE expert-routing statistics for
+ * locality-aware serving, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations:
+ *   [ELDR]  "ELDR: Expert-Locality-Aware Decode Routing for PD-Disaggregated
+ *           MoE Serving" (blog summary of arXiv 2607.00466).
+ *   [GRACE] "GRACE-MoE: grouping, replication and locality-aware routing for
+ *           distributed MoE inference" (research-notes summary).
+ *
+ * General conventions (every entry point):
+ *   - All tensor pointers are DEVICE pointers to caller-owned memory unless a
+ *     comment says "host".  The library allocates nothing and never frees.
+ *   - Layouts are dense and row-major as stated per argument.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     never synchronise the device, except moer_ws_status.
+ *   - Argument errors detectable on the host return a non-zero status and
+ *     launch nothing.  A failed launch returns MOER_ECUDA.
+ *   - Malformed DEVICE data (a block table that does not tile the tokens, a
+ *     cache slot out of range) is detected by the kernels, which then skip
+ *     the offending work and record MOER_EDATA in the workspace's status
+ *     word; moer_ws_status reports it.  No kernel traps.
+ *   - Device waits are bounded; an expired wait records MOER_ETIMEOUT.
+ *   - Limits: 4 <= E <= 256 with E % 4 == 0; 1 <= k <= min(E, 32);
+ *     1 <= L <= 256; 0 <= m <= L; 1 <= B <= 255; 1 <= D <= 64;
+ *     T < 2^31 per call; every count fits in int32.
+ */
+#ifndef MOEROUTE_H
+#define MOEROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOER_API __attribute__((visibility("default")))
+#else
+#define MOER_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* moer_stream_t;
+
+typedef enum moer_status {
+  MOER_OK = 0,
+  MOER_EINVAL = 1,   /* NULL or misaligned pointer, bad enum/flag value      */
+  MOER_ESHAPE = 2,   /* sizes inconsistent with each other                   */
+  MOER_ERANGE = 3,   /* a size or parameter outside the library limits        */
+  MOER_ECUDA = 4,    /* a CUDA runtime call or kernel launch failed           */
+  MOER_ENOMEM = 5,   /* the workspace passed is smaller than required         */
+  MOER_EDATA = 6,    /* device-side validation rejected input data            */
+  MOER_ETIMEOUT = 7  /* a bounded device-side wait expired                    */
+} moer_status;
+
+/* Shape of the routing problem. */
+typedef struct moer_dims {
+  int32_t E;            /* experts per MoE layer                                    */
+  int32_t k;            /* experts selected per token (top-k)                       */
+  int32_t L;            /* MoE layers present in the logits tensor                  */
+  int32_t m;            /* number of signature (mask) layers                        */
+  const int32_t* mask;  /* HOST pointer: m strictly increasing layer ids in [0, L)  */
+  int32_t block;        /* KV block size B in tokens                                */
+} moer_dims;
+
+/* Bytes of device workspace the calls below need for T computed tokens,
+ * nblk KV blocks, R requests and D decoders (pass 0 for sizes a call does not
+ * use).  One workspace may serve every call issued on one stream in order. */
+MOER_API size_t moer_workspace_bytes(const moer_dims* d, int64_t T, int32_t nblk, int32_t R, int32_t D);
+
+/* Top-k gating, per-KV-block signature counts and expert co-activation, in
+ * one pass over the router logits.
+ *   [ELDR] section "What it tries to solve" (each MoE token picks its own
+ *   top-k experts) and section "Key idea / structure / operation" (the gate
+ *   output is unchanged; the prefill hook records discrete top-k counts per
+ *   KV block over the selected layer mask); [GRACE] section 3 "Key
+ *   observations" and section 4 "Method", Figure 2(a) (per-layer expert
+ *   co-activation profiling).
+ *
+ * logits    [L][T][E] fp32, 16-byte aligned.  Row (l, t) holds the router
+ *           logits of computed token t at MoE layer l.
+ * T         computed tokens in this call (0 is a no-op).
+ * blk_tab   [nblk][2] int32 (tok0, len): the KV blocks of the computed
+ *           tokens in order; they must tile [0, T) contiguously and have
+ *           1 <= len <= B.  May be NULL when blk_cnt is NULL.
+ * topk      [L][T][k] uint8 or NULL: expert ids in rank order.  Ranking:
+ *           larger logit first; equal logits (-0.0 == +0.0) rank the lower
+ *           expert id first; NaN ranks below every number.
+ * blk_cnt   [nblk][m][E] uint8 or NULL: blk_cnt[b][i][e] = number of tokens
+ *           of block b whose top-k at layer mask[i] contains e (<= B).
+ * affinity  [L][E][E] int32 or NULL: ACCUMULATED (+=) co-activation counts,
+ *           affinity[l][a][b] += #tokens whose top-k at layer l holds a and b
+ *           (diagonal = expert load).  The caller zeroes it; streamed chunks
+ *           sum.  4-byte aligned.
+ * ws        device workspace of at least moer_workspace_bytes(d, T, nblk, 0, 0).
+ */
+MOER_API moer_status moer_topk_signature(const moer_dims* d, const float* logits, int64_t T,
+                                const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
+                                uint8_t* blk_cnt, int32_t* affinity, void* ws,
+                                size_t ws_bytes, moer_stream_t stream);
+
+/* Prefix-cache stitching of per-block counts into per-request counts.
+ *   [ELDR] table of what existing decode routing misses (signature cache),
+ *   component table (signature cache) and section "Practical
+ *   interpretation": a signature cache co-indexed with the KV cache keeps
+ *   the full-prompt signature on prefix hits.
+ * First every FULL computed block b (len == B) with insert_slot[b] >= 0 is
+ * copied into cache[insert_slot[b]]; then
+ *   req_cnt[r][i][e] = sum over c in [req_cache_off[r], req_cache_off[r+1])
+ *                      of cache[cache_idx[c]][i][e]
+ *                    + sum over b in [req_blk_off[r], req_blk_off[r+1])
+ *                      of blk_cnt[b][i][e].
+ * A request may therefore reuse blocks inserted in the same call by an
+ * earlier request.  Partial blocks are never inserted.
+ *
+ * blk_cnt [nblk][m][E] uint8; blk_tab [nblk][2] (tok0, len) as above;
+ * req_blk_off [R+1] int32; cache [nslots][m][E] uint8 (in/out) or NULL
+ * together with cache_idx [ncached], req_cache_off [R+1] and
+ * insert_slot [nblk] (all NULL when there is no cache);
+ * req_cnt [R][m][E] int32 (overwritten).  Slot ids outside [0, nslots)
+ * are skipped and recorded as MOER_EDATA in ws (ws may be NULL: then
+ * they are skipped silently).
+ */
+MOER_API moer_status moer_block_stitch(const moer_dims* d, const uint8_t* blk_cnt,
+                              const int32_t* blk_tab, int32_t nblk,
+                              const int32_t* req_blk_off, int32_t R,
+                              const int32_t* cache_idx, const int32_t* req_cache_off,
+                              uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
+                              int32_t* req_cnt, void* ws, size_t ws_bytes,
+                              moer_stream_t stream);
+
+/* Expert and group loads and load skew from the affinity matrices.
+ *   [GRACE] section 4 "Method" (load statistics from profiling), section 4.2
+ *   "Expert replication" (rho = W_max / W_mean) and section 7 glossary.
+ * affinity [L][E][E] int32; group_of [L][E] int32 in [0, G).
+ * W_expert [L][E] int64 = affinity[l][e][e];
+ * W_group  [L][G] int64 = sum of W_expert over the group's experts;
+ * rho_group [L] fp64 = max_g W_group / (sum_g W_group / G), 0 if the sum is 0;
+ * rho_expert [L] fp64 = the same over the E experts.  Any output may be NULL.
+ * Group ids outside [0, G) are skipped.
+ */
+MOER_API moer_status moer_affinity_load(const moer_dims* d, const int32_t* affinity,
+                               const int32_t* group_of, int32_t G, int64_t* W_expert,
+                               int64_t* W_group, double* rho_group, double* rho_expert,
+                               moer_stream_t stream);
+
+/* Signature, centroid distances and tau-band least-loaded decoder choice.
+ *   [ELDR] section "Key idea / structure / operation": count * idf
+ *   signature over the layer mask; comparison with D decoder centroids; the
+ *   least-loaded decoder within the tau = 0.1 locality band of the nearest.
+ * req_cnt [R][m][E] int32; idf [m][E] fp32; centroids [D][m*E] fp32.
+ * sig   [R][m*E] fp32 or NULL: s = w / ||w||_2, w = req_cnt * idf (0 if w == 0).
+ * dist  [R][D] fp32 or NULL: Euclidean ||s - c_d||_2.
+ * choice [R] int32: d_min = min_d dist; band = {d : dist_d <= d_min + tau};
+ *        the band member with the smallest load, ties to the lowest index.
+ * loads [D] int32: live == 0: read only; live == 1: requests are routed in
+ *        index order and each adds 1 to its decoder's load (updated in place).
+ * ws    at least moer_workspace_bytes(d, 0, 0, R, D) bytes.
+ */
+MOER_API moer_status moer_route(const moer_dims* d, const int32_t* req_cnt, int32_t R,
+                       const float* idf, const float* centroids, int32_t D, float tau,
+                       int32_t* loads, int32_t live, float* sig, float* dist,
+                       int32_t* choice, void* ws, size_t ws_bytes, moer_stream_t stream);
+
+/* Calibration helper (not on the per-request path): smoothed idf over R
+ * calibration requests.  [ELDR] section "Key idea / structure / operation"
+ * (idf reweighting fit offline on calibration prompts; formula not printed).
+ * idf[i][e] = ln((1 + R) / (1 + df)) + 1, df = #{r : req_cnt[r][i][e] > 0},
+ * evaluated in double and rounded to fp32.  req_cnt [R][m][E] int32.
+ */
+MOER_API moer_status moer_idf_fit(const moer_dims* d, const int32_t* req_cnt, int32_t R, float* idf,
+                         moer_stream_t stream);
+
+/* Waits for `stream`, then returns the status recorded in the workspace
+ * (MOER_OK, MOER_EDATA or MOER_ETIMEOUT) and clears it.  `ws` is a device
+ * workspace passed to earlier calls. */
+MOER_API moer_status moer_ws_status(void* ws, moer_stream_t stream);
+
+/* Static description of a status code. */
+MOER_API const char* moer_status_str(moer_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MOER_API int32_t moer_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEROUTE_H */

@@ -1,0 +1,194 @@
+// api.cu -- the extern "C" entry points of libmoeroute: argument validation,
+// workspace accounting and dispatch to the kernels.  Nothing here computes
+// routing statistics; every step runs on the GPU.
+#include <cstring>
+
+#include "common.cuh"
+
+namespace moer {
+int k1_tile_tokens(int E);
+moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64_t T,
+                                  const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
+                                  uint8_t* blk_cnt, int32_t* affinity, void* ws, cudaStream_t st);
+moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, const int32_t* blk_tab,
+                                int32_t nblk, const int32_t* req_blk_off, int32_t R,
+                                const int32_t* cache_idx, const int32_t* req_cache_off,
+                                uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
+                                int32_t* req_cnt, uint32_t* status, cudaStream_t st);
+moer_status affinity_load_launch(const moer_dims* d, const int32_t* affinity, const int32_t* group_of,
+                                 int32_t G, int64_t* W_expert, int64_t* W_group, double* rho_group,
+                                 double* rho_expert, cudaStream_t st);
+moer_status route_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, const float* idf,
+                         const float* centroids, int32_t D, float tau, int32_t* loads, int32_t live,
+                         float* sig, float* dist, int32_t* choice, void* ws, cudaStream_t st);
+moer_status idf_fit_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, float* idf,
+                           cudaStream_t st);
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+moer_status check_dims(const moer_dims* d, bool need_mask) {
+  if (d == nullptr) return MOER_EINVAL;
+  if (d->E < 4 || d->E > 256 || d->E % 4 != 0) return MOER_ERANGE;
+  if (d->k < 1 || d->k > 32 || d->k > d->E) return MOER_ERANGE;
+  if (d->L < 1 || d->L > 256) return MOER_ERANGE;
+  if (d->m < 0 || d->m > d->L) return MOER_ERANGE;
+  if (d->block < 1 || d->block > 255) return MOER_ERANGE;
+  if (d->m > 0 || need_mask) {
+    if (d->m > 0 && d->mask == nullptr) return MOER_EINVAL;
+    for (int i = 0; i < d->m; ++i) {
+      if (d->mask[i] < 0 || d->mask[i] >= d->L) return MOER_ERANGE;
+      if (i > 0 && d->mask[i] <= d->mask[i - 1]) return MOER_EINVAL;
+    }
+  }
+  return MOER_OK;
+}
+
+}  // namespace
+}  // namespace moer
+
+using namespace moer;
+
+extern "C" {
+
+size_t moer_workspace_bytes(const moer_dims* d, int64_t T, int32_t nblk, int32_t R, int32_t D) {
+  (void)nblk;
+  size_t scratch = 0;
+  if (d != nullptr && d->E >= 4 && d->E <= 256 && T > 0) {
+    const int TT = k1_tile_tokens(d->E);
+    scratch = round256((size_t)((T + TT - 1) / TT) * sizeof(int32_t));
+  }
+  if (R > 0 && D > 0) {
+    const size_t route = round256((size_t)R * (size_t)D * sizeof(float));
+    scratch = route > scratch ? route : scratch;
+  }
+  return WS_HEADER + scratch;
+}
+
+moer_status moer_topk_signature(const moer_dims* d, const float* logits, int64_t T,
+                                const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
+                                uint8_t* blk_cnt, int32_t* affinity, void* ws, size_t ws_bytes,
+                                moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (T < 0 || nblk < 0) return MOER_ERANGE;
+  if (T >= (int64_t(1) << 31)) return MOER_ERANGE;
+  if (T == 0) return MOER_OK;
+  if (logits == nullptr || !aligned(logits, 16)) return MOER_EINVAL;
+  if (affinity != nullptr && !aligned(affinity, 4)) return MOER_EINVAL;
+  const bool hist = blk_cnt != nullptr && d->m > 0;
+  if (hist) {
+    if (blk_tab == nullptr || !aligned(blk_tab, 4) || !aligned(blk_cnt, 4)) return MOER_EINVAL;
+    if (nblk < 1 || nblk > T) return MOER_ESHAPE;
+  }
+  if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
+  if (ws_bytes < moer_workspace_bytes(d, T, nblk, 0, 0)) return MOER_ENOMEM;
+  return topk_signature_launch(d, logits, T, blk_tab, nblk, topk, blk_cnt, affinity, ws,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+moer_status moer_block_stitch(const moer_dims* d, const uint8_t* blk_cnt, const int32_t* blk_tab,
+                              int32_t nblk, const int32_t* req_blk_off, int32_t R,
+                              const int32_t* cache_idx, const int32_t* req_cache_off,
+                              uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
+                              int32_t* req_cnt, void* ws, size_t ws_bytes, moer_stream_t stream) {
+  moer_status s = check_dims(d, true);
+  if (s != MOER_OK) return s;
+  if (d->m < 1) return MOER_ERANGE;
+  if (R < 0 || nblk < 0 || nslots < 0) return MOER_ERANGE;
+  if (R == 0) return MOER_OK;
+  if (req_blk_off == nullptr || req_cnt == nullptr) return MOER_EINVAL;
+  if (nblk > 0 && (blk_cnt == nullptr || !aligned(blk_cnt, 4))) return MOER_EINVAL;
+  const bool has_cache = cache != nullptr;
+  if (has_cache) {
+    if (!aligned(cache, 4) || req_cache_off == nullptr) return MOER_EINVAL;
+    if (insert_slot != nullptr && blk_tab == nullptr) return MOER_EINVAL;
+  } else if (cache_idx != nullptr || req_cache_off != nullptr || insert_slot != nullptr) {
+    return MOER_EINVAL;
+  }
+  if (ws != nullptr && (!aligned(ws, 16) || ws_bytes < WS_HEADER)) return MOER_ENOMEM;
+  return block_stitch_launch(d, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, req_cache_off,
+                             cache, nslots, insert_slot, req_cnt,
+                             ws ? reinterpret_cast<uint32_t*>(ws) : nullptr,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+moer_status moer_affinity_load(const moer_dims* d, const int32_t* affinity, const int32_t* group_of,
+                               int32_t G, int64_t* W_expert, int64_t* W_group, double* rho_group,
+                               double* rho_expert, moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (affinity == nullptr) return MOER_EINVAL;
+  if ((W_group != nullptr || rho_group != nullptr)) {
+    if (group_of == nullptr) return MOER_EINVAL;
+    if (G < 1 || G > 4096) return MOER_ERANGE;
+  }
+  if (G < 1) G = 1;
+  return affinity_load_launch(d, affinity, group_of, G, W_expert, W_group, rho_group, rho_expert,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+moer_status moer_route(const moer_dims* d, const int32_t* req_cnt, int32_t R, const float* idf,
+                       const float* centroids, int32_t D, float tau, int32_t* loads, int32_t live,
+                       float* sig, float* dist, int32_t* choice, void* ws, size_t ws_bytes,
+                       moer_stream_t stream) {
+  moer_status s = check_dims(d, true);
+  if (s != MOER_OK) return s;
+  if (d->m < 1) return MOER_ERANGE;
+  if (R < 0 || D < 1 || D > 64) return MOER_ERANGE;
+  if (live != 0 && live != 1) return MOER_EINVAL;
+  if (!(tau >= 0.f)) return MOER_ERANGE;
+  if (R == 0) return MOER_OK;
+  if (req_cnt == nullptr || idf == nullptr || centroids == nullptr || loads == nullptr ||
+      choice == nullptr)
+    return MOER_EINVAL;
+  if (live && dist == nullptr) {
+    if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
+    if (ws_bytes < moer_workspace_bytes(d, 0, 0, R, D)) return MOER_ENOMEM;
+  }
+  return route_launch(d, req_cnt, R, idf, centroids, D, tau, loads, live, sig, dist, choice, ws,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+moer_status moer_idf_fit(const moer_dims* d, const int32_t* req_cnt, int32_t R, float* idf,
+                         moer_stream_t stream) {
+  moer_status s = check_dims(d, true);
+  if (s != MOER_OK) return s;
+  if (d->m < 1) return MOER_ERANGE;
+  if (R < 1) return MOER_ERANGE;
+  if (req_cnt == nullptr || idf == nullptr) return MOER_EINVAL;
+  return idf_fit_launch(d, req_cnt, R, idf, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moer_status moer_ws_status(void* ws, moer_stream_t stream) {
+  if (ws == nullptr) return MOER_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t h[2] = {0u, 0u};
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOER_ECUDA;
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOER_ECUDA;
+  if (cudaMemset(ws, 0, sizeof(h)) != cudaSuccess) return MOER_ECUDA;
+  if (h[0] & WS_BIT_ETIMEOUT) return MOER_ETIMEOUT;
+  if (h[0] & WS_BIT_EDATA) return MOER_EDATA;
+  return MOER_OK;
+}
+
+const char* moer_status_str(moer_status s) {
+  switch (s) {
+    case MOER_OK: return "ok";
+    case MOER_EINVAL: return "invalid argument (null or misaligned pointer, bad flag)";
+    case MOER_ESHAPE: return "inconsistent sizes";
+    case MOER_ERANGE: return "size or parameter outside the library limits";
+    case MOER_ECUDA: return "CUDA call or kernel launch failed";
+    case MOER_ENOMEM: return "workspace too small";
+    case MOER_EDATA: return "device-side validation rejected input data";
+    case MOER_ETIMEOUT: return "bounded device wait expired";
+  }
+  return "unknown status";
+}
+
+int32_t moer_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,138 @@
+"""One routing-statistics step over a batch, through the C ABI.
+
+`RoutingStats` owns the caller-side buffers the C ABI expects (PyTorch
+allocates them; the library allocates nothing) and issues, on one CUDA
+stream:
+
+  moer_topk_signature  top-k + per-KV-block counts + co-activation (one pass)
+  moer_block_stitch    prefix-cache stitching into per-request counts
+  moer_affinity_load   expert / group loads and skew from the co-activation
+  moer_route           signatures, centroid distances, tau-band decoder choice
+
+This module only marshals arguments and orders calls; every step of the
+path runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _native as nat
+
+
+@dataclasses.dataclass
+class BatchDev:
+    """Device copies of one batch's metadata (see gen.workloads.Batch)."""
+    T: int
+    R: int
+    nblk: int
+    blk_tab: torch.Tensor
+    req_blk_off: torch.Tensor
+    cache_idx: Optional[torch.Tensor]
+    req_cache_off: Optional[torch.Tensor]
+    insert_slot: Optional[torch.Tensor]
+
+    @staticmethod
+    def from_host(b, device="cuda", with_cache=True, pin=False) -> "BatchDev":
+        def t(a, dt=torch.int32):
+            x = torch.from_numpy(np.ascontiguousarray(a)).to(dt)
+            if pin:
+                x = x.pin_memory()
+            return x.to(device, non_blocking=pin)
+        ci = t(b.cache_idx) if with_cache and len(b.cache_idx) else None
+        return BatchDev(T=b.T, R=b.R, nblk=b.nblk, blk_tab=t(b.blk_tab.reshape(-1)),
+                        req_blk_off=t(b.req_blk_off),
+                        cache_idx=ci if with_cache else None,
+                        req_cache_off=t(b.req_cache_off) if with_cache else None,
+                        insert_slot=t(b.insert_slot) if with_cache else None)
+
+
+class RoutingStats:
+    """Holds the model/serving state of the path and runs steps over batches."""
+
+    def __init__(self, E, k, L, mask, block, *, D, tau, centroids, idf, loads, live, G, group_of,
+                 nslots=0, max_T=0, max_nblk=0, max_R=0, device="cuda", stream=None):
+        self.dims = nat.make_dims(E, k, L, list(mask), block)
+        self.E, self.k, self.L, self.m, self.B = E, k, L, len(mask), block
+        self.D, self.tau, self.live, self.G = D, float(tau), bool(live), G
+        dev = torch.device(device)
+        self.device = dev
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        f32, i32 = torch.float32, torch.int32
+        self.centroids = torch.as_tensor(np.asarray(centroids), dtype=f32).to(dev).contiguous()
+        self.idf = torch.as_tensor(np.asarray(idf), dtype=f32).to(dev).contiguous()
+        self.loads = torch.as_tensor(np.asarray(loads), dtype=i32).to(dev).contiguous()
+        self.group_of = torch.as_tensor(np.asarray(group_of), dtype=i32).to(dev).contiguous()
+        self.affinity = torch.zeros((L, E, E), dtype=i32, device=dev)
+        self.W = torch.empty((L, E), dtype=torch.int64, device=dev)
+        self.Wg = torch.empty((L, G), dtype=torch.int64, device=dev)
+        self.rho_g = torch.empty(L, dtype=torch.float64, device=dev)
+        self.rho_e = torch.empty(L, dtype=torch.float64, device=dev)
+        self.cache = (torch.zeros((nslots, self.m, E), dtype=torch.uint8, device=dev)
+                      if nslots > 0 else None)
+        self.nslots = nslots
+        self._alloc(max_T, max_nblk, max_R)
+
+    def _alloc(self, T, nblk, R):
+        dev, E, k, L, m, D = self.device, self.E, self.k, self.L, self.m, self.D
+        self.cap = (T, nblk, R)
+        self.topk = torch.empty((L, max(T, 1), k), dtype=torch.uint8, device=dev)
+        self.blk_cnt = torch.empty((max(nblk, 1), m, E), dtype=torch.uint8, device=dev)
+        self.req_cnt = torch.empty((max(R, 1), m, E), dtype=torch.int32, device=dev)
+        self.sig = torch.empty((max(R, 1), m * E), dtype=torch.float32, device=dev)
+        self.dist = torch.empty((max(R, 1), D), dtype=torch.float32, device=dev)
+        self.choice = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
+        self.ws_bytes = nat.moer_workspace_bytes(self.dims, T, nblk, R, D)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def ensure(self, T, nblk, R):
+        if T > self.cap[0] or nblk > self.cap[1] or R > self.cap[2]:
+            self._alloc(max(T, self.cap[0]), max(nblk, self.cap[1]), max(R, self.cap[2]))
+
+    def reset_stats(self):
+        self.affinity.zero_()
+
+    # ------------------------------------------------------------ the step
+    def topk_signature(self, logits, bd: BatchDev, write_topk=True):
+        nat.moer_topk_signature(self.dims, logits, bd.T, bd.blk_tab, bd.nblk,
+                                self.topk if write_topk else None, self.blk_cnt, self.affinity,
+                                self.ws, self.ws_bytes, self.stream)
+
+    def block_stitch(self, bd: BatchDev):
+        use_cache = self.cache is not None and bd.req_cache_off is not None
+        nat.moer_block_stitch(self.dims, self.blk_cnt, bd.blk_tab, bd.nblk, bd.req_blk_off, bd.R,
+                              bd.cache_idx if use_cache else None,
+                              bd.req_cache_off if use_cache else None,
+                              self.cache if use_cache else None, self.nslots,
+                              bd.insert_slot if use_cache else None, self.req_cnt, self.ws,
+                              self.ws_bytes, self.stream)
+
+    def affinity_load(self):
+        nat.moer_affinity_load(self.dims, self.affinity, self.group_of, self.G, self.W, self.Wg,
+                               self.rho_g, self.rho_e, self.stream)
+
+    def route(self, R, write_sig=True):
+        nat.moer_route(self.dims, self.req_cnt, R, self.idf, self.centroids, self.D, self.tau,
+                       self.loads, int(self.live), self.sig if write_sig else None, self.dist,
+                       self.choice, self.ws, self.ws_bytes, self.stream)
+
+    def step(self, logits, bd: BatchDev, write_topk=True, write_sig=True):
+        """All rows of the path over one batch (loads and co-activation accumulate)."""
+        self.ensure(bd.T, bd.nblk, bd.R)
+        self.topk_signature(logits, bd, write_topk)
+        self.block_stitch(bd)
+        self.affinity_load()
+        self.route(bd.R, write_sig)
+
+    def status(self) -> int:
+        return nat.moer_ws_status(self.ws, self.stream)
+
+    @staticmethod
+    def for_workload(wl, *, max_T=0, max_nblk=0, max_R=0, device="cuda", stream=None):
+        return RoutingStats(wl.E, wl.k, wl.L, wl.mask, wl.B, D=wl.D, tau=wl.tau,
+                            centroids=wl.centroids, idf=wl.idf, loads=wl.loads0, live=wl.live,
+                            G=wl.G, group_of=wl.group_of, nslots=wl.nslots, max_T=max_T,
+                            max_nblk=max_nblk, max_R=max_R, device=device, stream=stream)

@@ -1,0 +1,92 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry point and
+rejects bad arguments on the host with the documented status codes (nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            src = open(os.path.join(inc, fn)).read()
+            names += re.findall(r"MOER_API\s+[\w\s\*]+?\b(moer_\w+)\s*\(", src)
+    return names
+
+
+@pytest.fixture(scope="module")
+def nat():
+    from moe_expert_routing_top_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from moe_expert_routing_top_gb300 import _native
+    return _native
+
+
+def test_exports_every_declared_symbol(nat):
+    names = _declared()
+    assert len(names) >= 9
+    lib = ctypes.CDLL(nat.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(nat.EXPORTS)
+
+
+def test_version_and_status_strings(nat):
+    assert nat.moer_version() >= 100
+    for code in range(8):
+        assert nat.moer_status_str(code)
+
+
+def _code(fn, *args):
+    from moe_expert_routing_top_gb300._native import MoerError
+    with pytest.raises(MoerError) as ei:
+        fn(*args)
+    return ei.value.code
+
+
+BADPTR = 0x1001  # misaligned, never dereferenced: validation rejects it first
+
+
+@pytest.mark.parametrize("E,k,L,mask,B,code", [
+    (3, 1, 2, [0], 16, 3), (260, 8, 2, [0], 16, 3), (64, 0, 2, [0], 16, 3), (64, 33, 2, [0], 16, 3),
+    (8, 9, 2, [0], 16, 3), (64, 8, 0, [], 16, 3), (64, 8, 2, [1, 0], 16, 1), (64, 8, 2, [2], 16, 3),
+    (64, 8, 2, [0], 0, 3), (64, 8, 2, [0], 256, 3)])
+def test_bad_dims(nat, E, k, L, mask, B, code):
+    d = nat.make_dims(E, k, L, mask, B)
+    assert _code(nat.moer_topk_signature, d, 64, 10, None, 0, None, None, None, 64, 4096, 0) == code
+
+
+def test_bad_pointers_and_sizes(nat):
+    d = nat.make_dims(128, 8, 4, [0, 2], 16)
+    ws = nat.moer_workspace_bytes(d, 1000, 70, 0, 0)
+    assert ws >= 256
+    f = nat.moer_topk_signature
+    assert _code(f, d, BADPTR, 1000, 64, 70, None, 64, None, 64, ws, 0) == 1      # misaligned logits
+    assert _code(f, d, 64, 1000, None, 70, None, 64, None, 64, ws, 0) == 1        # no block table
+    assert _code(f, d, 64, 1000, 64, 0, None, 64, None, 64, ws, 0) == 2           # no blocks
+    assert _code(f, d, 64, 1000, 64, 70, None, 64, None, 64, ws - 4, 0) == 5      # workspace
+    assert _code(f, d, 64, -1, 64, 70, None, 64, None, 64, ws, 0) == 3
+    r = nat.moer_route
+    assert _code(r, d, 64, 10, 64, 64, 0, 0.1, 64, 0, None, None, 64, None, 0, 0) == 3   # D = 0
+    assert _code(r, d, 64, 10, 64, 64, 65, 0.1, 64, 0, None, None, 64, None, 0, 0) == 3  # D > 64
+    assert _code(r, d, 64, 10, 64, 64, 16, -1.0, 64, 0, None, None, 64, None, 0, 0) == 3
+    assert _code(r, d, 64, 10, 64, 64, 16, 0.1, 64, 2, None, None, 64, None, 0, 0) == 1
+    assert _code(r, d, 64, 10, 64, 64, 16, 0.1, 64, 1, None, None, 64, None, 0, 0) == 1  # live, no ws
+    s = nat.moer_block_stitch
+    assert _code(s, d, 64, 64, 10, None, 5, None, None, None, 0, None, 64, None, 0, 0) == 1
+    assert _code(s, d, 64, 64, 10, 64, 5, 64, None, None, 0, None, 64, None, 0, 0) == 1  # idx w/o cache
+    nat.moer_topk_signature(d, 64, 0, None, 0, None, None, None, 64, ws, 0)  # T = 0: no-op
+
+
+def test_workspace_size_covers_calls(nat):
+    d = nat.make_dims(128, 8, 48, list(range(12)), 16)
+    t = nat.moer_workspace_bytes(d, 1305533, 82065, 0, 0)
+    r = nat.moer_workspace_bytes(d, 0, 0, 14000, 16)
+    both = nat.moer_workspace_bytes(d, 1305533, 82065, 14000, 16)
+    assert both == max(t, r) and t >= 256 + 4 * (1305533 // 64)

@@ -1,0 +1,157 @@
+"""Edge cases of the fused top-k / block-count / co-activation call against the oracle.
+
+Shapes off the fast path (E from 4 to 256, k from 1 to 32), tie-heavy and
+special-valued logits (NaN, +-inf, -0.0/+0.0), length-1 requests, partial
+blocks, B = 1 and B = 255, an empty layer mask, a single token, and
+malformed block tables (reported through the workspace status, never a
+fault).
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_routing_top_gb300 import _native as nat
+    return torch, nat
+
+
+def _blocks(lengths, B):
+    req_off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    tab = []
+    for r in range(len(lengths)):
+        for t0 in range(req_off[r], req_off[r + 1], B):
+            tab.append((t0, min(B, req_off[r + 1] - t0)))
+    return req_off, np.array(tab, dtype=np.int32).reshape(-1, 2)
+
+
+def _logits(rs, kind, L, T, E):
+    if kind == "normal":
+        x = rs.standard_normal((L, T, E)).astype(np.float32)
+    elif kind == "ties":
+        x = rs.randint(-2, 3, size=(L, T, E)).astype(np.float32)
+    elif kind == "equal":
+        x = np.full((L, T, E), 0.5, dtype=np.float32)
+    else:  # specials mixed into small integers
+        x = rs.randint(-3, 4, size=(L, T, E)).astype(np.float32)
+        sp = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, 1e-45, -1e-45], dtype=np.float32)
+        hit = rs.random_sample(x.shape) < 0.2
+        x[hit] = sp[rs.randint(0, len(sp), size=int(hit.sum()))]
+    return x
+
+
+def _run(env, x, k, lengths, B, mask, want_aff=True):
+    torch, nat = env
+    L, T, E = x.shape
+    req_off, tab = _blocks(lengths, B)
+    dims = nat.make_dims(E, k, L, mask, B)
+    m = len(mask)
+    dx = torch.from_numpy(x).cuda()
+    dtab = torch.from_numpy(tab.reshape(-1)).cuda()
+    topk = torch.full((L, T, k), 255, dtype=torch.uint8, device="cuda")
+    cnt = torch.full((max(len(tab), 1), max(m, 1), E), 77, dtype=torch.uint8, device="cuda")
+    aff = torch.zeros((L, E, E), dtype=torch.int32, device="cuda") if want_aff else None
+    wsb = nat.moer_workspace_bytes(dims, T, len(tab), 0, 0)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    nat.moer_topk_signature(dims, dx, T, dtab, len(tab), topk, cnt if m else None, aff, ws, wsb)
+    assert nat.moer_ws_status(ws) == 0
+    orc = oracle.get()
+    tk = orc.topk(x, k)
+    assert np.array_equal(topk.cpu().numpy(), tk)
+    if m:
+        bc = orc.block_counts(tk, E, req_off, B, mask)
+        assert np.array_equal(cnt.cpu().numpy()[:len(tab)], bc)
+    if want_aff:
+        assert np.array_equal(aff.cpu().numpy().astype(np.int64), orc.affinity(tk, E))
+
+
+SHAPES = [  # (E, k, L)
+    (4, 1, 2), (8, 8, 2), (12, 5, 3), (32, 32, 2), (64, 8, 3), (64, 6, 3), (64, 1, 2),
+    (64, 32, 2), (100, 7, 2), (128, 8, 3), (128, 2, 2), (128, 32, 2), (200, 9, 2), (256, 8, 2),
+    (256, 32, 2),
+]
+
+
+@pytest.mark.parametrize("E,k,L", SHAPES, ids=[f"E{e}k{k}" for e, k, _ in SHAPES])
+@pytest.mark.parametrize("kind", ["normal", "ties", "specials"])
+def test_shapes_and_values(env, E, k, L, kind):
+    rs = np.random.RandomState(E * 131 + k * 7 + L)
+    lengths = [1, 17, 16, 3, 40, 1, 129, 64, 2]
+    T = sum(lengths)
+    x = _logits(rs, kind, L, T, E)
+    mask = list(range(0, L, 2))
+    _run(env, x, k, lengths, 16, mask)
+
+
+@pytest.mark.parametrize("E,k", [(128, 8), (64, 6), (64, 8)])
+def test_all_equal_logits(env, E, k):
+    rs = np.random.RandomState(3)
+    x = _logits(rs, "equal", 2, 300, E)
+    _run(env, x, k, [100, 200], 16, [1])
+
+
+@pytest.mark.parametrize("B", [1, 5, 64, 255])
+def test_block_sizes(env, B):
+    rs = np.random.RandomState(B)
+    lengths = [1, 300, 255, 256, 7, 512]
+    x = _logits(rs, "normal", 2, sum(lengths), 128)
+    _run(env, x, 8, lengths, B, [0, 1])
+
+
+def test_single_token_and_empty_mask(env):
+    rs = np.random.RandomState(9)
+    _run(env, _logits(rs, "normal", 3, 1, 128), 8, [1], 16, [2])
+    _run(env, _logits(rs, "normal", 3, 50, 64), 6, [50], 16, [])
+    _run(env, _logits(rs, "normal", 3, 50, 64), 6, [20, 30], 16, [0, 1, 2], want_aff=False)
+
+
+def test_many_tiles_ragged_tail(env):
+    rs = np.random.RandomState(21)
+    lengths = list(rs.randint(1, 200, size=60))
+    x = _logits(rs, "normal", 5, sum(lengths), 128)
+    _run(env, x, 8, lengths, 16, [0, 3, 4])
+
+
+def test_malformed_block_table_is_reported(env):
+    torch, nat = env
+    E, k, L, T = 128, 8, 2, 64
+    dims = nat.make_dims(E, k, L, [0], 16)
+    x = torch.randn((L, T, E), device="cuda")
+    bad = torch.tensor([0, 16, 16, 16, 40, 16, 48, 16], dtype=torch.int32, device="cuda")  # gap at 32
+    cnt = torch.full((4, 1, E), 7, dtype=torch.uint8, device="cuda")
+    topk = torch.full((L, T, k), 255, dtype=torch.uint8, device="cuda")
+    wsb = nat.moer_workspace_bytes(dims, T, 4, 0, 0)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    nat.moer_topk_signature(dims, x, T, bad, 4, topk, cnt, None, ws, wsb)
+    assert nat.moer_ws_status(ws) == 6  # MOER_EDATA
+    assert (topk == 255).all() and (cnt == 7).all()
+    # the status word is cleared by the read; a good call afterwards succeeds
+    good = torch.tensor([0, 16, 16, 16, 32, 16, 48, 16], dtype=torch.int32, device="cuda")
+    nat.moer_topk_signature(dims, x, T, good, 4, topk, cnt, None, ws, wsb)
+    assert nat.moer_ws_status(ws) == 0
+    assert (topk != 255).all()
+
+
+def test_stitch_bad_slot_is_reported(env):
+    torch, nat = env
+    E, m = 64, 1
+    dims = nat.make_dims(E, 8, 1, [0], 16)
+    blk = torch.ones((2, m, E), dtype=torch.uint8, device="cuda")
+    tab = torch.tensor([0, 16, 16, 16], dtype=torch.int32, device="cuda")
+    rbo = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
+    cache = torch.zeros((3, m, E), dtype=torch.uint8, device="cuda")
+    cidx = torch.tensor([5], dtype=torch.int32, device="cuda")      # out of range
+    rco = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    ins = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    out = torch.empty((1, m, E), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    nat.moer_block_stitch(dims, blk, tab, 2, rbo, 1, cidx, rco, cache, 3, ins, out, ws, 256)
+    assert nat.moer_ws_status(ws) == 6
+    assert (out == 2).all()
