@@ -50,6 +50,7 @@ struct K1Geo {
   static constexpr int STAGES = (EPL == 4) ? 3 : 4;
   static constexpr bool SMEM_AFF = EPL <= 4;
   static constexpr int CWARPS = 16;
+  static constexpr int NR = 4;  // rows a consumer warp works on at once
   static constexpr int CTHREADS = CWARPS * 32;
   static constexpr int THREADS = CTHREADS + 32;
   static constexpr size_t STAGE_BYTES = (size_t)TT * EMAX * 4;
@@ -60,7 +61,7 @@ struct K1Geo {
   static constexpr size_t OFF_AFF = align_up(OFF_MAP + (size_t)STAGES * TT, 16);
   static constexpr size_t AFF_WORDS = SMEM_AFF ? (size_t)EMAX * (EMAX + 1) : 0;
   static constexpr size_t OFF_WSCR = align_up(OFF_AFF + AFF_WORDS * 4, 16);
-  static constexpr size_t OFF_META = OFF_WSCR + (size_t)CWARPS * 16 * 4;
+  static constexpr size_t OFF_META = OFF_WSCR + (size_t)CWARPS * NR * 16 * 4;
   static constexpr size_t OFF_BAR = align_up(OFF_META + (size_t)STAGES * 8 * 4, 16);
   static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8;
 };
@@ -163,63 +164,74 @@ __device__ int topk_exact(const float* row, int E, int k, int lane) {
   return myidx;
 }
 
-// Fast top-K of a row with E == 32*EPL (EPL 2 or 4), K <= 8.  Returns false
-// when the truncated keys cannot certify the exact result.
-template <int EPL, int K>
-__device__ __forceinline__ bool topk_fast(const float* row, int lane, int* wscr, int& myidx) {
+// Fast top-K of NR rows at once (E == 32*EPL, EPL 2 or 4, K <= 8).  The NR
+// rows are independent, so their redux chains interleave and hide each
+// other's latency.  Keys: upper 24 bits of the float's bit pattern (as a
+// signed int: exact order among positive floats), lower 8 bits 255 - e, so
+// keys are unique and carry the expert id.  Row q's result is certified when
+// its k+1 leading keys are positive, finite and pairwise distinct in their
+// upper 24 bits; otherwise bit q of the returned mask is set and the caller
+// redoes that row exactly.  Every lane writes the same winners to scr, so
+// each lane reads back values it wrote itself (no warp barrier needed).
+template <int EPL, int K, int NR>
+__device__ __forceinline__ unsigned topk_fast_rows(const float* const (&rowp)[NR], int lane, int* scr,
+                                                   int (&myidx)[NR]) {
   static_assert(EPL == 2 || EPL == 4, "fast path needs 2 or 4 experts per lane");
   static_assert(K >= 1 && K <= 8, "fast path needs k <= 8");
-  int key[EPL];
-  if constexpr (EPL == 4) {
-    const float4 v = reinterpret_cast<const float4*>(row)[lane];
-    key[0] = __float_as_int(v.x);
-    key[1] = __float_as_int(v.y);
-    key[2] = __float_as_int(v.z);
-    key[3] = __float_as_int(v.w);
-  } else {
-    const float2 v = reinterpret_cast<const float2*>(row)[lane];
-    key[0] = __float_as_int(v.x);
-    key[1] = __float_as_int(v.y);
-  }
+  int h[NR], s1[NR], s2[NR];
 #pragma unroll
-  for (int j = 0; j < EPL; ++j) key[j] = (key[j] & (int)0xFFFFFF00) | (255 - (lane * EPL + j));
-  int s0, s1, s2;
-  if constexpr (EPL == 4) {
-    const int a = max(key[0], key[1]), b = min(key[0], key[1]);
-    const int c = max(key[2], key[3]), d = min(key[2], key[3]);
-    s0 = max(a, c);
-    const int x = min(a, c), y = max(b, d);
-    s1 = max(x, y);
-    s2 = max(min(x, y), min(b, d));
-  } else {
-    s0 = max(key[0], key[1]);
-    s1 = min(key[0], key[1]);
-    s2 = INT_MIN;
+  for (int q = 0; q < NR; ++q) {
+    int key[EPL];
+    if constexpr (EPL == 4) {
+      const float4 v = reinterpret_cast<const float4*>(rowp[q])[lane];
+      key[0] = __float_as_int(v.x);
+      key[1] = __float_as_int(v.y);
+      key[2] = __float_as_int(v.z);
+      key[3] = __float_as_int(v.w);
+    } else {
+      const float2 v = reinterpret_cast<const float2*>(rowp[q])[lane];
+      key[0] = __float_as_int(v.x);
+      key[1] = __float_as_int(v.y);
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) key[j] = (key[j] & (int)0xFFFFFF00) | (255 - (lane * EPL + j));
+    if constexpr (EPL == 4) {
+      const int a = max(key[0], key[1]), b = min(key[0], key[1]);
+      const int c = max(key[2], key[3]), d = min(key[2], key[3]);
+      h[q] = max(a, c);
+      const int x = min(a, c), y = max(b, d);
+      s1[q] = max(x, y);
+      s2[q] = max(min(x, y), min(b, d));
+    } else {
+      h[q] = max(key[0], key[1]);
+      s1[q] = min(key[0], key[1]);
+      s2[q] = INT_MIN;
+    }
   }
-  int h = s0;
-  int Ms[K + 1];
 #pragma unroll
   for (int r = 0; r < K; ++r) {
-    const int M = __reduce_max_sync(FULL, h);
-    const bool p = (h == M);
-    h = p ? s1 : h;
-    s1 = p ? INT_MIN : s1;
-    Ms[r] = M;
-  }
-  Ms[K] = __reduce_max_sync(FULL, max(h, s2));
-  if (lane == 0) {
 #pragma unroll
-    for (int r = 0; r <= K; ++r) wscr[r] = Ms[r];
+    for (int q = 0; q < NR; ++q) {
+      const int M = __reduce_max_sync(FULL, h[q]);
+      const bool p = (h[q] == M);
+      h[q] = p ? s1[q] : h[q];
+      s1[q] = p ? INT_MIN : s1[q];
+      scr[q * 16 + r] = M;
+    }
   }
-  __syncwarp();
-  const int Mr = wscr[min(lane, K)];
-  const int Mn = wscr[min(lane + 1, K)];
-  __syncwarp();
-  bool bad = (lane < K) && ((Mn >= (Mr & (int)0xFFFFFF00)) || (Mr < 256));
-  bad = bad || (lane == 0 && Mr >= 0x7F800000);
-  if (__any_sync(FULL, bad)) return false;
-  myidx = (lane < K) ? (255 - (Mr & 0xFF)) : -1;
-  return true;
+#pragma unroll
+  for (int q = 0; q < NR; ++q) scr[q * 16 + K] = __reduce_max_sync(FULL, max(h[q], s2[q]));
+  unsigned badmask = 0u;
+#pragma unroll
+  for (int q = 0; q < NR; ++q) {
+    const int Mr = scr[q * 16 + min(lane, K)];
+    const int Mn = scr[q * 16 + min(lane + 1, K)];
+    bool bad = (lane < K) && ((Mn >= (Mr & (int)0xFFFFFF00)) || (Mr < 256));
+    bad = bad || (lane == 0 && Mr >= 0x7F800000);
+    if (__any_sync(FULL, bad)) badmask |= 1u << q;
+    myidx[q] = (lane < K) ? (255 - (Mr & 0xFF)) : -1;
+  }
+  return badmask;
 }
 
 // ------------------------------------------------------- co-activation adds
@@ -382,12 +394,13 @@ __device__ void k1_flush_aff(const K1Params& p, int* aff, int layer, int ctid) {
 template <int EPL, int FASTK>
 __device__ void k1_consumer(const K1Params& p, char* smem, int64_t i0, int64_t i1) {
   using G = K1Geo<EPL>;
+  constexpr int NR = G::NR;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* rows = reinterpret_cast<const float*>(smem + G::OFF_ROWS);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + G::OFF_CNT);
   const uint8_t* map = reinterpret_cast<const uint8_t*>(smem + G::OFF_MAP);
   int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
-  int* wscr = reinterpret_cast<int*>(smem + G::OFF_WSCR) + warp * 16;
+  int* wscr = reinterpret_cast<int*>(smem + G::OFF_WSCR) + warp * 16 * G::NR;
   const int* meta = reinterpret_cast<const int*>(smem + G::OFF_META);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   uint64_t* empty = full + G::STAGES;
@@ -419,27 +432,36 @@ __device__ void k1_consumer(const K1Params& p, char* smem, int64_t i0, int64_t i
     const int64_t tok0 = (int64_t)tile * G::TT;
     const float* stage = rows + (size_t)s * G::TT * G::EMAX;
     uint32_t* scnt = cnt + (size_t)s * G::CNT_WORDS;
-    for (int r = warp; r < ntok; r += G::CWARPS) {
-      const float* row = stage + (size_t)r * p.E;
-      int myidx = -1;
-      bool done = false;
-      if constexpr (FASTK > 0) done = topk_fast<EPL, FASTK>(row, lane, wscr, myidx);
-      if (!done) myidx = topk_exact<EPL>(row, p.E, p.k, lane);
-      if (p.topk != nullptr && lane < kk)
-        p.topk[((size_t)l * p.T + tok0 + r) * kk + lane] = (uint8_t)myidx;
-      if (aff_on) {
-        if constexpr (G::SMEM_AFF) {
-          if constexpr (FASTK > 0)
-            aff_pairs_fixed<FASTK>(aff, stride, myidx, lane);
-          else
-            aff_pairs_any(aff, stride, myidx, kk, lane);
-        } else {
-          aff_pairs_any(p.affinity + (size_t)l * p.E * p.E, p.E, myidx, kk, lane);
+    for (int r0 = warp * NR; r0 < ntok; r0 += G::CWARPS * NR) {
+      const float* rowp[NR];
+      int myidx[NR];
+#pragma unroll
+      for (int q = 0; q < NR; ++q) rowp[q] = stage + (size_t)min(r0 + q, ntok - 1) * p.E;
+      unsigned redo = (1u << NR) - 1u;
+      if constexpr (FASTK > 0) redo = topk_fast_rows<EPL, FASTK, NR>(rowp, lane, wscr, myidx);
+#pragma unroll
+      for (int q = 0; q < NR; ++q)
+        if ((redo >> q) & 1u) myidx[q] = topk_exact<EPL>(rowp[q], p.E, p.k, lane);
+#pragma unroll
+      for (int q = 0; q < NR; ++q) {
+        const int r = r0 + q;
+        if (r >= ntok) break;
+        if (p.topk != nullptr && lane < kk)
+          p.topk[((size_t)l * p.T + tok0 + r) * kk + lane] = (uint8_t)myidx[q];
+        if (aff_on) {
+          if constexpr (G::SMEM_AFF) {
+            if constexpr (FASTK > 0)
+              aff_pairs_fixed<FASTK>(aff, stride, myidx[q], lane);
+            else
+              aff_pairs_any(aff, stride, myidx[q], kk, lane);
+          } else {
+            aff_pairs_any(p.affinity + (size_t)l * p.E * p.E, p.E, myidx[q], kk, lane);
+          }
         }
-      }
-      if (slot >= 0 && lane < kk) {
-        const int lb = map[s * G::TT + r];
-        atomicAdd(&scnt[lb * wpb + (myidx >> 2)], 1u << ((myidx & 3) * 8));
+        if (slot >= 0 && lane < kk) {
+          const int lb = map[s * G::TT + r];
+          atomicAdd(&scnt[lb * wpb + (myidx[q] >> 2)], 1u << ((myidx[q] & 3) * 8));
+        }
       }
     }
     __syncwarp();

@@ -79,7 +79,7 @@ class RoutingStats:
     def _alloc(self, T, nblk, R):
         dev, E, k, L, m, D = self.device, self.E, self.k, self.L, self.m, self.D
         self.cap = (T, nblk, R)
-        self.topk = torch.empty((L, max(T, 1), k), dtype=torch.uint8, device=dev)
+        self.topk = torch.empty(L * max(T, 1) * k, dtype=torch.uint8, device=dev)
         self.blk_cnt = torch.empty((max(nblk, 1), m, E), dtype=torch.uint8, device=dev)
         self.req_cnt = torch.empty((max(R, 1), m, E), dtype=torch.int32, device=dev)
         self.sig = torch.empty((max(R, 1), m * E), dtype=torch.float32, device=dev)
@@ -91,6 +91,10 @@ class RoutingStats:
     def ensure(self, T, nblk, R):
         if T > self.cap[0] or nblk > self.cap[1] or R > self.cap[2]:
             self._alloc(max(T, self.cap[0]), max(nblk, self.cap[1]), max(R, self.cap[2]))
+
+    def topk_for(self, T: int) -> torch.Tensor:
+        """The top-k ids of the last batch of T tokens, as [L][T][k]."""
+        return self.topk[:self.L * T * self.k].view(self.L, T, self.k)
 
     def reset_stats(self):
         self.affinity.zero_()

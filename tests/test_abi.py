@@ -21,7 +21,11 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def nat():
-    from moe_expert_routing_top_gb300 import build
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "moer_libbuild", os.path.join(ROOT, "moe_expert_routing_top_gb300", "build.py"))
+    build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build)
     if not os.path.exists(build.LIB):
         build.build()
     from moe_expert_routing_top_gb300 import _native

@@ -58,7 +58,7 @@ def test_path_parity(env, cfg, R, nchunks):
         assert rs.status() == 0
         lh = gen.host_logits(wl, b.tok_key, b.tok_dom)
         tk = orc.topk(lh, wl.k)
-        assert np.array_equal(gu.host(rs.topk[:, :b.T]), tk), "top-k ids"
+        assert np.array_equal(gu.host(rs.topk_for(b.T)), tk), "top-k ids"
         topk_all.append(tk)
         bc = orc.block_counts(tk, wl.E, b.req_off, wl.B, wl.mask)
         assert np.array_equal(gu.host(rs.blk_cnt[:b.nblk]), bc), "block counts"
