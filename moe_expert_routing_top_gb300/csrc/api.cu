@@ -6,7 +6,7 @@
 #include "common.cuh"
 
 namespace moer {
-int k1_tile_tokens(int E);
+size_t k1_scratch_bytes(int64_t T);
 moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64_t T,
                                   const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
                                   uint8_t* blk_cnt, int32_t* affinity, void* ws, cudaStream_t st);
@@ -57,10 +57,7 @@ extern "C" {
 size_t moer_workspace_bytes(const moer_dims* d, int64_t T, int32_t nblk, int32_t R, int32_t D) {
   (void)nblk;
   size_t scratch = 0;
-  if (d != nullptr && d->E >= 4 && d->E <= 256 && T > 0) {
-    const int TT = k1_tile_tokens(d->E);
-    scratch = round256((size_t)((T + TT - 1) / TT) * sizeof(int32_t));
-  }
+  if (d != nullptr && T > 0) scratch = k1_scratch_bytes(T);
   if (R > 0 && D > 0) {
     const size_t route = round256((size_t)R * (size_t)D * sizeof(float));
     scratch = route > scratch ? route : scratch;
@@ -79,6 +76,7 @@ moer_status moer_topk_signature(const moer_dims* d, const float* logits, int64_t
   if (T == 0) return MOER_OK;
   if (logits == nullptr || !aligned(logits, 16)) return MOER_EINVAL;
   if (affinity != nullptr && !aligned(affinity, 4)) return MOER_EINVAL;
+  if (topk != nullptr && !aligned(topk, 8)) return MOER_EINVAL;
   const bool hist = blk_cnt != nullptr && d->m > 0;
   if (hist) {
     if (blk_tab == nullptr || !aligned(blk_tab, 4) || !aligned(blk_cnt, 4)) return MOER_EINVAL;

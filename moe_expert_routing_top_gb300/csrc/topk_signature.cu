@@ -38,6 +38,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "k1_params.cuh"
 
 namespace moer {
 
@@ -89,12 +90,23 @@ int k1_tile_tokens(int E) {
   return K1Geo<8>::TT;
 }
 
+// Workspace after the header: a per-tile table sized for the smallest tile
+// (32 tokens), then one block id per token.
+size_t k1_scratch_bytes(int64_t T) {
+  const size_t tiles = (size_t)((T + 31) / 32) * sizeof(int32_t);
+  return (tiles + 255) / 256 * 256 + ((size_t)T * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+
+
 // ---------------------------------------------------------------- pre-pass
-// Validates the block table, records each tile's first block and zeroes the
-// count rows of blocks that straddle a tile boundary.
+// Validates the block table, records each tile's first block (warp-per-row
+// kernel) or each token's block (thread-per-row kernel), and zeroes the count
+// rows of blocks that straddle a tile boundary.
 __global__ void k1_tile_index(const int32_t* __restrict__ blk_tab, int nblk, int64_t T, int B,
-                              int TT, int32_t* __restrict__ tile_blk0, uint32_t* status,
-                              uint32_t* call_flag, uint8_t* __restrict__ blk_cnt, int m, int E) {
+                              int TT, int32_t* __restrict__ tile_blk0, int32_t* __restrict__ tok_blk,
+                              uint32_t* status, uint32_t* call_flag, uint8_t* __restrict__ blk_cnt,
+                              int m, int E) {
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += gridDim.x * blockDim.x) {
     const int t0 = blk_tab[2 * b], ln = blk_tab[2 * b + 1];
     bool ok = ln >= 1 && ln <= B && t0 >= 0 && (int64_t)t0 + ln <= T;
@@ -110,8 +122,10 @@ __global__ void k1_tile_index(const int32_t* __restrict__ blk_tab, int nblk, int
       atomicOr(call_flag, 1u);
       continue;
     }
-    for (int64_t j = ((int64_t)t0 + TT - 1) / TT; j * TT < (int64_t)t0 + ln; ++j)
-      tile_blk0[j] = b;
+    if (tile_blk0 != nullptr)
+      for (int64_t j = ((int64_t)t0 + TT - 1) / TT; j * TT < (int64_t)t0 + ln; ++j) tile_blk0[j] = b;
+    if (tok_blk != nullptr)
+      for (int t = t0; t < t0 + ln; ++t) tok_blk[t] = b;
     if (blk_cnt != nullptr && m > 0 && (t0 / TT) != ((t0 + ln - 1) / TT)) {
       uint32_t* row = reinterpret_cast<uint32_t*>(blk_cnt + (size_t)b * m * E);
       for (int w = 0; w < m * E / 4; ++w) row[w] = 0u;
@@ -523,19 +537,45 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
                                   uint8_t* blk_cnt, int32_t* affinity, void* ws,
                                   cudaStream_t st) {
   const int E = d->E, k = d->k;
-  const int TT = k1_tile_tokens(E);
+  const bool tpr = tpr_supported(E, k);
+  const int TT = tpr ? 32 : k1_tile_tokens(E);
   const int ntiles = (int)((T + TT - 1) / TT);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* call_flag = status + 1;
   int32_t* tile_blk0 = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + WS_HEADER);
+  int32_t* tok_blk = reinterpret_cast<int32_t*>(
+      static_cast<char*>(ws) + WS_HEADER + ((size_t)((T + 31) / 32) * sizeof(int32_t) + 255) / 256 * 256);
   if (cudaMemsetAsync(call_flag, 0, sizeof(uint32_t), st) != cudaSuccess) return MOER_ECUDA;
   const bool hist = blk_cnt != nullptr && d->m > 0;
   if (hist) {
     const int blocks = (int)min64((nblk + 255) / 256, 4096);
     k1_tile_index<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(blk_tab, nblk, T, d->block, TT,
-                                                            tile_blk0, status, call_flag, blk_cnt,
-                                                            d->m, E);
+                                                            tpr ? nullptr : tile_blk0,
+                                                            tpr ? tok_blk : nullptr, status, call_flag,
+                                                            blk_cnt, d->m, E);
     if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
+  }
+  int sms = device_sm_count();
+  if (sms <= 0) return MOER_ECUDA;
+  if (tpr) {
+    TprParams q;
+    q.logits = logits;
+    q.T = T;
+    q.k = k;
+    q.L = d->L;
+    q.m = d->m;
+    q.topk = topk;
+    q.blk_cnt = hist ? blk_cnt : nullptr;
+    q.affinity = affinity;
+    q.tok_blk = tok_blk;
+    q.ntiles = ntiles;
+    q.nitems = (int64_t)d->L * ntiles;
+    q.status = status;
+    q.call_flag = call_flag;
+    for (int l = 0; l < 256; ++l) q.slot_of_layer[l] = -1;
+    for (int i = 0; i < d->m; ++i) q.slot_of_layer[d->mask[i]] = (int16_t)i;
+    const int grid = (int)min64(q.nitems, sms);
+    return tpr_run(E, k, q, grid, st) == cudaSuccess ? MOER_OK : MOER_ECUDA;
   }
   K1Params p;
   p.logits = logits;
@@ -557,17 +597,9 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
   p.call_flag = call_flag;
   for (int l = 0; l < 256; ++l) p.slot_of_layer[l] = -1;
   for (int i = 0; i < d->m; ++i) p.slot_of_layer[d->mask[i]] = (int16_t)i;
-  int sms = device_sm_count();
-  if (sms <= 0) return MOER_ECUDA;
   const int grid = (int)min64(p.nitems, sms);
   cudaError_t e;
-  if (E == 64 && k == 8)
-    e = k1_launch<2, 8>(p, grid, st);
-  else if (E == 64 && k == 6)
-    e = k1_launch<2, 6>(p, grid, st);
-  else if (E == 128 && k == 8)
-    e = k1_launch<4, 8>(p, grid, st);
-  else if (E <= 32)
+  if (E <= 32)
     e = k1_launch<1, 0>(p, grid, st);
   else if (E <= 64)
     e = k1_launch<2, 0>(p, grid, st);
