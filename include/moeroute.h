@@ -85,17 +85,23 @@ MOER_API size_t moer_workspace_bytes(const moer_dims* d, int64_t T, int32_t nblk
  * T         computed tokens in this call (0 is a no-op).
  * blk_tab   [nblk][2] int32 (tok0, len): the KV blocks of the computed
  *           tokens in order; they must tile [0, T) contiguously and have
- *           1 <= len <= B.  May be NULL when blk_cnt is NULL.
- * topk      [L][T][k] uint8 or NULL: expert ids in rank order.  Ranking:
- *           larger logit first; equal logits (-0.0 == +0.0) rank the lower
- *           expert id first; NaN ranks below every number.
+ *           1 <= len <= B.  A block that breaks this (wrong length, gap or
+ *           overlap with its predecessor, past T) is skipped -- its blk_cnt
+ *           rows are left untouched -- and MOER_EDATA is recorded in ws; the
+ *           top-k ids and co-activation counts are still produced.  May be
+ *           NULL when blk_cnt is NULL.
+ * topk      [L][T][k] uint8 or NULL, 8-byte aligned: expert ids in rank
+ *           order.  Ranking: larger logit first; equal logits (-0.0 == +0.0)
+ *           rank the lower expert id first; NaN ranks below every number.
  * blk_cnt   [nblk][m][E] uint8 or NULL: blk_cnt[b][i][e] = number of tokens
  *           of block b whose top-k at layer mask[i] contains e (<= B).
  * affinity  [L][E][E] int32 or NULL: ACCUMULATED (+=) co-activation counts,
  *           affinity[l][a][b] += #tokens whose top-k at layer l holds a and b
  *           (diagonal = expert load).  The caller zeroes it; streamed chunks
  *           sum.  4-byte aligned.
- * ws        device workspace of at least moer_workspace_bytes(d, T, nblk, 0, 0).
+ * ws        device workspace of at least moer_workspace_bytes(d, T, nblk, 0, 0)
+ *           bytes, 16-byte aligned (it holds the status word and, when topk
+ *           is NULL, the mask layers' top-k ids).
  */
 MOER_API moer_status moer_topk_signature(const moer_dims* d, const float* logits, int64_t T,
                                 const int32_t* blk_tab, int32_t nblk, uint8_t* topk,

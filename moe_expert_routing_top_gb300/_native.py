@@ -11,7 +11,7 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "libmoeroute.so")
+LIB_PATH = os.environ.get("MOER_LIBRARY", os.path.join(HERE, "_build", "libmoeroute.so"))
 
 STATUS = {0: "MOER_OK", 1: "MOER_EINVAL", 2: "MOER_ESHAPE", 3: "MOER_ERANGE", 4: "MOER_ECUDA",
           5: "MOER_ENOMEM", 6: "MOER_EDATA", 7: "MOER_ETIMEOUT"}

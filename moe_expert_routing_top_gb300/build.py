@@ -15,8 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoeroute.so")
-SOURCES = ["api.cu", "topk_signature.cu", "topk_signature_tpr.cu", "stitch.cu", "affinity_load.cu",
-           "route.cu"]
+SOURCES = ["api.cu", "topk_signature.cu", "topk_signature_tpr.cu", "block_counts.cu", "stitch.cu",
+           "affinity_load.cu", "route.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", os.path.join(os.path.dirname(HERE), "include")]

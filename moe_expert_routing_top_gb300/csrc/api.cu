@@ -6,7 +6,7 @@
 #include "common.cuh"
 
 namespace moer {
-size_t k1_scratch_bytes(int64_t T);
+size_t k1_scratch_bytes(const moer_dims* d, int64_t T);
 moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64_t T,
                                   const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
                                   uint8_t* blk_cnt, int32_t* affinity, void* ws, cudaStream_t st);
@@ -57,7 +57,7 @@ extern "C" {
 size_t moer_workspace_bytes(const moer_dims* d, int64_t T, int32_t nblk, int32_t R, int32_t D) {
   (void)nblk;
   size_t scratch = 0;
-  if (d != nullptr && T > 0) scratch = k1_scratch_bytes(T);
+  if (d != nullptr && T > 0 && d->m > 0 && d->m <= 256 && d->k > 0) scratch = k1_scratch_bytes(d, T);
   if (R > 0 && D > 0) {
     const size_t route = round256((size_t)R * (size_t)D * sizeof(float));
     scratch = route > scratch ? route : scratch;

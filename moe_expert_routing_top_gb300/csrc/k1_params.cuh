@@ -1,5 +1,5 @@
-// k1_params.cuh -- launch parameters shared by the host dispatch of
-// moer_topk_signature and the thread-per-row kernel.
+// k1_params.cuh -- launch parameters of the logits pass of
+// moer_topk_signature, shared by its host dispatch and both kernels.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -7,23 +7,21 @@
 
 namespace moer {
 
-// Thread-per-row kernel: one (layer, 32-token tile) work item per tile.
-struct TprParams {
-  const float* logits;
+struct K1Params {
+  const float* logits;  // [L][T][E]
   int64_t T;
-  int k, L, m;
-  uint8_t* topk;
-  uint8_t* blk_cnt;
-  int32_t* affinity;
-  const int32_t* tok_blk;
-  int ntiles;
-  int64_t nitems;
-  uint32_t* status;
-  uint32_t* call_flag;
-  int16_t slot_of_layer[256];
+  int E, k, L;
+  uint8_t* ids;          // top-k ids out, or NULL: the caller's [L][T][k], or
+  int ids_mask_only;     //   (when set) mask layers only, [m][T][k]
+  int32_t* affinity;     // [L][E][E] accumulated, or NULL
+  int ntiles;            // token tiles per layer
+  int64_t nitems;        // L * ntiles work items
+  uint32_t* status;      // sticky workspace status word
+  int16_t slot_of_layer[256];  // mask slot of each layer, -1 if not a mask layer
 };
 
 bool tpr_supported(int E, int k);
-cudaError_t tpr_run(int E, int k, const TprParams& p, int grid, cudaStream_t st);
+int tpr_tile_tokens(int E);  // tokens per work item of the thread-per-row kernel
+cudaError_t tpr_run(int E, int k, const K1Params& p, int grid, cudaStream_t st);
 
 }  // namespace moer

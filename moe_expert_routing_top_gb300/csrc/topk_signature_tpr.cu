@@ -1,5 +1,5 @@
-// topk_signature_tpr.cu -- thread-per-row variant of the fused top-k /
-// per-KV-block count / co-activation pass, for the model shapes the path is
+// topk_signature_tpr.cu -- thread-per-row logits pass of moer_topk_signature
+// (top-k ids and expert co-activation) for the model shapes the path is
 // built around (E = 64 or 128 experts, k = 6 or 8).
 //
 // What it computes is identical to the warp-per-row kernel (see
@@ -9,16 +9,19 @@
 // Figure 2(a) (per-layer expert co-activation).
 //
 // Design (GB300):
-//   * Persistent grid, one CTA per SM: one producer warp and four consumer
-//     warps.  Work items are (layer, 32-token tile); tile n of the CTA goes to
-//     ring stage n % STAGES (one cp.async.bulk copy of 32 contiguous logit
-//     rows, completing on an mbarrier) and to consumer warp n % 4.
-//   * Each consumer lane owns one token row.  It reads the row from shared
+//   * Persistent grid, one CTA per SM: one producer warp and eight consumer
+//     warps.  Work items are (layer, 16-token tile); tile n of the CTA goes to
+//     consumer warp n % 8 and to one of that warp's own ring stages (one
+//     cp.async.bulk copy of 16 contiguous logit rows, completing on an
+//     mbarrier).  Stages are never shared between consumer warps, so each
+//     warp meets its stages' barrier phases strictly in order.
+//   * Two consumer lanes share one token row; each reads its half from shared
 //     memory in 16-byte units whose order is XOR-rotated by (lane & 7), which
-//     makes every LDS.128 conflict-free, and folds the row 8 values at a
-//     time into a sorted top-8 held in registers: an optimal 19-comparator
-//     sorting network per chunk, then a bitonic split/merge with the running
-//     top-8 (the split's losers give the 9th-ranked key).  Keys are the
+//     makes every LDS.128 conflict-free, and folds it 8 values at a time into
+//     a sorted top-8 held in registers: an optimal 19-comparator sorting
+//     network per chunk, then a bitonic split/merge with the running top-8
+//     (the split's losers give the 9th-ranked key).  The two halves are then
+//     merged the same way across the lane pair with shuffles.  Keys are the
 //     float's upper 24 bits (signed-int order equals value order for positive
 //     floats) with the value's position in the lane's read order in the low
 //     8 bits, so keys are unique and min/max networks apply.
@@ -30,12 +33,8 @@
 //   * Co-activation: each lane adds its row's k*k ordered pairs to a
 //     shared-memory E x E int32 tile with shared atomics; the four consumer
 //     warps flush it to global memory (atomic adds) at each layer change.
-//   * KV-block counts: each consumer warp accumulates its tile's counts in a
-//     private packed-byte buffer (four experts per 32-bit word) indexed by
-//     the token's block relative to the tile's first block (from the
-//     per-token block ids the pre-pass writes), then writes the tile's blocks
-//     out itself: plain stores for blocks inside the tile, atomic adds for
-//     the two edge blocks that straddle tiles (zeroed by the pre-pass).
+//   * The top-k ids go out as 8 (or 6) bytes per row; the per-KV-block
+//     counts are computed from them by block_counts.cu.
 #include <climits>
 
 #include "common.cuh"
@@ -43,19 +42,36 @@
 
 namespace moer {
 
+// Geometry (compile-time tunables with the measured defaults).
+#ifndef MOER_TPR_LPR
+#define MOER_TPR_LPR 2
+#endif
+#ifndef MOER_TPR_CW
+#define MOER_TPR_CW 8
+#endif
+#ifndef MOER_TPR_STAGE_KB
+#define MOER_TPR_STAGE_KB 128
+#endif
+
 template <int E>
 struct TprGeo {
-  static constexpr int NU = E / 4;  // 16-byte units per row
-  static constexpr int TT = 32;     // rows per tile: one per consumer lane
-  static constexpr int CW = 4;      // consumer warps
-  static constexpr int STAGES = (E == 128) ? 8 : 16;
+  static constexpr int LPR = MOER_TPR_LPR;  // lanes per row: each folds E / LPR values
+  static constexpr int TT = 32 / LPR;       // rows per tile (one tile per consumer warp)
+  static constexpr int CW = MOER_TPR_CW;    // consumer warps
+  static constexpr int STAGES = MOER_TPR_STAGE_KB * 1024 / (TT * E * 4);
+  // Each stage belongs to one consumer warp (STAGES / CW stages per warp), so
+  // a warp always waits on its stages' phases in order and can never pass a
+  // barrier one phase early.
+  static_assert(STAGES % CW == 0, "stages must divide evenly among consumer warps");
+  static constexpr int SPW = STAGES / CW;
+  // Ring stage of the CTA's n-th tile: warp n % CW, that warp's (n / CW)-th use.
+  __device__ static int stage_of(int64_t n) { return (int)(n % CW) + CW * (int)((n / CW) % SPW); }
+  // Phase (use count) of that stage: n / STAGES.
   static constexpr int CTHREADS = CW * 32;
   static constexpr int THREADS = CTHREADS + 32;
   static constexpr size_t STAGE_BYTES = (size_t)TT * E * 4;
-  static constexpr size_t CNT_WORDS = (size_t)TT * E / 4;  // per consumer warp
   static constexpr size_t OFF_ROWS = 0;
-  static constexpr size_t OFF_CNT = OFF_ROWS + STAGES * STAGE_BYTES;
-  static constexpr size_t OFF_AFF = OFF_CNT + CW * CNT_WORDS * 4;
+  static constexpr size_t OFF_AFF = OFF_ROWS + STAGES * STAGE_BYTES;
   static constexpr size_t AFF_WORDS = (size_t)E * E;
   static constexpr size_t OFF_BAR = OFF_AFF + AFF_WORDS * 4;
   static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8;
@@ -86,27 +102,25 @@ __device__ __forceinline__ void clean8_desc(int (&m)[8]) {
   cas(m[0], m[1]); cas(m[2], m[3]); cas(m[4], m[5]); cas(m[6], m[7]);
 }
 
-// Top-8 keys (descending) of the lane's row and, if WANT9, the 9th key.
-// Position p (0..E-1) of a value in the lane's read order goes into the key's
-// low byte as 255 - p; the expert id of position p is p ^ (4 * (lane & 7)).
-template <int E, bool WANT9>
-__device__ __forceinline__ void row_top8(const float* row, int lane, int (&T)[8], int& L9) {
-  const char* base = reinterpret_cast<const char*>(row);
-  const int rot = (lane & 7) * 16;
+// Top-8 keys (descending) of this lane's part of a row and, if WANT9, the
+// 9th key.  The part holds NV values starting at expert PART * NV; it is read
+// in 16-byte units whose order is XOR-rotated by (lane & 7).  The value at
+// read position p of part h gets the low key byte 255 - (h * NV + p); its
+// expert id is h * NV + (p ^ (4 * rot)) with rot the reading lane's rotation.
+template <int NV, bool WANT9>
+__device__ __forceinline__ void part_top8(const float* part, int h, int rot, int (&T)[8], int& L9) {
+  const char* base = reinterpret_cast<const char*>(part);
+  const int r16 = rot * 16;
+  const int hb = h * NV;
   L9 = INT_MIN;
 #pragma unroll
-  for (int g = 0; g < E / 8; ++g) {
-    const float4 a = *reinterpret_cast<const float4*>(base + (((2 * g) * 16) ^ rot));
-    const float4 b = *reinterpret_cast<const float4*>(base + (((2 * g + 1) * 16) ^ rot));
+  for (int g = 0; g < NV / 8; ++g) {
+    const float4 a = *reinterpret_cast<const float4*>(base + (((2 * g) * 16) ^ r16));
+    const float4 b = *reinterpret_cast<const float4*>(base + (((2 * g + 1) * 16) ^ r16));
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     int c[8];
-    c[0] = (__float_as_int(a.x) & (int)0xFFFFFF00) | (255 - (8 * g + 0));
-    c[1] = (__float_as_int(a.y) & (int)0xFFFFFF00) | (255 - (8 * g + 1));
-    c[2] = (__float_as_int(a.z) & (int)0xFFFFFF00) | (255 - (8 * g + 2));
-    c[3] = (__float_as_int(a.w) & (int)0xFFFFFF00) | (255 - (8 * g + 3));
-    c[4] = (__float_as_int(b.x) & (int)0xFFFFFF00) | (255 - (8 * g + 4));
-    c[5] = (__float_as_int(b.y) & (int)0xFFFFFF00) | (255 - (8 * g + 5));
-    c[6] = (__float_as_int(b.z) & (int)0xFFFFFF00) | (255 - (8 * g + 6));
-    c[7] = (__float_as_int(b.w) & (int)0xFFFFFF00) | (255 - (8 * g + 7));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j] = (__float_as_int(v[j]) & (int)0xFFFFFF00) | (255 - hb - (8 * g + j));
     sort8_desc(c);
     if (g == 0) {
 #pragma unroll
@@ -122,6 +136,28 @@ __device__ __forceinline__ void row_top8(const float* row, int lane, int (&T)[8]
 #pragma unroll
       for (int i = 0; i < 8; ++i) T[i] = mrg[i];
     }
+  }
+}
+
+// Merges the sorted top-8 of the lanes that share a row (xor butterfly over
+// LPR lanes); afterwards every lane of the row holds the row's top-8 and 9th.
+template <int LPR, bool WANT9>
+__device__ __forceinline__ void merge_lanes(int (&T)[8], int& L9) {
+#pragma unroll
+  for (int sh = 1; sh < LPR; sh <<= 1) {
+    int P[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) P[i] = __shfl_xor_sync(FULL, T[i], sh);
+    if constexpr (WANT9) L9 = max(L9, __shfl_xor_sync(FULL, L9, sh));
+    int mrg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mrg[i] = max(T[i], P[7 - i]);
+      if constexpr (WANT9) L9 = max(L9, min(T[i], P[7 - i]));
+    }
+    clean8_desc(mrg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) T[i] = mrg[i];
   }
 }
 
@@ -166,36 +202,39 @@ __device__ int row_topk_exact(const float* row, int k, int lane) {
 
 // --------------------------------------------------------------- producer
 template <int E>
-__device__ void tpr_producer(const TprParams& p, char* smem, int64_t i0, int64_t i1) {
+__device__ void tpr_producer(const K1Params& p, char* smem, int64_t i0, int64_t i1) {
   using G = TprGeo<E>;
   if ((threadIdx.x & 31) != 0) return;
   float* rows = reinterpret_cast<float*>(smem + G::OFF_ROWS);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   uint64_t* empty = full + G::STAGES;
   const int64_t N = i1 - i0;
+  // (layer, tile) of the next copy, advanced incrementally (no division per item)
+  int cl = (int)(i0 / p.ntiles), ct = (int)(i0 % p.ntiles);
   int64_t n = 0;
   for (; n < N; ++n) {
-    const int s = (int)(n % G::STAGES);
+    const int s = G::stage_of(n);
     if (n >= G::STAGES && !mbar_wait(&empty[s], (uint32_t)((n / G::STAGES - 1) & 1), p.status)) break;
-    const int64_t it = i0 + n;
-    const int l = (int)(it / p.ntiles);
-    const int64_t tok0 = (it - (int64_t)l * p.ntiles) * G::TT;
-    const int ntok = (int)min64(G::TT, p.T - tok0);
-    const uint32_t bytes = (uint32_t)ntok * E * 4u;
+    const int64_t tok0 = (int64_t)ct * G::TT;
+    const uint32_t bytes = (uint32_t)min64(G::TT, p.T - tok0) * E * 4u;
     mbar_arrive_expect_tx(&full[s], bytes);
-    bulk_g2s(rows + (size_t)s * G::TT * E, p.logits + ((size_t)l * p.T + tok0) * E, bytes, &full[s]);
+    bulk_g2s(rows + (size_t)s * G::TT * E, p.logits + ((size_t)cl * p.T + tok0) * E, bytes, &full[s]);
+    if (++ct == p.ntiles) {
+      ct = 0;
+      ++cl;
+    }
   }
   if (n < N) {
     // a consumer stopped answering: wait (bounded) for the copies still in
     // flight into this CTA's shared memory before leaving
     for (int64_t q = (n > G::STAGES ? n - G::STAGES : 0); q < n; ++q)
-      mbar_wait(&full[q % G::STAGES], (uint32_t)((q / G::STAGES) & 1), nullptr);
+      mbar_wait(&full[G::stage_of(q)], (uint32_t)((q / G::STAGES) & 1), nullptr);
   }
 }
 
 // -------------------------------------------------------------- consumers
 template <int E>
-__device__ void tpr_flush_aff(const TprParams& p, int* aff, int layer) {
+__device__ void tpr_flush_aff(const K1Params& p, int* aff, int layer) {
   using G = TprGeo<E>;
   int32_t* dst = p.affinity + (size_t)layer * E * E;
   for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) {
@@ -208,24 +247,33 @@ __device__ void tpr_flush_aff(const TprParams& p, int* aff, int layer) {
 }
 
 template <int E, int K>
-__device__ void tpr_consumer(const TprParams& p, char* smem, int64_t i0, int64_t i1) {
+__device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t i1) {
   using G = TprGeo<E>;
-  constexpr int WPB = E / 4;  // packed count words per block
+  constexpr int LPR = G::LPR;
+  constexpr int NV = E / LPR;              // values folded by one lane
+  constexpr int KA = (K + LPR - 1) / LPR;  // ranks whose pairs this lane adds
+  static_assert(LPR == 1 || LPR == 2, "rank split assumes one or two lanes per row");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rrow = lane / LPR, h = lane % LPR, rot = lane & 7;
   const float* rows = reinterpret_cast<const float*>(smem + G::OFF_ROWS);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + G::OFF_CNT) + (size_t)warp * G::CNT_WORDS;
   int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   uint64_t* empty = full + G::STAGES;
   const bool aff_on = p.affinity != nullptr;
   const int64_t N = i1 - i0;
   const int l_first = (int)(i0 / p.ntiles), l_last = (int)((i1 - 1) / p.ntiles);
-  const int x4 = 4 * (lane & 7);
   int cur = l_first;
   bool dead = false;
+  int l = (int)((i0 + warp) / p.ntiles);
+  int tile = (int)((i0 + warp) - (int64_t)l * p.ntiles);
   for (int64_t n = warp; n < N; n += G::CW) {
-    const int64_t it = i0 + n;
-    const int l = (int)(it / p.ntiles);
+    if (n > warp) {
+      tile += G::CW;
+      while (tile >= p.ntiles) {
+        tile -= p.ntiles;
+        ++l;
+      }
+    }
     while (aff_on && cur < l) {
       named_bar(1, G::CTHREADS);
       if (!dead) tpr_flush_aff<E>(p, aff, cur);
@@ -234,25 +282,21 @@ __device__ void tpr_consumer(const TprParams& p, char* smem, int64_t i0, int64_t
     }
     cur = l;
     if (dead) continue;
-    const int s = (int)(n % G::STAGES);
-    const int64_t tok0 = (it - (int64_t)l * p.ntiles) * G::TT;
-    const int ntok = (int)min64(G::TT, p.T - tok0);
-    const int slot = p.slot_of_layer[l];
-    const bool hist = slot >= 0 && p.blk_cnt != nullptr;
-    int tb = 0, nbr = -1;
-    if (hist) {
-      tb = lane < ntok ? p.tok_blk[tok0 + lane] : 0;
-      if (lane == 0 && tok0 > 0) nbr = p.tok_blk[tok0 - 1];
-      if (lane == 1 && tok0 + ntok < p.T) nbr = p.tok_blk[tok0 + ntok];
-    }
+    const int s = G::stage_of(n);
     if (!mbar_wait(&full[s], (uint32_t)((n / G::STAGES) & 1), p.status)) {
       dead = true;
       continue;
     }
+    const int64_t tok0 = (int64_t)tile * G::TT;
+    const int ntok = (int)min64(G::TT, p.T - tok0);
+    const int slot = p.slot_of_layer[l];
+    uint8_t* out = nullptr;
+    if (p.ids != nullptr && (!p.ids_mask_only || slot >= 0))
+      out = p.ids + ((size_t)(p.ids_mask_only ? slot : l) * p.T + tok0) * K;
     const float* stage = rows + (size_t)s * G::TT * E;
-    const float* row = stage + (size_t)lane * E;
     int Tk[8], L9;
-    row_top8<E, (K == 8)>(row, lane, Tk, L9);
+    part_top8<NV, (K == 8)>(stage + (size_t)rrow * E + h * NV, h, rot, Tk, L9);
+    merge_lanes<LPR, (K == 8)>(Tk, L9);
     // certification of the truncated-key result
     const int nxt = (K == 8) ? L9 : Tk[K < 8 ? K : 7];
     bool bad = (Tk[K - 1] < 256) || (Tk[0] >= 0x7F800000);
@@ -262,50 +306,53 @@ __device__ void tpr_consumer(const TprParams& p, char* smem, int64_t i0, int64_t
       const int b = (i + 1 < K) ? Tk[i + 1] : nxt;
       bad = bad || (b >= (a & (int)0xFFFFFF00));
     }
-    const bool live = lane < ntok;
-    const unsigned redo = __ballot_sync(FULL, bad && live);
-    const bool mine = live && !bad;
-    const int blk0 = __shfl_sync(FULL, tb, 0);
-    const int lb = tb - blk0;
+    const bool live = rrow < ntok;
+    const unsigned redo = __ballot_sync(FULL, bad && live && h == 0);
+    // expert ids: position pos = 255 - low byte lies in part pos / NV, read
+    // by lane (row lanes) | part, whose rotation is that lane's (lane & 7)
     int idx[K];
 #pragma unroll
-    for (int i = 0; i < K; ++i) idx[i] = ((~Tk[i]) & 0xFF) ^ x4;
-    const size_t orow = (size_t)l * p.T + tok0;
-    if (mine) {
-      if (p.topk != nullptr) {
+    for (int i = 0; i < K; ++i) {
+      const int pos = (~Tk[i]) & 0xFF;
+      const int hp = pos / NV;
+      const int orot = ((lane & ~(LPR - 1)) | hp) & 7;
+      idx[i] = hp * NV + ((pos % NV) ^ (4 * orot));
+    }
+    if (live && !bad) {
+      if (out != nullptr && h == 0) {
         if constexpr (K == 8) {
           const uint32_t lo = (uint32_t)idx[0] | ((uint32_t)idx[1] << 8) | ((uint32_t)idx[2] << 16) |
                               ((uint32_t)idx[3] << 24);
           const uint32_t hi = (uint32_t)idx[4] | ((uint32_t)idx[5] << 8) | ((uint32_t)idx[6] << 16) |
                               ((uint32_t)idx[7] << 24);
-          *reinterpret_cast<uint2*>(p.topk + (orow + lane) * 8) = make_uint2(lo, hi);
+          *reinterpret_cast<uint2*>(out + (size_t)rrow * 8) = make_uint2(lo, hi);
         } else {
-          uint8_t* o = p.topk + (orow + lane) * K;
+          uint8_t* o = out + (size_t)rrow * K;
 #pragma unroll
           for (int i = 0; i < K; i += 2)
             *reinterpret_cast<uint16_t*>(o + i) = (uint16_t)(idx[i] | (idx[i + 1] << 8));
         }
       }
       if (aff_on) {
+        // this lane adds the pairs (a, *) of ranks a in [h*KA, h*KA+KA)
 #pragma unroll
-        for (int a = 0; a < K; ++a) {
-          int* ra = aff + idx[a] * E;
+        for (int j = 0; j < KA; ++j) {
+          const int ia = (LPR == 2 && h) ? idx[(KA + j < K) ? KA + j : 0] : idx[j];
+          if (h * KA + j < K) {
+            int* ra = aff + ia * E;
 #pragma unroll
-          for (int b = 0; b < K; ++b) atomicAdd(ra + idx[b], 1);
+            for (int b = 0; b < K; ++b) atomicAdd(ra + idx[b], 1);
+          }
         }
-      }
-      if (hist) {
-#pragma unroll
-        for (int i = 0; i < K; ++i) atomicAdd(&cnt[lb * WPB + (idx[i] >> 2)], 1u << ((idx[i] & 3) * 8));
       }
     }
     // rows the fast path could not certify: the whole warp redoes each exactly
     unsigned todo = redo;
     while (todo) {
-      const int f = __ffs(todo) - 1;
+      const int f = (__ffs(todo) - 1) / LPR;
       todo &= todo - 1;
       const int e = row_topk_exact<E>(stage + (size_t)f * E, K, lane);
-      if (p.topk != nullptr && lane < K) p.topk[(orow + f) * K + lane] = (uint8_t)e;
+      if (out != nullptr && lane < K) out[(size_t)f * K + lane] = (uint8_t)e;
       if (aff_on) {
 #pragma unroll
         for (int base = 0; base < K * K; base += 32) {
@@ -315,35 +362,9 @@ __device__ void tpr_consumer(const TprParams& p, char* smem, int64_t i0, int64_t
           if (q < K * K) atomicAdd(&aff[ia * E + ib], 1);
         }
       }
-      const int lbf = __shfl_sync(FULL, lb, f);
-      if (hist && lane < K) atomicAdd(&cnt[lbf * WPB + (e >> 2)], 1u << ((e & 3) * 8));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (hist) {
-      // write this tile's block counts (edge blocks may be shared with the
-      // neighbouring tiles: those were zeroed by the pre-pass and take atomics)
-      __syncwarp();
-      const int blkN = __shfl_sync(FULL, tb, ntok - 1);
-      const int before = __shfl_sync(FULL, nbr, 0);
-      const int after = __shfl_sync(FULL, nbr, 1);
-      const int nb = blkN - blk0 + 1;
-      for (int j = 0; j < nb; ++j) {
-        const bool partial = (j == 0 && before == blk0) || (j == nb - 1 && after == blkN);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(p.blk_cnt + ((size_t)(blk0 + j) * p.m + slot) * E);
-        uint32_t* src = cnt + j * WPB;
-#pragma unroll
-        for (int w = lane; w < WPB; w += 32) {
-          const uint32_t v = src[w];
-          if (!partial)
-            dst[w] = v;
-          else if (v != 0u)
-            atomicAdd(&dst[w], v);
-          src[w] = 0u;
-        }
-      }
-      __syncwarp();
-    }
   }
   if (aff_on) {
     while (cur < l_last) {
@@ -358,15 +379,12 @@ __device__ void tpr_consumer(const TprParams& p, char* smem, int64_t i0, int64_t
 }
 
 template <int E, int K>
-__global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __grid_constant__ TprParams p) {
+__global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __grid_constant__ K1Params p) {
   using G = TprGeo<E>;
   extern __shared__ __align__(1024) char smem[];
-  if (*reinterpret_cast<volatile uint32_t*>(p.call_flag) != 0u) return;
   const int64_t i0 = (int64_t)blockIdx.x * p.nitems / gridDim.x;
   const int64_t i1 = ((int64_t)blockIdx.x + 1) * p.nitems / gridDim.x;
   if (i1 <= i0) return;
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + G::OFF_CNT);
-  for (size_t w = threadIdx.x; w < G::CW * G::CNT_WORDS; w += G::THREADS) cnt[w] = 0u;
   if (p.affinity != nullptr) {
     int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
     for (size_t w = threadIdx.x; w < G::AFF_WORDS; w += G::THREADS) aff[w] = 0;
@@ -387,7 +405,7 @@ __global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __g
 }
 
 template <int E, int K>
-cudaError_t tpr_launch(const TprParams& p, int grid, cudaStream_t st) {
+cudaError_t tpr_launch(const K1Params& p, int grid, cudaStream_t st) {
   using G = TprGeo<E>;
   static bool configured = false;
   if (!configured) {
@@ -402,7 +420,9 @@ cudaError_t tpr_launch(const TprParams& p, int grid, cudaStream_t st) {
 
 bool tpr_supported(int E, int k) { return (E == 128 || E == 64) && (k == 8 || k == 6); }
 
-cudaError_t tpr_run(int E, int k, const TprParams& p, int grid, cudaStream_t st) {
+int tpr_tile_tokens(int E) { return E == 128 ? TprGeo<128>::TT : TprGeo<64>::TT; }
+
+cudaError_t tpr_run(int E, int k, const K1Params& p, int grid, cudaStream_t st) {
   if (E == 128 && k == 8) return tpr_launch<128, 8>(p, grid, st);
   if (E == 128 && k == 6) return tpr_launch<128, 6>(p, grid, st);
   if (E == 64 && k == 8) return tpr_launch<64, 8>(p, grid, st);

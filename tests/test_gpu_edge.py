@@ -3,8 +3,8 @@
 Shapes off the fast path (E from 4 to 256, k from 1 to 32), tie-heavy and
 special-valued logits (NaN, +-inf, -0.0/+0.0), length-1 requests, partial
 blocks, B = 1 and B = 255, an empty layer mask, a single token, and
-malformed block tables (reported through the workspace status, never a
-fault).
+malformed block tables (the bad blocks are skipped and reported through
+the workspace status, never a fault).
 """
 import numpy as np
 import pytest
@@ -47,7 +47,7 @@ def _logits(rs, kind, L, T, E):
     return x
 
 
-def _run(env, x, k, lengths, B, mask, want_aff=True):
+def _run(env, x, k, lengths, B, mask, want_aff=True, want_topk=True):
     torch, nat = env
     L, T, E = x.shape
     req_off, tab = _blocks(lengths, B)
@@ -60,11 +60,15 @@ def _run(env, x, k, lengths, B, mask, want_aff=True):
     aff = torch.zeros((L, E, E), dtype=torch.int32, device="cuda") if want_aff else None
     wsb = nat.moer_workspace_bytes(dims, T, len(tab), 0, 0)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-    nat.moer_topk_signature(dims, dx, T, dtab, len(tab), topk, cnt if m else None, aff, ws, wsb)
+    nat.moer_topk_signature(dims, dx, T, dtab, len(tab), topk if want_topk else None,
+                            cnt if m else None, aff, ws, wsb)
     assert nat.moer_ws_status(ws) == 0
     orc = oracle.get()
     tk = orc.topk(x, k)
-    assert np.array_equal(topk.cpu().numpy(), tk)
+    if want_topk:
+        assert np.array_equal(topk.cpu().numpy(), tk)
+    else:
+        assert (topk == 255).all()
     if m:
         bc = orc.block_counts(tk, E, req_off, B, mask)
         assert np.array_equal(cnt.cpu().numpy()[:len(tab)], bc)
@@ -112,6 +116,14 @@ def test_single_token_and_empty_mask(env):
     _run(env, _logits(rs, "normal", 3, 50, 64), 6, [20, 30], 16, [0, 1, 2], want_aff=False)
 
 
+@pytest.mark.parametrize("E,k", [(128, 8), (64, 6), (100, 5)])
+def test_block_counts_without_topk_output(env, E, k):
+    rs = np.random.RandomState(31 + E)
+    lengths = [5, 33, 16, 90]
+    x = _logits(rs, "normal", 4, sum(lengths), E)
+    _run(env, x, k, lengths, 16, [1, 3], want_topk=False)
+
+
 def test_many_tiles_ragged_tail(env):
     rs = np.random.RandomState(21)
     lengths = list(rs.randint(1, 200, size=60))
@@ -131,12 +143,17 @@ def test_malformed_block_table_is_reported(env):
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     nat.moer_topk_signature(dims, x, T, bad, 4, topk, cnt, None, ws, wsb)
     assert nat.moer_ws_status(ws) == 6  # MOER_EDATA
-    assert (topk == 255).all() and (cnt == 7).all()
+    # the malformed blocks are skipped; the good ones and the top-k are produced
+    c = cnt.cpu().numpy().astype(np.int64)
+    assert (c[2:] == 7).all()
+    assert (c[:2].sum(axis=2) == k * 16).all()
+    tk = oracle.get().topk(x.cpu().numpy(), k)
+    assert np.array_equal(topk.cpu().numpy(), tk)
     # the status word is cleared by the read; a good call afterwards succeeds
     good = torch.tensor([0, 16, 16, 16, 32, 16, 48, 16], dtype=torch.int32, device="cuda")
     nat.moer_topk_signature(dims, x, T, good, 4, topk, cnt, None, ws, wsb)
     assert nat.moer_ws_status(ws) == 0
-    assert (topk != 255).all()
+    assert (cnt.cpu().numpy().astype(np.int64).sum(axis=2) == k * 16).all()
 
 
 def test_stitch_bad_slot_is_reported(env):
