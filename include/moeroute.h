@@ -108,6 +108,38 @@ MOER_API moer_status moer_topk_signature(const moer_dims* d, const float* logits
                                 uint8_t* blk_cnt, int32_t* affinity, void* ws,
                                 size_t ws_bytes, moer_stream_t stream);
 
+/* moer_topk_signature for callers that cannot allocate device memory.
+ *
+ * No passage of the pages corresponds to this entry point; it exists for
+ * the integration.  Some callers cannot call cudaMalloc: code running inside
+ * another framework's memory pool or arena, plugins that must not grow the
+ * process's device-memory footprint after start-up, and latency-critical
+ * paths that must not allocate.  This call takes no workspace.  Its scratch
+ * is one fixed array in device memory, compiled into the library: 256 bytes
+ * of status plus MOER_NOALLOC_IDS_BYTES (32 MiB) for staging the mask
+ * layers' top-k ids, so every GPU that loads the library holds about 32 MiB
+ * until the process exits.
+ *
+ * Arguments and results are those of moer_topk_signature, without ws.
+ * The caller still passes every input and output.
+ *  - With topk == NULL and blk_cnt requested, m * T * k must not exceed
+ *    32 MiB, else MOER_ENOMEM is returned and nothing is launched.  With a
+ *    topk buffer the size limit does not apply.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current.  Make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array; each call clears the
+ *    status part before use.  Calls whose kernels overlap on the GPU (for
+ *    example on different streams without ordering) race on it.
+ *  - Malformed block-table entries are skipped as in moer_topk_signature,
+ *    but their MOER_EDATA status is not readable from the host; use
+ *    moer_topk_signature with a workspace when that report is needed.
+ */
+MOER_API moer_status moer_topk_signature_noalloc(const moer_dims* d, const float* logits, int64_t T,
+                                                 const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
+                                                 uint8_t* blk_cnt, int32_t* affinity,
+                                                 moer_stream_t stream);
+
 /* Prefix-cache stitching of per-block counts into per-request counts.
  *   [ELDR] table of what existing decode routing misses (signature cache),
  *   component table (signature cache) and section "Practical

@@ -7,5 +7,5 @@ binds it (`_native.py`, ctypes, same names as the C entry points).
 that the tests and the bench run.
 """
 from ._native import (moer_dims, make_dims, MoerError, moer_workspace_bytes,  # noqa: F401
-                      moer_topk_signature, moer_block_stitch, moer_affinity_load, moer_route,
+                      moer_topk_signature, moer_topk_signature_noalloc, moer_block_stitch, moer_affinity_load, moer_route,
                       moer_idf_fit, moer_ws_status, moer_status_str, moer_version, EXPORTS)

@@ -49,6 +49,7 @@ def _load():
     sigs = {
         "moer_workspace_bytes": ([dp, i64, i32, i32, i32], sz),
         "moer_topk_signature": ([dp, vp, i64, vp, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "moer_topk_signature_noalloc": ([dp, vp, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
         "moer_block_stitch": ([dp, vp, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp],
                               ctypes.c_int),
         "moer_affinity_load": ([dp, vp, vp, i32, vp, vp, vp, vp, vp], ctypes.c_int),
@@ -67,7 +68,8 @@ def _load():
 
 
 LIB = _load()
-EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_block_stitch", "moer_affinity_load",
+EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_noalloc",
+           "moer_block_stitch", "moer_affinity_load",
            "moer_route", "moer_idf_fit", "moer_ws_status", "moer_status_str", "moer_version")
 
 
@@ -100,6 +102,15 @@ def moer_topk_signature(dims, logits, T, blk_tab, nblk, topk, blk_cnt, affinity,
     _check("moer_topk_signature", LIB.moer_topk_signature(
         ctypes.byref(dims), _ptr(logits), int(T), _ptr(blk_tab), int(nblk), _ptr(topk),
         _ptr(blk_cnt), _ptr(affinity), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def moer_topk_signature_noalloc(dims, logits, T, blk_tab, nblk, topk, blk_cnt, affinity,
+                                stream=None) -> None:
+    """moer_topk_signature without a workspace: the scratch is a fixed array inside the library,
+    for callers that cannot allocate device memory (see include/moeroute.h)."""
+    _check("moer_topk_signature_noalloc", LIB.moer_topk_signature_noalloc(
+        ctypes.byref(dims), _ptr(logits), int(T), _ptr(blk_tab), int(nblk), _ptr(topk),
+        _ptr(blk_cnt), _ptr(affinity), _stream(stream)))
 
 
 def moer_block_stitch(dims, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, req_cache_off,

@@ -48,6 +48,26 @@ moer_status check_dims(const moer_dims* d, bool need_mask) {
 }
 
 }  // namespace
+
+// Host-side argument check of moer_topk_signature_noalloc: the same checks as
+// moer_topk_signature except the workspace, which that entry point does not take.
+moer_status topk_signature_check(const moer_dims* d, const float* logits, int64_t T,
+                                 const int32_t* blk_tab, int32_t nblk, const uint8_t* topk,
+                                 const uint8_t* blk_cnt, const int32_t* affinity) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (T < 0 || nblk < 0) return MOER_ERANGE;
+  if (T >= (int64_t(1) << 31)) return MOER_ERANGE;
+  if (T == 0) return MOER_OK;
+  if (logits == nullptr || !aligned(logits, 16)) return MOER_EINVAL;
+  if (affinity != nullptr && !aligned(affinity, 4)) return MOER_EINVAL;
+  if (topk != nullptr && !aligned(topk, 8)) return MOER_EINVAL;
+  if (blk_cnt != nullptr && d->m > 0) {
+    if (blk_tab == nullptr || !aligned(blk_tab, 4) || !aligned(blk_cnt, 4)) return MOER_EINVAL;
+    if (nblk < 1 || nblk > T) return MOER_ESHAPE;
+  }
+  return MOER_OK;
+}
 }  // namespace moer
 
 using namespace moer;

@@ -16,6 +16,8 @@ constexpr unsigned FULL = 0xffffffffu;
 // Workspace header: word 0 = sticky status bits (cleared by moer_ws_status),
 // word 1 = per-call validation flag of moer_topk_signature.
 constexpr size_t WS_HEADER = 256;
+// Capacity of moer_topk_signature_noalloc's fixed scratch for staged top-k ids.
+#define MOER_NOALLOC_IDS_BYTES (32u << 20)
 constexpr uint32_t WS_BIT_EDATA = 1u;
 constexpr uint32_t WS_BIT_ETIMEOUT = 2u;
 
