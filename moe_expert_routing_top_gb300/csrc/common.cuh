@@ -21,8 +21,10 @@ constexpr size_t WS_HEADER = 256;
 constexpr uint32_t WS_BIT_EDATA = 1u;
 constexpr uint32_t WS_BIT_ETIMEOUT = 2u;
 
-// Bounded waits: give up after this much wall time (ns).
+// Bounded waits: give up after this much wall time (ns), or after this many
+// polls should the wall clock not advance.
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint32_t WAIT_LIMIT_ITERS = 1u << 26;
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -73,7 +75,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+    if ((it & 63u) == 63u && (globaltimer_ns() - t0 > WAIT_LIMIT_NS || it >= WAIT_LIMIT_ITERS)) {
       if (status) atomicOr(status, WS_BIT_ETIMEOUT);
       return false;
     }
