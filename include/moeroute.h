@@ -203,6 +203,32 @@ MOER_API moer_status moer_route(const moer_dims* d, const int32_t* req_cnt, int3
                        int32_t* loads, int32_t live, float* sig, float* dist,
                        int32_t* choice, void* ws, size_t ws_bytes, moer_stream_t stream);
 
+/* Router (gate) GEMM with the top-k gate fused into its epilogue, on the
+ * 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA operands).
+ *   The router logits of every MoE layer, logit[l][t][e] = sum_h x[t][h] *
+ *   W[l][h][e] with bf16 operands and fp32 accumulation, feed the standard
+ *   top-k gate ([ELDR] section "What it tries to solve": each MoE token
+ *   picks its own top-k experts; section "Key idea / structure / operation":
+ *   the gate is unchanged), then the same per-KV-block counts and
+ *   co-activation counts as moer_topk_signature.
+ * Limits: E == 128, k in {6, 8}, H a multiple of 64 (64 .. 65536).
+ * hidden  [T][H] bf16 bits (uint16), 16-byte aligned; one hidden state per
+ *         computed token, shared by all L layers.
+ * w_gate  [L][H][E] bf16 bits, 16-byte aligned.
+ * logits  [L][T][E] fp32 or NULL: the fp32 logits (for inspection).
+ * topk    [L][T][k] uint8, required, 8-byte aligned: ranking as in
+ *         moer_topk_signature (on the fp32 accumulated logits).
+ * blk_tab, blk_cnt, affinity: as in moer_topk_signature (blk_cnt and
+ *         affinity may be NULL).
+ * ws      at least moer_gate_workspace_bytes(d, H) bytes, 256-byte aligned
+ *         (status word and the transposed gate weights).
+ */
+MOER_API size_t moer_gate_workspace_bytes(const moer_dims* d, int32_t H);
+MOER_API moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, int64_t T, int32_t H,
+                                    const uint16_t* w_gate, const int32_t* blk_tab, int32_t nblk,
+                                    float* logits, uint8_t* topk, uint8_t* blk_cnt, int32_t* affinity,
+                                    void* ws, size_t ws_bytes, moer_stream_t stream);
+
 /* Calibration helper (not on the per-request path): smoothed idf over R
  * calibration requests.  [ELDR] section "Key idea / structure / operation"
  * (idf reweighting fit offline on calibration prompts; formula not printed).

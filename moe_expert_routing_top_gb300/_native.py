@@ -56,6 +56,8 @@ def _load():
         "moer_route": ([dp, vp, i32, vp, vp, i32, f32, vp, i32, vp, vp, vp, vp, sz, vp],
                        ctypes.c_int),
         "moer_idf_fit": ([dp, vp, i32, vp, vp], ctypes.c_int),
+        "moer_gate_workspace_bytes": ([dp, i32], sz),
+        "moer_gate_topk": ([dp, vp, i64, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_ws_status": ([vp, vp], ctypes.c_int),
         "moer_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "moer_version": ([], ctypes.c_int32),
@@ -70,7 +72,8 @@ def _load():
 LIB = _load()
 EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_noalloc",
            "moer_block_stitch", "moer_affinity_load",
-           "moer_route", "moer_idf_fit", "moer_ws_status", "moer_status_str", "moer_version")
+           "moer_route", "moer_idf_fit", "moer_gate_workspace_bytes", "moer_gate_topk", "moer_ws_status",
+           "moer_status_str", "moer_version")
 
 
 def _ptr(x):
@@ -139,6 +142,18 @@ def moer_route(dims, req_cnt, R, idf, centroids, D, tau, loads, live, sig, dist,
 def moer_idf_fit(dims, req_cnt, R, idf, stream=None) -> None:
     _check("moer_idf_fit", LIB.moer_idf_fit(ctypes.byref(dims), _ptr(req_cnt), int(R), _ptr(idf),
                                             _stream(stream)))
+
+
+def moer_gate_workspace_bytes(dims, H: int) -> int:
+    return int(LIB.moer_gate_workspace_bytes(ctypes.byref(dims), int(H)))
+
+
+def moer_gate_topk(dims, hidden, T, H, w_gate, blk_tab, nblk, logits, topk, blk_cnt, affinity, ws,
+                   ws_bytes, stream=None) -> None:
+    _check("moer_gate_topk", LIB.moer_gate_topk(
+        ctypes.byref(dims), _ptr(hidden), int(T), int(H), _ptr(w_gate), _ptr(blk_tab), int(nblk),
+        _ptr(logits), _ptr(topk), _ptr(blk_cnt), _ptr(affinity), _ptr(ws), int(ws_bytes),
+        _stream(stream)))
 
 
 def moer_ws_status(ws, stream=None) -> int:

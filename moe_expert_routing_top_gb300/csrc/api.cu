@@ -23,6 +23,14 @@ moer_status route_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, 
                          float* sig, float* dist, int32_t* choice, void* ws, cudaStream_t st);
 moer_status idf_fit_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, float* idf,
                            cudaStream_t st);
+size_t gate_scratch_bytes(const moer_dims* d, int32_t H);
+moer_status gate_topk_launch(const moer_dims* d, const uint16_t* hidden, int64_t T, int32_t H,
+                             const uint16_t* w_gate, float* logits, uint8_t* topk, void* ws, cudaStream_t st);
+moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t T, int32_t* affinity,
+                                cudaStream_t st);
+moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mask_only, int64_t T,
+                                const int32_t* blk_tab, int nblk, uint8_t* blk_cnt, uint32_t* status,
+                                cudaStream_t st);
 
 namespace {
 
@@ -179,6 +187,44 @@ moer_status moer_idf_fit(const moer_dims* d, const int32_t* req_cnt, int32_t R, 
   if (R < 1) return MOER_ERANGE;
   if (req_cnt == nullptr || idf == nullptr) return MOER_EINVAL;
   return idf_fit_launch(d, req_cnt, R, idf, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moer_gate_workspace_bytes(const moer_dims* d, int32_t H) {
+  if (d == nullptr || d->L < 1 || H < 1) return WS_HEADER;
+  return WS_HEADER + gate_scratch_bytes(d, H);
+}
+
+moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, int64_t T, int32_t H,
+                           const uint16_t* w_gate, const int32_t* blk_tab, int32_t nblk, float* logits,
+                           uint8_t* topk, uint8_t* blk_cnt, int32_t* affinity, void* ws, size_t ws_bytes,
+                           moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (d->E != 128 || (d->k != 8 && d->k != 6)) return MOER_ERANGE;
+  if (H < 64 || H % 64 != 0 || H > 65536) return MOER_ERANGE;
+  if (T < 0 || T >= (int64_t(1) << 31) || nblk < 0) return MOER_ERANGE;
+  if (T == 0) return MOER_OK;
+  if (hidden == nullptr || w_gate == nullptr || topk == nullptr) return MOER_EINVAL;
+  if (!aligned(hidden, 16) || !aligned(w_gate, 16) || !aligned(topk, 8)) return MOER_EINVAL;
+  if (logits != nullptr && !aligned(logits, 16)) return MOER_EINVAL;
+  if (affinity != nullptr && !aligned(affinity, 4)) return MOER_EINVAL;
+  const bool hist = blk_cnt != nullptr && d->m > 0;
+  if (hist) {
+    if (blk_tab == nullptr || !aligned(blk_tab, 4) || !aligned(blk_cnt, 4)) return MOER_EINVAL;
+    if (nblk < 1 || nblk > T) return MOER_ESHAPE;
+  }
+  if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
+  if (ws_bytes < moer_gate_workspace_bytes(d, H)) return MOER_ENOMEM;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  s = gate_topk_launch(d, hidden, T, H, w_gate, logits, topk, ws, st);
+  if (s != MOER_OK) return s;
+  if (affinity != nullptr) {
+    s = affinity_ids_launch(d, topk, T, affinity, st);
+    if (s != MOER_OK) return s;
+  }
+  if (hist)
+    s = block_counts_launch(d, topk, false, T, blk_tab, nblk, blk_cnt, reinterpret_cast<uint32_t*>(ws), st);
+  return s;
 }
 
 moer_status moer_ws_status(void* ws, moer_stream_t stream) {

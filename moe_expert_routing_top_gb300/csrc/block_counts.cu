@@ -91,3 +91,83 @@ moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mas
 }
 
 }  // namespace moer
+
+namespace moer {
+
+// Per-layer co-activation counts from top-k ids (the gate path, where the ids
+// come out of the GEMM epilogue rather than from a logits pass).  GRACE-MoE,
+// section 3 and section 4 / Figure 2(a): A_l[a][b] += #tokens whose top-k
+// at layer l holds both a and b.  Persistent grid over (layer, 512-token
+// chunk) items in layer-major order; each CTA accumulates into a shared
+// E x (E+1) tile and flushes it (atomic adds) when its layer changes.
+constexpr int AI_CHUNK = 512;
+constexpr int AI_THREADS = 256;
+
+__global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t* __restrict__ ids, int64_t T,
+                                                                  int k, int E, int L, int nchunks,
+                                                                  int32_t* __restrict__ affinity) {
+  extern __shared__ int ai_tile[];  // [E][E+1]
+  const int stride = E + 1;
+  const int64_t nitems = (int64_t)L * nchunks;
+  const int64_t i0 = (int64_t)blockIdx.x * nitems / gridDim.x;
+  const int64_t i1 = ((int64_t)blockIdx.x + 1) * nitems / gridDim.x;
+  for (int c = threadIdx.x; c < E * stride; c += AI_THREADS) ai_tile[c] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane >> 3, j = lane & 7;  // four rows per warp step, eight id lanes per row
+  int cur = (int)(i0 / nchunks);
+  for (int64_t it = i0; it < i1; ++it) {
+    const int l = (int)(it / nchunks);
+    if (l != cur) {
+      __syncthreads();
+      for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
+        const int a = c / E, b = c - a * E;
+        const int v = ai_tile[a * stride + b];
+        if (v != 0) {
+          atomicAdd(&affinity[(size_t)cur * E * E + c], v);
+          ai_tile[a * stride + b] = 0;
+        }
+      }
+      __syncthreads();
+      cur = l;
+    }
+    const int64_t tb = (it - (int64_t)l * nchunks) * AI_CHUNK;
+    for (int r = warp * 4; r < AI_CHUNK; r += (AI_THREADS / 32) * 4) {
+      const int64_t t = tb + r + sub;
+      const bool ok = t < T && j < k;
+      const int e = ok ? ids[((size_t)l * T + t) * k + j] : 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int eb = __shfl_sync(FULL, e, (lane & ~7) | b);
+        if (ok && b < k) atomicAdd(&ai_tile[e * stride + eb], 1);
+      }
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
+    const int a = c / E, b = c - a * E;
+    const int v = ai_tile[a * stride + b];
+    if (v != 0) atomicAdd(&affinity[(size_t)cur * E * E + c], v);
+  }
+}
+
+moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t T, int32_t* affinity,
+                                cudaStream_t st) {
+  const int nchunks = (int)((T + AI_CHUNK - 1) / AI_CHUNK);
+  const int64_t nitems = (int64_t)d->L * nchunks;
+  const int sms = device_sm_count();
+  if (sms <= 0) return MOER_ECUDA;
+  const size_t smem = (size_t)d->E * (d->E + 1) * sizeof(int);
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(affinity_ids_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(129 * 128 * 4)) !=
+        cudaSuccess)
+      return MOER_ECUDA;
+    configured = true;
+  }
+  const int grid = (int)min64(nitems, (int64_t)sms * 2);
+  affinity_ids_kernel<<<grid, AI_THREADS, smem, st>>>(ids, T, d->k, d->E, d->L, nchunks, affinity);
+  return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
+}
+
+}  // namespace moer
