@@ -12,9 +12,10 @@
 //   * The weights are transposed once per call into the workspace,
 //     Wt[l*128 + e][h], so both operands are K-major.
 //   * One CTA per SM, persistent over tiles of 128 tokens x 2 layers
-//     (M = 128, N = 256 experts), K = H in blocks of 64.  Consecutive tiles of
-//     a CTA share the token block, so its hidden-state panel is re-read from
-//     L2, not HBM, for the other layers; the 25 MB of weights stay in L2.
+//     (M = 128, N = 256 experts), K = H in blocks of 64.  Tiles are dealt
+//     round-robin, token block major, so the grid works on a few token
+//     blocks at a time: each hidden-state panel is read from HBM once and
+//     shared through L2; the 25 MB of weights stay in L2.
 //   * Warp 0 streams both operands with TMA (cp.async.bulk.tensor, 128-byte
 //     swizzle) into a 4-stage ring of 48 KB stages (mbarrier full/empty).
 //   * Warp 1 owns a 512-column TMEM allocation (two fp32 128 x 256
@@ -190,8 +191,11 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t0 = (int64_t)blockIdx.x * p.ntiles / gridDim.x;
-  const int64_t t1 = ((int64_t)blockIdx.x + 1) * p.ntiles / gridDim.x;
+  // tiles are dealt round-robin: at any moment the grid works on ~gridDim.x
+  // consecutive tiles, i.e. on few token blocks, so each hidden-state panel
+  // comes from HBM once and is shared through L2 by the CTAs on its layers
+  const int64_t t0 = blockIdx.x, tstep = gridDim.x;
+  const int64_t t1 = p.ntiles;
   const int nkb = p.H / GK_BK;
 
   if (threadIdx.x == 0) {
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
     if (lane == 0) {
       int64_t g = 0;
       bool ok = true;
-      for (int64_t t = t0; t < t1 && ok; ++t) {
+      for (int64_t t = t0; t < t1 && ok; t += tstep) {
         const int mt = (int)(t / p.npairs), pair = (int)(t - (int64_t)mt * p.npairs);
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int s = (int)(g % GK_STAGES);
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
       int64_t g = 0;
       bool ok = true;
       int64_t j = 0;
-      for (int64_t t = t0; t < t1 && ok; ++t, ++j) {
+      for (int64_t t = t0; t < t1 && ok; t += tstep, ++j) {
         const int a = (int)(j & 1);
         if (j >= 2 && !mbar_wait(&tempty[a], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
           ok = false;
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
     const int row = q * 32 + lane;   // token row within the tile
     bool dead = false;
     int64_t j = 0;
-    for (int64_t t = t0; t < t1; ++t, ++j) {
+    for (int64_t t = t0; t < t1; t += tstep, ++j) {
       const int a = (int)(j & 1);
       if (dead) continue;
       if (!mbar_wait(&tfull[a], (uint32_t)((j >> 1) & 1), p.status)) {
