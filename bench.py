@@ -11,6 +11,15 @@ Inputs are seeded and synthetic (counter-based generator, filled on the GPU
 outside the timed region); the ~32.6 GB logits tensor is larger than L2, so no
 explicit L2 flush is needed between steps.
 
+The same line carries `gate_path`: the path from hidden states on the gate
+workload (bf16 hidden [524288, 2048] x 48 bf16 W_gate [2048, 128], 256
+requests of 2,048 tokens), whose first call is the tensor-core gate GEMM
+with the top-k fused behind it:
+
+    moer_gate_topk  ->  moer_block_stitch  ->  moer_affinity_load  ->  moer_route
+
+`--config c5` makes that path the line's main measurement.
+
 Output: one JSON line (rank 0).  `--impl reference` times the plain CPU oracle
 on host cores over a bounded sample of the same workload instead.
 """
@@ -37,8 +46,10 @@ WORKLOAD = {
     "c1": "OLMoE-shaped tiny (E=64,k=8,L=16,R=32)",
     "c2": "DeepSeek-V2-Lite-shaped calibration (E=64,k=6,L=26,R=1000)",
     "c3": "Qwen3-30B-A3B-shaped (E=128,k=8,L=48,R=1000,mask=12,D=16,G=8)",
+    "c5": "gate GEMM then path (bf16 hidden T=524288 x H=2048, E=128,k=8,L=48,R=256x2048)",
 }
 KERNEL_SOURCES = ["moe_expert_routing_top_gb300/csrc/topk_signature.cu",
+                  "moe_expert_routing_top_gb300/csrc/topk_signature_tpr.cu",
                   "moe_expert_routing_top_gb300/csrc/common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k1_dram_traffic.json")
 
@@ -56,8 +67,11 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
 
 
 # ----------------------------------------------------------------- clocks
@@ -164,12 +178,57 @@ def cpu_sample(wl, nreq):
     return b, logits
 
 
+def oracle_gate_pass(orc, wl, x, w):
+    """The plain oracle over the gate path for one request made of the given tokens."""
+    ntok = x.shape[0]
+    tk = orc.topk(orc.gate_logits(x, w), wl.k)
+    req_off = np.array([0, ntok], dtype=np.int32)
+    nblk = -(-ntok // wl.B)
+    bc = orc.block_counts(tk, wl.E, req_off, wl.B, wl.mask)
+    cache = np.zeros((1, wl.m, wl.E), dtype=np.uint8)
+    rc = orc.stitch(bc, req_off, wl.B, np.zeros(0, np.int32), np.zeros(2, np.int32), cache,
+                    np.full(nblk, -1, np.int32))
+    orc.affinity(tk, wl.E)
+    orc.loads(tk, wl.E, wl.group_of, wl.G)
+    _, dist = orc.sig_dist(rc, wl.idf, wl.centroids)
+    orc.route(dist, wl.tau, wl.loads0, wl.live)
+
+
+def run_reference_gate(args, ws):
+    import oracle
+    import gen
+    wl = gen.make_workload("c5")
+    orc = oracle.get()
+    ntok = args.ref_tokens
+    x = gen.host_hidden(wl.seed, 0, ntok, wl.hidden_dim)
+    w = gen.host_wgate(wl.seed, wl.L, wl.hidden_dim, wl.E, wl.wgate_scale)
+    for _ in range(args.warmup):
+        oracle_gate_pass(orc, wl, x, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_gate_pass(orc, wl, x, w)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = wl.L * ntok / dt
+    sample = f"first {ntok} tokens of c5 as one request ({ntok} tokens x {wl.L} layers) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD["c5"], "sample": sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     import oracle
     import gen
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.config == "c5":
+        return run_reference_gate(args, ws)
     wl = gen.make_workload(args.config)
     orc = oracle.get()
     b, logits = cpu_sample(wl, args.ref_requests)
@@ -205,6 +264,8 @@ def run_gpu(args):
     dist = init_dist(ws, "nccl")
     stream = torch.cuda.current_stream(device)
     sh = stream.cuda_stream
+    if args.config == "c5":
+        return run_gate_main(args, ws, rank, local, device, dist, stream)
 
     wl = gen.make_workload(args.config, R=args.requests)
     b = wl.batch()
@@ -262,6 +323,13 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_requests)
 
+    logits_gb = logits.numel() * 4 / 1e9
+    gate = None
+    if args.gate:
+        del logits, rs
+        torch.cuda.empty_cache()
+        gate = measure_gate(args, device, dist, stream, args.gate_steps, with_e2e=False)
+
     peaks = measured_peaks()
     achieved = alg_bytes / (k1_ms / 1e3) / 1e9
     traffic = None
@@ -279,7 +347,7 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD.get(args.config, args.config), "tokens": b.T,
                        "layers": wl.L, "requests": b.R, "kv_blocks": b.nblk,
                        "parallelism": f"replicas x{ws}",
-                       "l2": "inputs larger than L2 (logits %.1f GB per step)" % (logits.numel() * 4 / 1e9)},
+                       "l2": "inputs larger than L2 (logits %.1f GB per step)" % logits_gb},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "k1_kernel (moer_topk_signature)", "kernel_ms": k1_ms,
@@ -290,11 +358,190 @@ def run_gpu(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if gate is not None:
+            line["gate_path"] = {key: gate[key] for key in
+                                 ("workload", "value", "unit", "ms_per_step", "steps", "roofline",
+                                  "gpu_launches", "clocks")}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+GATE_LAUNCHES_PER_CALL = 4   # W_gate transpose, GEMM + top-k, co-activation, block counts
+
+
+def measure_gate(args, device, dist, stream, steps, with_e2e):
+    """The path from hidden states on the gate workload: per step moer_gate_topk (GEMM
+    with fused top-k, then co-activation and block counts from the ids), stitch, loads,
+    route.  The tensor roofline is taken on the moer_gate_topk call's duration (CUDA
+    events on the launching stream around the call, so the three short kernels behind
+    the GEMM count against it)."""
+    import torch
+    import gen
+    from moe_expert_routing_top_gb300 import pipeline
+    sh = stream.cuda_stream
+    wl = gen.make_workload("c5", R=args.requests)
+    b = wl.batch()
+    H = wl.hidden_dim
+    bd = pipeline.BatchDev.from_host(b, device=device)
+    hidden = torch.empty((b.T, H), dtype=torch.int16, device=device)
+    w_gate = torch.empty((wl.L, H, wl.E), dtype=torch.int16, device=device)
+    gen.dev_hidden(wl.seed, b.T, H, hidden, sh)
+    gen.dev_wgate(wl.seed, wl.L, H, wl.E, wl.wgate_scale, w_gate, sh)
+    rs = pipeline.RoutingStats.for_workload(wl, max_T=b.T, max_nblk=b.nblk, max_R=b.R,
+                                            device=device, stream=stream)
+    rs.ensure(b.T, b.nblk, b.R, H)
+    flops = 2.0 * b.T * H * wl.E * wl.L
+    launches = (GATE_LAUNCHES_PER_CALL + (2 if rs.cache is not None else 1) + 1
+                + (2 if wl.live else 1))
+    for _ in range(max(args.warmup, 3)):
+        rs.gate_step(hidden, w_gate, bd)
+    torch.cuda.synchronize()
+    if rs.status() != 0:
+        raise RuntimeError("device-side status after gate warm-up is not OK")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index or 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        rs.gate_topk(hidden, w_gate, bd)
+        ev[i][1].record(stream)
+        rs.block_stitch(bd)
+        rs.affinity_load()
+        rs.route(bd.R)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    if rs.status() != 0:
+        raise RuntimeError("device-side status after the timed gate steps is not OK")
+    ms_total = max_over_ranks(dist, start.elapsed_time(stop), device)
+    call_ms = statistics.mean(a.elapsed_time(z) for a, z in ev)
+    units = sum_over_ranks(dist, wl.L * b.T * steps, device)
+    peaks = measured_peaks()
+    achieved = flops / (call_ms / 1e3) / 1e12
+    out = {
+        "workload": WORKLOAD["c5"] if args.requests is None else f"c5 with {b.R} requests",
+        "value": units / (ms_total / 1e3), "unit": UNIT, "ms_per_step": ms_total / steps,
+        "steps": steps, "tokens": b.T, "layers": wl.L, "requests": b.R, "kv_blocks": b.nblk,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "traffic": None,
+                     "kernel": "gate_topk_kernel (moer_gate_topk call)", "kernel_ms": call_ms,
+                     "algorithmic_flops_per_launch": flops,
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"},
+        "gpu_launches": launches * steps,
+        "clocks": clk,
+        "l2": "inputs larger than L2 (hidden %.1f GB per step)" % (hidden.numel() * 2 / 1e9),
+    }
+    if with_e2e:
+        out["e2e"] = run_gate_e2e(args, wl, b, rs, hidden, w_gate, stream, device, dist)
+    return out
+
+
+def run_gate_main(args, ws, rank, local, device, dist, stream):
+    import gen
+    g = measure_gate(args, device, dist, stream, args.steps, with_e2e=args.e2e)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = gate_cpu_baseline(gen.make_workload("c5"), args.cpu_tokens)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": g["value"], "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": g["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded counter-based generator; stands in for the pages' datasets)",
+            "config": {"workload": g["workload"], "tokens": g["tokens"], "layers": g["layers"],
+                       "requests": g["requests"], "kv_blocks": g["kv_blocks"],
+                       "parallelism": f"replicas x{ws}", "l2": g["l2"]},
+            "roofline": g["roofline"], "gpu_launches": g["gpu_launches"], "clocks": g["clocks"],
+            "e2e": g.get("e2e"), "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_gate_e2e(args, wl, b, rs, hidden, w_gate, stream, device, dist):
+    """The gate path with host buffers: per step the hidden states go host -> device in
+    request chunks on a copy stream (W_gate stays resident, as model weights do),
+    overlapped with the path on the compute stream; the choices come back to the host."""
+    import torch
+    from moe_expert_routing_top_gb300 import pipeline
+    nch = args.e2e_chunks
+    bounds = np.linspace(0, wl.R, nch + 1).astype(int)
+    batches = [wl.batch(int(a), int(z)) for a, z in zip(bounds[:-1], bounds[1:])]
+    H = wl.hidden_dim
+    pinned = torch.empty((b.T, H), dtype=torch.int16, pin_memory=True)
+    pinned.copy_(hidden)  # untimed: the host copy of the same inputs
+    offs = np.concatenate([[0], np.cumsum([x.T for x in batches])]).astype(int)
+    copy_stream = torch.cuda.Stream(device)
+    maxT = max(x.T for x in batches)
+    dev_bufs = [torch.empty((maxT, H), dtype=torch.int16, device=device) for _ in range(2)]
+    bds = [pipeline.BatchDev.from_host(bb, device=device) for bb in batches]
+    choice_host = torch.empty(wl.R, dtype=torch.int32, pin_memory=True)
+
+    def one_step():
+        copied = [torch.cuda.Event() for _ in range(nch)]
+        freed = [torch.cuda.Event() for _ in range(nch)]
+        for i, bb in enumerate(batches):
+            dst = dev_bufs[i % 2][:bb.T]
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(freed[i - 2])
+                dst.copy_(pinned[offs[i]:offs[i + 1]], non_blocking=True)
+                copied[i].record(copy_stream)
+            stream.wait_event(copied[i])
+            rs.gate_step(dst, w_gate, bds[i])
+            freed[i].record(stream)
+            r0 = int(bounds[i])
+            choice_host[r0:r0 + bb.R].copy_(rs.choice[:bb.R], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        one_step()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one_step()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    dt = max_over_ranks(dist, dt, device)
+    units = sum_over_ranks(dist, wl.L * b.T, device)
+    return {"value": units / dt, "unit": UNIT, "h2d_bytes_per_step": int(b.T * H * 2),
+            "d2h_bytes_per_step": int(wl.R * 4), "ms_per_step": dt * 1e3, "chunks": nch,
+            "steps": args.e2e_steps}
+
+
+def gate_cpu_baseline(wl, ntok):
+    """The oracle's gate logits + top-k over the first `ntok` tokens (every layer), the
+    dominant CPU cost of the gate path, single thread."""
+    import oracle
+    import gen
+    orc = oracle.get()
+    H = wl.hidden_dim
+    x = gen.host_hidden(wl.seed, 0, ntok, H)
+    w = gen.host_wgate(wl.seed, wl.L, H, wl.E, wl.wgate_scale)
+    t0 = time.perf_counter()
+    orc.topk(orc.gate_logits(x, w), wl.k)
+    dt = time.perf_counter() - t0
+    return {"value": wl.L * ntok / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"gate logits (fp64 sums) + top-k of the first {ntok} tokens x {wl.L} "
+                      f"layers, one pass, {dt:.1f} s, single thread"}
 
 
 def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
@@ -374,16 +621,24 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["own", "reference"], default="own")
-    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3"])
+    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c5"])
     ap.add_argument("--requests", type=int, default=None,
                     help="run a reduced workload with this many requests (profiling)")
     ap.add_argument("--cpu-requests", type=int, default=16)
     ap.add_argument("--ref-requests", type=int, default=4)
+    ap.add_argument("--ref-tokens", type=int, default=32,
+                    help="gate path reference arm: tokens per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e", dest="e2e", action="store_true", default=True)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--gate", dest="gate", action="store_true", default=True,
+                    help="also measure the gate path (moer_gate_topk first) into gate_path")
+    ap.add_argument("--no-gate", dest="gate", action="store_false")
+    ap.add_argument("--gate-steps", type=int, default=10)
+    ap.add_argument("--cpu-tokens", type=int, default=512,
+                    help="gate path: tokens in the oracle's CPU-baseline sample")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "own":
         args.warmup = 3

@@ -97,76 +97,120 @@ namespace moer {
 // Per-layer co-activation counts from top-k ids (the gate path, where the ids
 // come out of the GEMM epilogue rather than from a logits pass).  GRACE-MoE,
 // section 3 and section 4 / Figure 2(a): A_l[a][b] += #tokens whose top-k
-// at layer l holds both a and b.  Persistent grid over (layer, 512-token
-// chunk) items in layer-major order; each CTA accumulates into a shared
-// E x (E+1) tile and flushes it (atomic adds) when its layer changes.
+// at layer l holds both a and b.
+//
+// Persistent grid over (layer, 512-token chunk) items in layer-major order,
+// one thread per token row.  A row's k distinct ids, in rank order, add its
+// k(k-1)/2 rank-ordered pairs to a shared tile of directed counts
+// D[a][b] (= # rows where a ranks above b).  When the CTA's layer changes
+// the tile is folded into the symmetric co-activation -- A[a][b] = D[a][b] +
+// D[b][a] off the diagonal, and A[a][a] = (sum over b != a of A[a][b]) /
+// (k - 1), since each row holding a holds k - 1 other experts -- and added to
+// global memory.  Needs k >= 2.
 constexpr int AI_CHUNK = 512;
-constexpr int AI_THREADS = 256;
+constexpr int AI_THREADS = 512;
 
+__device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* dst) {
+  for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
+    const int a = c / E, b = c - a * E;
+    if (a < b) {
+      const int v = tile[a * E + b] + tile[b * E + a];
+      if (v != 0) {
+        atomicAdd(&dst[a * E + b], v);
+        atomicAdd(&dst[b * E + a], v);
+        atomicAdd(&rsum[a], v);
+        atomicAdd(&rsum[b], v);
+      }
+    }
+  }
+  __syncthreads();
+  for (int a = threadIdx.x; a < E; a += AI_THREADS) {
+    const int v = rsum[a];
+    if (v != 0) {
+      atomicAdd(&dst[a * E + a], v / (k - 1));
+      rsum[a] = 0;
+    }
+  }
+  for (int c = threadIdx.x; c < E * E; c += AI_THREADS) tile[c] = 0;
+  __syncthreads();
+}
+
+template <int K>
 __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t* __restrict__ ids, int64_t T,
-                                                                  int k, int E, int L, int nchunks,
+                                                                  int E, int L, int nchunks,
                                                                   int32_t* __restrict__ affinity) {
-  extern __shared__ int ai_tile[];  // [E][E+1]
-  const int stride = E + 1;
+  extern __shared__ int ai_tile[];  // [E][E] directed counts, then [E] row sums
+  int* rsum = ai_tile + E * E;
   const int64_t nitems = (int64_t)L * nchunks;
   const int64_t i0 = (int64_t)blockIdx.x * nitems / gridDim.x;
   const int64_t i1 = ((int64_t)blockIdx.x + 1) * nitems / gridDim.x;
-  for (int c = threadIdx.x; c < E * stride; c += AI_THREADS) ai_tile[c] = 0;
+  for (int c = threadIdx.x; c < E * E + E; c += AI_THREADS) ai_tile[c] = 0;
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane >> 3, j = lane & 7;  // four rows per warp step, eight id lanes per row
   int cur = (int)(i0 / nchunks);
   for (int64_t it = i0; it < i1; ++it) {
     const int l = (int)(it / nchunks);
     if (l != cur) {
       __syncthreads();
-      for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
-        const int a = c / E, b = c - a * E;
-        const int v = ai_tile[a * stride + b];
-        if (v != 0) {
-          atomicAdd(&affinity[(size_t)cur * E * E + c], v);
-          ai_tile[a * stride + b] = 0;
-        }
-      }
-      __syncthreads();
+      affinity_ids_flush(ai_tile, rsum, E, K, affinity + (size_t)cur * E * E);
       cur = l;
     }
-    const int64_t tb = (it - (int64_t)l * nchunks) * AI_CHUNK;
-    for (int r = warp * 4; r < AI_CHUNK; r += (AI_THREADS / 32) * 4) {
-      const int64_t t = tb + r + sub;
-      const bool ok = t < T && j < k;
-      const int e = ok ? ids[((size_t)l * T + t) * k + j] : 0;
+    const int64_t t = (it - (int64_t)l * nchunks) * AI_CHUNK + threadIdx.x;
+    if (threadIdx.x < AI_CHUNK && t < T) {
+      const uint8_t* src = ids + ((size_t)l * T + t) * K;
+      int e[K];
+      if constexpr (K == 8) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int eb = __shfl_sync(FULL, e, (lane & ~7) | b);
-        if (ok && b < k) atomicAdd(&ai_tile[e * stride + eb], 1);
+        for (int j = 0; j < 4; ++j) {
+          e[j] = (w.x >> (8 * j)) & 0xFF;
+          e[4 + j] = (w.y >> (8 * j)) & 0xFF;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < K; j += 2) {
+          const uint32_t h = *reinterpret_cast<const uint16_t*>(src + j);
+          e[j] = h & 0xFF;
+          e[j + 1] = h >> 8;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < K - 1; ++i) {
+        int* ra = ai_tile + e[i] * E;
+#pragma unroll
+        for (int j = i + 1; j < K; ++j) atomicAdd(ra + e[j], 1);
       }
     }
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
-    const int a = c / E, b = c - a * E;
-    const int v = ai_tile[a * stride + b];
-    if (v != 0) atomicAdd(&affinity[(size_t)cur * E * E + c], v);
-  }
+  affinity_ids_flush(ai_tile, rsum, E, K, affinity + (size_t)cur * E * E);
 }
 
+// ids [L][T][k] (k = 6 or 8, 8-byte aligned rows for k = 8) -> affinity
+// [L][E][E] accumulated.
 moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t T, int32_t* affinity,
                                 cudaStream_t st) {
+  if (d->k != 8 && d->k != 6) return MOER_ERANGE;
+  if (d->E > 128) return MOER_ERANGE;
   const int nchunks = (int)((T + AI_CHUNK - 1) / AI_CHUNK);
   const int64_t nitems = (int64_t)d->L * nchunks;
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
-  const size_t smem = (size_t)d->E * (d->E + 1) * sizeof(int);
+  const size_t smem = ((size_t)d->E * d->E + d->E) * sizeof(int);
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(affinity_ids_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(129 * 128 * 4)) !=
-        cudaSuccess)
+    const int most = (int)((128 * 128 + 128) * sizeof(int));
+    if (cudaFuncSetAttribute(affinity_ids_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(affinity_ids_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
+            cudaSuccess)
       return MOER_ECUDA;
     configured = true;
   }
   const int grid = (int)min64(nitems, (int64_t)sms * 2);
-  affinity_ids_kernel<<<grid, AI_THREADS, smem, st>>>(ids, T, d->k, d->E, d->L, nchunks, affinity);
+  if (d->k == 8)
+    affinity_ids_kernel<8><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity);
+  else
+    affinity_ids_kernel<6><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 

@@ -17,6 +17,11 @@ struct K1Params {
   int ntiles;            // token tiles per layer
   int64_t nitems;        // L * ntiles work items
   uint32_t* status;      // sticky workspace status word
+  // 2^24 and 2^8, passed at run time so that the key builder's shift-and-
+  // insert stays a multiply-high and a multiply-add (FMA pipe) instead of
+  // being folded into a logic op on the integer ALU pipe, which the
+  // comparator networks already saturate
+  uint32_t key_hi_mul, key_lo_mul;
   int16_t slot_of_layer[256];  // mask slot of each layer, -1 if not a mask layer
 };
 

@@ -312,6 +312,8 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
   p.ntiles = ntiles;
   p.nitems = (int64_t)d->L * ntiles;
   p.status = status;
+  p.key_hi_mul = 1u << 24;
+  p.key_lo_mul = 1u << 8;
   for (int l = 0; l < 256; ++l) p.slot_of_layer[l] = -1;
   for (int i = 0; i < d->m; ++i) p.slot_of_layer[d->mask[i]] = (int16_t)i;
   const int grid = (int)min64(p.nitems, sms);

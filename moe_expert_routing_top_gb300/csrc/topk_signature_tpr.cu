@@ -9,30 +9,33 @@
 // Figure 2(a) (per-layer expert co-activation).
 //
 // Design (GB300):
-//   * Persistent grid, one CTA per SM: one producer warp and eight consumer
-//     warps.  Work items are (layer, 16-token tile); tile n of the CTA goes to
-//     consumer warp n % 8 and to one of that warp's own ring stages (one
-//     cp.async.bulk copy of 16 contiguous logit rows, completing on an
+//   * Persistent grid, one CTA per SM: one producer warp and ten consumer
+//     warps.  Work items are (layer, 32-token tile); tile n of the CTA goes to
+//     consumer warp n % 10 and to that warp's own ring stage (one
+//     cp.async.bulk copy of 32 contiguous logit rows, completing on an
 //     mbarrier).  Stages are never shared between consumer warps, so each
 //     warp meets its stages' barrier phases strictly in order.
-//   * Two consumer lanes share one token row; each reads its half from shared
-//     memory in 16-byte units whose order is XOR-rotated by (lane & 7), which
-//     makes every LDS.128 conflict-free, and folds it 8 values at a time into
-//     a sorted top-8 held in registers: an optimal 19-comparator sorting
-//     network per chunk, then a bitonic split/merge with the running top-8
-//     (the split's losers give the 9th-ranked key).  The two halves are then
-//     merged the same way across the lane pair with shuffles.  Keys are the
-//     float's upper 24 bits (signed-int order equals value order for positive
-//     floats) with the value's position in the lane's read order in the low
-//     8 bits, so keys are unique and min/max networks apply.
+//   * One consumer lane per token row (two lanes per row is a build option:
+//     the halves are then merged across the lane pair with shuffles).  A lane
+//     reads its row from shared memory in 16-byte units whose order is
+//     XOR-rotated by (lane & 7), which makes every LDS.128 conflict-free, and
+//     folds it 8 values at a time into a sorted top-8 held in registers: an
+//     optimal 19-comparator sorting network per chunk, then a bitonic
+//     split/merge with the running top-8 (the split's losers, folded with
+//     3-input maxima, give the 9th-ranked key).  Keys are the float's upper
+//     24 bits (signed-int order equals value order for positive floats) with
+//     the value's position in the lane's read order in the low 8 bits, so
+//     keys are unique and min/max networks apply.
 //   * A row's result is certified when its k leading keys are positive and
 //     finite and the k+1 leading keys are pairwise distinct in their upper
 //     24 bits (then truncation cannot have changed membership or order).
 //     Rows that fail (ties, NaN, +-inf, zeros, negatives in the top k) are
 //     redone exactly by the whole warp with the ballot tie-breaking path.
-//   * Co-activation: each lane adds its row's k*k ordered pairs to a
-//     shared-memory E x E int32 tile with shared atomics; the four consumer
-//     warps flush it to global memory (atomic adds) at each layer change.
+//   * Co-activation: each lane adds its row's k(k-1)/2 rank-ordered pairs to
+//     a shared-memory E x E int32 tile of directed counts with shared atomics
+//     (28 adds per row at k = 8 instead of the 64 of the full k x k block);
+//     the consumer warps fold the tile into the symmetric co-activation,
+//     diagonal included, and add it to global memory at each layer change.
 //   * The top-k ids go out as 8 (or 6) bytes per row; the per-KV-block
 //     counts are computed from them by block_counts.cu.
 #include <climits>
@@ -44,13 +47,13 @@ namespace moer {
 
 // Geometry (compile-time tunables with the measured defaults).
 #ifndef MOER_TPR_LPR
-#define MOER_TPR_LPR 2
+#define MOER_TPR_LPR 1
 #endif
 #ifndef MOER_TPR_CW
-#define MOER_TPR_CW 8
+#define MOER_TPR_CW 10
 #endif
 #ifndef MOER_TPR_STAGE_KB
-#define MOER_TPR_STAGE_KB 128
+#define MOER_TPR_STAGE_KB 160
 #endif
 
 template <int E>
@@ -73,7 +76,8 @@ struct TprGeo {
   static constexpr size_t OFF_ROWS = 0;
   static constexpr size_t OFF_AFF = OFF_ROWS + STAGES * STAGE_BYTES;
   static constexpr size_t AFF_WORDS = (size_t)E * E;
-  static constexpr size_t OFF_BAR = OFF_AFF + AFF_WORDS * 4;
+  static constexpr size_t OFF_RSUM = OFF_AFF + AFF_WORDS * 4;  // E row sums used by the flush
+  static constexpr size_t OFF_BAR = OFF_RSUM + (size_t)E * 4;
   static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8;
 };
 
@@ -102,13 +106,44 @@ __device__ __forceinline__ void clean8_desc(int (&m)[8]) {
   cas(m[0], m[1]); cas(m[2], m[3]); cas(m[4], m[5]); cas(m[6], m[7]);
 }
 
+// Folds the losers of a half-cleaner step (mins of T[i] and U[7 - i]) into
+// the running 9th key with 3-input maxima (one ALU op each).
+__device__ __forceinline__ int fold_losers(int L9, const int (&lo)[8]) {
+  const int a = __vimax3_s32(lo[0], lo[1], lo[2]);
+  const int b = __vimax3_s32(lo[3], lo[4], lo[5]);
+  const int c = __vimax3_s32(lo[6], lo[7], L9);
+  return __vimax3_s32(a, b, c);
+}
+
+// T <- top-8 of T and U (both sorted descending), sorted descending; with
+// WANT9, L9 <- max(L9, 9th key of T and U).
+template <bool WANT9>
+__device__ __forceinline__ void merge8(int (&T)[8], const int (&U)[8], int& L9) {
+  int mrg[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mrg[i] = max(T[i], U[7 - i]);
+  if constexpr (WANT9) {
+    int lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo[i] = min(T[i], U[7 - i]);
+    L9 = fold_losers(L9, lo);
+  }
+  clean8_desc(mrg);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) T[i] = mrg[i];
+}
+
 // Top-8 keys (descending) of this lane's part of a row and, if WANT9, the
 // 9th key.  The part holds NV values starting at expert PART * NV; it is read
 // in 16-byte units whose order is XOR-rotated by (lane & 7).  The value at
 // read position p of part h gets the low key byte 255 - (h * NV + p); its
 // expert id is h * NV + (p ^ (4 * rot)) with rot the reading lane's rotation.
+// The key keeps the float's upper 24 bits: (bits >> 8) * 256 + byte, computed
+// as a multiply-high and a multiply-add by the run-time constants hi_mul =
+// 2^24 and lo_mul = 2^8.
 template <int NV, bool WANT9>
-__device__ __forceinline__ void part_top8(const float* part, int h, int rot, int (&T)[8], int& L9) {
+__device__ __forceinline__ void part_top8(const float* part, int h, int rot, uint32_t hi_mul, uint32_t lo_mul,
+                                          int (&T)[8], int& L9) {
   const char* base = reinterpret_cast<const char*>(part);
   const int r16 = rot * 16;
   const int hb = h * NV;
@@ -120,21 +155,14 @@ __device__ __forceinline__ void part_top8(const float* part, int h, int rot, int
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     int c[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = (__float_as_int(v[j]) & (int)0xFFFFFF00) | (255 - hb - (8 * g + j));
+    for (int j = 0; j < 8; ++j)
+      c[j] = (int)(__umulhi(__float_as_uint(v[j]), hi_mul) * lo_mul + (uint32_t)(255 - hb - (8 * g + j)));
     sort8_desc(c);
     if (g == 0) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) T[i] = c[i];
     } else {
-      int mrg[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mrg[i] = max(T[i], c[7 - i]);
-        if constexpr (WANT9) L9 = max(L9, min(T[i], c[7 - i]));
-      }
-      clean8_desc(mrg);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) T[i] = mrg[i];
+      merge8<WANT9>(T, c, L9);
     }
   }
 }
@@ -149,15 +177,7 @@ __device__ __forceinline__ void merge_lanes(int (&T)[8], int& L9) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) P[i] = __shfl_xor_sync(FULL, T[i], sh);
     if constexpr (WANT9) L9 = max(L9, __shfl_xor_sync(FULL, L9, sh));
-    int mrg[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      mrg[i] = max(T[i], P[7 - i]);
-      if constexpr (WANT9) L9 = max(L9, min(T[i], P[7 - i]));
-    }
-    clean8_desc(mrg);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) T[i] = mrg[i];
+    merge8<WANT9>(T, P, L9);
   }
 }
 
@@ -233,16 +253,41 @@ __device__ void tpr_producer(const K1Params& p, char* smem, int64_t i0, int64_t 
 }
 
 // -------------------------------------------------------------- consumers
-template <int E>
-__device__ void tpr_flush_aff(const K1Params& p, int* aff, int layer) {
+// The shared tile holds directed pair counts D[a][b] = # rows of this CTA's
+// current layer in which expert a ranks above expert b.  Co-activation is
+// symmetric: A[a][b] = D[a][b] + D[b][a] for a != b, and, every row holding
+// k distinct experts, the diagonal (the expert's load) is its off-diagonal
+// row sum divided by k - 1.  Adds the tile to layer `layer` of the global
+// co-activation and clears it.  All consumer threads call this (it holds a
+// barrier); `skip` leaves the tile alone (a consumer warp timed out).
+template <int E, int K>
+__device__ void tpr_flush_aff(const K1Params& p, int* aff, int* rsum, int layer, bool skip) {
   using G = TprGeo<E>;
   int32_t* dst = p.affinity + (size_t)layer * E * E;
-  for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) {
-    const int v = aff[c];
-    if (v != 0) {
-      atomicAdd(&dst[c], v);
-      aff[c] = 0;
+  if (!skip) {
+    for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) {
+      const int a = c / E, b = c % E;
+      if (a < b) {
+        const int v = aff[a * E + b] + aff[b * E + a];
+        if (v != 0) {
+          atomicAdd(&dst[a * E + b], v);
+          atomicAdd(&dst[b * E + a], v);
+          atomicAdd(&rsum[a], v);
+          atomicAdd(&rsum[b], v);
+        }
+      }
     }
+  }
+  named_bar(1, G::CTHREADS);
+  if (!skip) {
+    for (int a = threadIdx.x; a < E; a += G::CTHREADS) {
+      const int v = rsum[a];
+      if (v != 0) {
+        atomicAdd(&dst[a * E + a], v / (K - 1));
+        rsum[a] = 0;
+      }
+    }
+    for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) aff[c] = 0;
   }
 }
 
@@ -251,12 +296,12 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   using G = TprGeo<E>;
   constexpr int LPR = G::LPR;
   constexpr int NV = E / LPR;              // values folded by one lane
-  constexpr int KA = (K + LPR - 1) / LPR;  // ranks whose pairs this lane adds
   static_assert(LPR == 1 || LPR == 2, "rank split assumes one or two lanes per row");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rrow = lane / LPR, h = lane % LPR, rot = lane & 7;
   const float* rows = reinterpret_cast<const float*>(smem + G::OFF_ROWS);
   int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
+  int* rsum = reinterpret_cast<int*>(smem + G::OFF_RSUM);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   uint64_t* empty = full + G::STAGES;
   const bool aff_on = p.affinity != nullptr;
@@ -276,7 +321,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     }
     while (aff_on && cur < l) {
       named_bar(1, G::CTHREADS);
-      if (!dead) tpr_flush_aff<E>(p, aff, cur);
+      tpr_flush_aff<E, K>(p, aff, rsum, cur, dead);
       named_bar(1, G::CTHREADS);
       ++cur;
     }
@@ -295,7 +340,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
       out = p.ids + ((size_t)(p.ids_mask_only ? slot : l) * p.T + tok0) * K;
     const float* stage = rows + (size_t)s * G::TT * E;
     int Tk[8], L9;
-    part_top8<NV, (K == 8)>(stage + (size_t)rrow * E + h * NV, h, rot, Tk, L9);
+    part_top8<NV, (K == 8)>(stage + (size_t)rrow * E + h * NV, h, rot, p.key_hi_mul, p.key_lo_mul, Tk, L9);
     merge_lanes<LPR, (K == 8)>(Tk, L9);
     // certification of the truncated-key result
     const int nxt = (K == 8) ? L9 : Tk[K < 8 ? K : 7];
@@ -308,15 +353,19 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     }
     const bool live = rrow < ntok;
     const unsigned redo = __ballot_sync(FULL, bad && live && h == 0);
-    // expert ids: position pos = 255 - low byte lies in part pos / NV, read
-    // by lane (row lanes) | part, whose rotation is that lane's (lane & 7)
+    // expert ids: position pos = 255 - low byte lies in part hp = pos / NV,
+    // read by lane (row lanes) | hp with rotation orot = that lane's & 7, so
+    // id = hp * NV + ((pos % NV) ^ 4 orot).  4 orot < NV leaves bit log2(NV)
+    // alone, hence id = pos ^ 4 orot = pos ^ xrow ^ 4 hp with the row's
+    // constant xrow = 4 ((lane & ~(LPR-1)) & 7) and 4 hp = (pos >> (log2(NV) - 2)) & 4.
+    static_assert(4 * 7 < NV && (NV & (NV - 1)) == 0, "id recovery assumes NV a power of two >= 32");
+    constexpr int HSH = (NV == 64) ? 4 : 3;
+    const int xrow = 4 * ((lane & ~(LPR - 1)) & 7);
     int idx[K];
 #pragma unroll
     for (int i = 0; i < K; ++i) {
       const int pos = (~Tk[i]) & 0xFF;
-      const int hp = pos / NV;
-      const int orot = ((lane & ~(LPR - 1)) | hp) & 7;
-      idx[i] = hp * NV + ((pos % NV) ^ (4 * orot));
+      idx[i] = (LPR == 2) ? (pos ^ xrow ^ ((pos >> HSH) & 4)) : (pos ^ xrow);
     }
     if (live && !bad) {
       if (out != nullptr && h == 0) {
@@ -334,14 +383,14 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
         }
       }
       if (aff_on) {
-        // this lane adds the pairs (a, *) of ranks a in [h*KA, h*KA+KA)
+        // directed pairs (rank i above rank j): k(k-1)/2 adds per row; with
+        // two lanes per row, lane h takes the ranks i with i % 2 == h
 #pragma unroll
-        for (int j = 0; j < KA; ++j) {
-          const int ia = (LPR == 2 && h) ? idx[(KA + j < K) ? KA + j : 0] : idx[j];
-          if (h * KA + j < K) {
-            int* ra = aff + ia * E;
+        for (int i = 0; i < K - 1; ++i) {
+          if (i % LPR == h) {
+            int* ra = aff + idx[i] * E;
 #pragma unroll
-            for (int b = 0; b < K; ++b) atomicAdd(ra + idx[b], 1);
+            for (int j = i + 1; j < K; ++j) atomicAdd(ra + idx[j], 1);
           }
         }
       }
@@ -359,7 +408,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
           const int q = base + lane;
           const int ia = __shfl_sync(FULL, e, q < K * K ? q / K : 0);
           const int ib = __shfl_sync(FULL, e, q < K * K ? q % K : 0);
-          if (q < K * K) atomicAdd(&aff[ia * E + ib], 1);
+          if (q < K * K && q / K < q % K) atomicAdd(&aff[ia * E + ib], 1);
         }
       }
     }
@@ -369,12 +418,12 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   if (aff_on) {
     while (cur < l_last) {
       named_bar(1, G::CTHREADS);
-      if (!dead) tpr_flush_aff<E>(p, aff, cur);
+      tpr_flush_aff<E, K>(p, aff, rsum, cur, dead);
       named_bar(1, G::CTHREADS);
       ++cur;
     }
     named_bar(1, G::CTHREADS);
-    if (!dead) tpr_flush_aff<E>(p, aff, cur);
+    tpr_flush_aff<E, K>(p, aff, rsum, cur, dead);
   }
 }
 
@@ -387,7 +436,7 @@ __global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __g
   if (i1 <= i0) return;
   if (p.affinity != nullptr) {
     int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
-    for (size_t w = threadIdx.x; w < G::AFF_WORDS; w += G::THREADS) aff[w] = 0;
+    for (size_t w = threadIdx.x; w < G::AFF_WORDS + E; w += G::THREADS) aff[w] = 0;  // tile and row sums
   }
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   if (threadIdx.x == 0) {

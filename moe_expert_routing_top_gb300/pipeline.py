@@ -9,6 +9,10 @@ stream:
   moer_affinity_load   expert / group loads and skew from the co-activation
   moer_route           signatures, centroid distances, tau-band decoder choice
 
+or, when the router logits are not materialised, `moer_gate_topk` (the bf16
+gate GEMM with top-k, block counts and co-activation fused behind it) in
+place of the first call.
+
 This module only marshals arguments and orders calls; every step of the
 path runs in the library's kernels.
 """
@@ -74,6 +78,7 @@ class RoutingStats:
         self.cache = (torch.zeros((nslots, self.m, E), dtype=torch.uint8, device=dev)
                       if nslots > 0 else None)
         self.nslots = nslots
+        self.gate_H = 0
         self._alloc(max_T, max_nblk, max_R)
 
     def _alloc(self, T, nblk, R):
@@ -86,10 +91,15 @@ class RoutingStats:
         self.dist = torch.empty((max(R, 1), D), dtype=torch.float32, device=dev)
         self.choice = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
         self.ws_bytes = nat.moer_workspace_bytes(self.dims, T, nblk, R, D)
+        if self.gate_H:
+            self.ws_bytes = max(self.ws_bytes, nat.moer_gate_workspace_bytes(self.dims, self.gate_H))
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
 
-    def ensure(self, T, nblk, R):
-        if T > self.cap[0] or nblk > self.cap[1] or R > self.cap[2]:
+    def ensure(self, T, nblk, R, H=0):
+        grow_gate = H > self.gate_H
+        if grow_gate:
+            self.gate_H = H
+        if grow_gate or T > self.cap[0] or nblk > self.cap[1] or R > self.cap[2]:
             self._alloc(max(T, self.cap[0]), max(nblk, self.cap[1]), max(R, self.cap[2]))
 
     def topk_for(self, T: int) -> torch.Tensor:
@@ -104,6 +114,13 @@ class RoutingStats:
         nat.moer_topk_signature(self.dims, logits, bd.T, bd.blk_tab, bd.nblk,
                                 self.topk if write_topk else None, self.blk_cnt, self.affinity,
                                 self.ws, self.ws_bytes, self.stream)
+
+    def gate_topk(self, hidden, w_gate, bd: BatchDev, logits=None):
+        """hidden bf16 [T][H] x w_gate bf16 [L][H][E] -> top-k, block counts, co-activation."""
+        H = hidden.shape[-1]
+        nat.moer_gate_topk(self.dims, hidden, bd.T, H, w_gate, bd.blk_tab, bd.nblk, logits,
+                           self.topk, self.blk_cnt, self.affinity, self.ws, self.ws_bytes,
+                           self.stream)
 
     def block_stitch(self, bd: BatchDev):
         use_cache = self.cache is not None and bd.req_cache_off is not None
@@ -127,6 +144,14 @@ class RoutingStats:
         """All rows of the path over one batch (loads and co-activation accumulate)."""
         self.ensure(bd.T, bd.nblk, bd.R)
         self.topk_signature(logits, bd, write_topk)
+        self.block_stitch(bd)
+        self.affinity_load()
+        self.route(bd.R, write_sig)
+
+    def gate_step(self, hidden, w_gate, bd: BatchDev, write_sig=True):
+        """All rows of the path over one batch, starting from hidden states (gate GEMM)."""
+        self.ensure(bd.T, bd.nblk, bd.R, hidden.shape[-1])
+        self.gate_topk(hidden, w_gate, bd)
         self.block_stitch(bd)
         self.affinity_load()
         self.route(bd.R, write_sig)

@@ -82,3 +82,27 @@ def check_live_route(choice, dist_ref, tau, loads0, oracle_choice):
             assert valid_choice(q, dist_ref[r], tau, loads), f"invalid live pick at request {r}"
         loads[q] += 1
     return int(edge.sum()), len(diff)
+
+
+def _gate_rows(args):
+    import oracle
+    x, w = args
+    return oracle.get().gate_logits(x, w)
+
+
+def oracle_gate_logits(x, w, nproc=None):
+    """The oracle's gate logits [L][T][E], token ranges spread over spawned worker processes
+    (the oracle itself is single-threaded; spawn, because this process holds a CUDA context;
+    an executor, so a worker that dies raises instead of leaving the pool waiting)."""
+    import multiprocessing as mp
+    import os
+    from concurrent.futures import ProcessPoolExecutor
+    T = x.shape[0]
+    nproc = nproc or max(1, min(16, os.cpu_count() or 1))
+    cuts = np.linspace(0, T, min(nproc, T) + 1).astype(int)
+    parts = [(x[a:z], w) for a, z in zip(cuts[:-1], cuts[1:]) if z > a]
+    if len(parts) == 1:
+        return _gate_rows(parts[0])
+    with ProcessPoolExecutor(len(parts), mp_context=mp.get_context("spawn")) as ex:
+        outs = list(ex.map(_gate_rows, parts, timeout=900))
+    return np.concatenate(outs, axis=1)

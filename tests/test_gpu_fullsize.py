@@ -73,7 +73,10 @@ def test_qwen3_full(env):
     req = gu.host(rs.req_cnt[:b.R])
     sig = gu.host(rs.sig[:b.R])
     dist = gu.host(rs.dist[:b.R])
-    for r in rng.choice(b.R, size=12, replace=False):
+    choice = gu.host(rs.choice[:b.R])
+    picks = rng.choice(b.R, size=12, replace=False)
+    dref = np.zeros((len(picks), wl.D))
+    for j, r in enumerate(picks):
         keys = b.tok_key[b.req_off[r]:b.req_off[r + 1]]
         doms = b.tok_dom[b.req_off[r]:b.req_off[r + 1]]
         cnt = np.zeros((wl.m, wl.E), dtype=np.int32)
@@ -83,13 +86,16 @@ def test_qwen3_full(env):
             cnt[i] = np.bincount(orc.topk(rr, wl.k).reshape(-1), minlength=wl.E)
         assert np.array_equal(req[r], cnt), r
         s = orc.signature(cnt, wl.idf)
+        dref[j] = orc.distances(s, wl.centroids)
         gu.assert_close(sig[r], s, "signature")
-        gu.assert_close(dist[r], orc.distances(s, wl.centroids), "distance")
-    # static route of every request against the oracle on the GPU's counts' oracle distances
-    _, dref = orc.sig_dist(req, wl.idf, wl.centroids)
+        gu.assert_close(dist[r], dref[j], "distance")
+    # sampled requests' decoder choices against the oracle's route on the oracle's distances
     och, _ = orc.route(dref, wl.tau, wl.loads0, False)
-    e, d = gu.check_static_route(gu.host(rs.choice[:b.R]), dref, wl.tau, wl.loads0, och)
-    print(f"c3 full: band-edge {e}, differing {d}")
+    e, d = gu.check_static_route(choice[picks], dref, wl.tau, wl.loads0, och)
+    print(f"c3 full: sampled band-edge {e}, differing {d}")
+    # every request: a valid tau-band least-loaded pick on its own distances
+    for r in range(b.R):
+        assert gu.valid_choice(int(choice[r]), dist[r].astype(np.float64), wl.tau, wl.loads0), r
     rg = gu.host(rs.rho_g)
     assert (rg >= 1.0).all()
 
