@@ -48,18 +48,34 @@ WORKLOAD = {
     "c3": "Qwen3-30B-A3B-shaped (E=128,k=8,L=48,R=1000,mask=12,D=16,G=8)",
     "c5": "gate GEMM then path (bf16 hidden T=524288 x H=2048, E=128,k=8,L=48,R=256x2048)",
 }
-KERNEL_SOURCES = ["moe_expert_routing_top_gb300/csrc/topk_signature.cu",
-                  "moe_expert_routing_top_gb300/csrc/topk_signature_tpr.cu",
-                  "moe_expert_routing_top_gb300/csrc/common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k1_dram_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_full.txt")
 
 
-def kernel_sha() -> str:
+def sources_sha(paths) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in paths:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, config: str):
+    """DRAM bytes per launch from the committed ncu record, or None when the record is
+    missing or the kernel's sources changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        for ln in f:
+            if ln.startswith("#") or not ln.strip():
+                continue
+            tr = json.loads(ln)
+            if tr.get("kernel") == kernel and tr.get("config") == config:
+                try:
+                    if sources_sha(tr["sources"]) == tr.get("kernel_sha"):
+                        return tr.get("dram_bytes_per_launch")
+                except OSError:
+                    return None
+    return None
 
 
 def measured_peaks() -> dict:
@@ -332,12 +348,7 @@ def run_gpu(args):
 
     peaks = measured_peaks()
     achieved = alg_bytes / (k1_ms / 1e3) / 1e9
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("kernel_sha") == kernel_sha() and tr.get("config") == args.config:
-            traffic = tr.get("dram_bytes_per_launch")
+    traffic = recorded_traffic("k1_tpr_kernel", args.config) if args.requests is None else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -350,7 +361,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (logits %.1f GB per step)" % logits_gb},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "k1_kernel (moer_topk_signature)", "kernel_ms": k1_ms,
+                         "kernel": "k1_tpr_kernel (moer_topk_signature call)", "kernel_ms": k1_ms,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
             "gpu_launches": launches_per_step * args.steps,
@@ -437,7 +448,8 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "traffic": None,
+                     "traffic": (recorded_traffic("gate_topk_kernel", "c5")
+                                 if args.requests is None else None),
                      "kernel": "gate_topk_kernel (moer_gate_topk call)", "kernel_ms": call_ms,
                      "algorithmic_flops_per_launch": flops,
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"},
