@@ -14,8 +14,10 @@ __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return
 constexpr unsigned FULL = 0xffffffffu;
 
 // Workspace header: word 0 = sticky status bits (cleared by moer_ws_status),
-// word 1 = per-call validation flag of moer_topk_signature.
+// word 1 = per-call validation flag of moer_topk_signature, byte 128 = the
+// gate GEMM's tile counter (zeroed by each moer_gate_topk call).
 constexpr size_t WS_HEADER = 256;
+constexpr size_t WS_TILE_CTR = 128;
 // Capacity of moer_topk_signature_noalloc's fixed scratch for staged top-k ids.
 #define MOER_NOALLOC_IDS_BYTES (32u << 20)
 constexpr uint32_t WS_BIT_EDATA = 1u;

@@ -12,10 +12,10 @@
 //   * The weights are transposed once per call into the workspace,
 //     Wt[l*128 + e][h], so both operands are K-major.
 //   * One CTA per SM, persistent over tiles of 128 tokens x 2 layers
-//     (M = 128, N = 256 experts), K = H in blocks of 64.  Tiles are dealt
-//     round-robin, token block major, so the grid works on a few token
-//     blocks at a time: each hidden-state panel is read from HBM once and
-//     shared through L2; the 25 MB of weights stay in L2.
+//     (M = 128, N = 256 experts), K = H in blocks of 64.  Tiles, token block
+//     major, are handed out in order from a global counter, so the grid
+//     works on a few token blocks at a time: each hidden-state panel is read
+//     from HBM once and shared through L2; the 25 MB of weights stay in L2.
 //   * Warp 0 streams both operands with TMA (cp.async.bulk.tensor, 128-byte
 //     swizzle) into a 4-stage ring of 48 KB stages (mbarrier full/empty).
 //   * Warp 1 owns a 512-column TMEM allocation (two fp32 128 x 256
@@ -46,8 +46,17 @@ constexpr int GK_B_BYTES = GK_BN * GK_BK * 2;  // 32 KB
 constexpr int GK_STAGE_BYTES = GK_A_BYTES + GK_B_BYTES;
 constexpr int GK_THREADS = 6 * 32;
 constexpr int GK_TMEM_COLS = 512;
+// Tile ids travel from the producer to the MMA and epilogue warps through a
+// ring of GK_TRING slots.  The producer leads the epilogue by at most
+// GK_STAGES + 2 tiles (stages in flight, two accumulators), so a slot is never
+// rewritten before every reader has taken it.
+constexpr int GK_TRING = 16;
+static_assert(GK_TRING > GK_STAGES + 2, "tile-id ring shorter than the pipeline's lead");
 constexpr size_t GK_OFF_BAR = (size_t)GK_STAGES * GK_STAGE_BYTES;
-constexpr size_t GK_SMEM = GK_OFF_BAR + 256 + 1024;  // + barriers/slot, + 1 KB alignment slack
+// barriers (full, empty, tfull, tempty, drain, tile ids), the TMEM address, the tile-id ring
+constexpr size_t GK_BAR_BYTES = (2 * GK_STAGES + 2 + 2 + 1 + GK_TRING) * 8 + 16 + GK_TRING * 4;
+constexpr size_t GK_SMEM = GK_OFF_BAR + 512 + 1024;  // + barrier area, + 1 KB alignment slack
+static_assert(GK_BAR_BYTES <= 512, "barrier area");
 
 struct GateParams {
   CUtensorMap tmx;  // hidden [T][H] bf16, box 64 x 128, 128B swizzle
@@ -59,6 +68,7 @@ struct GateParams {
   float* logits;    // [L][T][128] or nullptr
   uint8_t* topk;    // [L][T][k]
   uint32_t* status;
+  uint32_t* tile_ctr;  // next tile to hand out (zeroed before the launch)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -189,13 +199,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
   uint64_t* tfull = empty + GK_STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tid_full = drain + 1;  // [GK_TRING]: slot j % GK_TRING holds tile j's id
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tid_full + GK_TRING);
+  int* tile_ring = reinterpret_cast<int*>(tmem_slot + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // tiles are dealt round-robin: at any moment the grid works on ~gridDim.x
-  // consecutive tiles, i.e. on few token blocks, so each hidden-state panel
-  // comes from HBM once and is shared through L2 by the CTAs on its layers
-  const int64_t t0 = blockIdx.x, tstep = gridDim.x;
-  const int64_t t1 = p.ntiles;
+  // Tiles are handed out in order from one global counter, so at any moment
+  // the grid works on ~gridDim.x consecutive tiles, i.e. on few token blocks:
+  // each hidden-state panel comes from HBM once and is shared through L2 by
+  // the CTAs on its layers, however unevenly the CTAs progress.
   const int nkb = p.H / GK_BK;
 
   if (threadIdx.x == 0) {
@@ -208,6 +219,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
       mbar_init(&tempty[a], 4);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < GK_TRING; ++i) mbar_init(&tid_full[i], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -225,8 +237,13 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
     if (lane == 0) {
       int64_t g = 0;
       bool ok = true;
-      for (int64_t t = t0; t < t1 && ok; t += tstep) {
-        const int mt = (int)(t / p.npairs), pair = (int)(t - (int64_t)mt * p.npairs);
+      for (int64_t j = 0;; ++j) {
+        int t = ok ? (int)atomicAdd(p.tile_ctr, 1u) : -1;
+        if (t >= p.ntiles) t = -1;
+        tile_ring[j % GK_TRING] = t;
+        mbar_arrive(&tid_full[j % GK_TRING]);  // release: the id is visible to the waiters
+        if (t < 0) break;
+        const int mt = t / p.npairs, pair = t - mt * p.npairs;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int s = (int)(g % GK_STAGES);
           if (g >= GK_STAGES && !mbar_wait(&empty[s], (uint32_t)((g / GK_STAGES - 1) & 1), p.status)) {
@@ -250,8 +267,12 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
     if (lane == 0) {
       int64_t g = 0;
       bool ok = true;
-      int64_t j = 0;
-      for (int64_t t = t0; t < t1 && ok; t += tstep, ++j) {
+      for (int64_t j = 0; ok; ++j) {
+        if (!mbar_wait(&tid_full[j % GK_TRING], (uint32_t)((j / GK_TRING) & 1), p.status)) {
+          ok = false;
+          break;
+        }
+        if (tile_ring[j % GK_TRING] < 0) break;
         const int a = (int)(j & 1);
         if (j >= 2 && !mbar_wait(&tempty[a], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
           ok = false;
@@ -283,17 +304,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_c
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;   // token row within the tile
-    bool dead = false;
-    int64_t j = 0;
-    for (int64_t t = t0; t < t1; t += tstep, ++j) {
+    for (int64_t j = 0;; ++j) {
+      if (!mbar_wait(&tid_full[j % GK_TRING], (uint32_t)((j / GK_TRING) & 1), p.status)) break;
+      const int t = tile_ring[j % GK_TRING];
+      if (t < 0) break;
       const int a = (int)(j & 1);
-      if (dead) continue;
-      if (!mbar_wait(&tfull[a], (uint32_t)((j >> 1) & 1), p.status)) {
-        dead = true;
-        continue;
-      }
+      if (!mbar_wait(&tfull[a], (uint32_t)((j >> 1) & 1), p.status)) break;
       tc_fence_after();
-      const int mt = (int)(t / p.npairs), pair = (int)(t - (int64_t)mt * p.npairs);
+      const int mt = t / p.npairs, pair = t - mt * p.npairs;
       const int64_t tok = (int64_t)mt * GK_BM + row;
 #pragma unroll 1
       for (int hl = 0; hl < 2; ++hl) {
@@ -482,9 +500,12 @@ moer_status gate_topk_launch(const moer_dims* d, const uint16_t* hidden, int64_t
   p.logits = logits;
   p.topk = topk;
   p.status = reinterpret_cast<uint32_t*>(ws);
+  p.tile_ctr = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + WS_TILE_CTR);
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
   const int grid = (int)min64(p.ntiles, sms);
+  if (p.ntiles + grid >= (int64_t(1) << 31)) return MOER_ERANGE;
+  if (cudaMemsetAsync(p.tile_ctr, 0, sizeof(uint32_t), st) != cudaSuccess) return MOER_ECUDA;
   const cudaError_t e = d->k == 8 ? gate_launch_k<8>(p, grid, st) : gate_launch_k<6>(p, grid, st);
   return e == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
