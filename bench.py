@@ -335,9 +335,10 @@ def run_gpu(args):
     # end-to-end through the public API: pinned host logits -> device, step, results -> host
     e2e = run_e2e(args, wl, b, bd, rs, logits, stream, device, dist) if args.e2e else None
 
-    cpu = None
+    cpu = cpu1 = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_requests)
+        cpu1 = cpu_baseline(wl, args.cpu_requests)
+        cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests)
 
     logits_gb = logits.numel() * 4 / 1e9
     gate = None
@@ -361,6 +362,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (logits %.1f GB per step)" % logits_gb},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "frac_of_8tbs": achieved / 8000.0,
                          "kernel": "k1_tpr_kernel (moer_topk_signature call)", "kernel_ms": k1_ms,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
@@ -368,6 +370,7 @@ def run_gpu(args):
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "cpu_baseline_1core": cpu1,
         }
         if gate is not None:
             line["gate_path"] = {key: gate[key] for key in
@@ -465,9 +468,11 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
 def run_gate_main(args, ws, rank, local, device, dist, stream):
     import gen
     g = measure_gate(args, device, dist, stream, args.steps, with_e2e=args.e2e)
-    cpu = None
+    cpu = cpu1 = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = gate_cpu_baseline(gen.make_workload("c5"), args.cpu_tokens)
+        wl5 = gen.make_workload("c5")
+        cpu1 = gate_cpu_baseline(wl5, args.cpu_tokens)
+        cpu = gate_cpu_baseline_all_cores(wl5, args.cpu_tokens)
     if rank == 0:
         line = {
             "metric": METRIC, "value": g["value"], "unit": UNIT, "n_gpus": ws,
@@ -478,7 +483,7 @@ def run_gate_main(args, ws, rank, local, device, dist, stream):
                        "requests": g["requests"], "kv_blocks": g["kv_blocks"],
                        "parallelism": f"replicas x{ws}", "l2": g["l2"]},
             "roofline": g["roofline"], "gpu_launches": g["gpu_launches"], "clocks": g["clocks"],
-            "e2e": g.get("e2e"), "cpu_baseline": cpu,
+            "e2e": g.get("e2e"), "cpu_baseline": cpu, "cpu_baseline_1core": cpu1,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -556,6 +561,53 @@ def gate_cpu_baseline(wl, ntok):
                       f"layers, one pass, {dt:.1f} s, single thread"}
 
 
+def _gate_cpu_worker(t0_tok, ntok, barrier, results):
+    import gen
+    import oracle
+    orc = oracle.get()
+    wl = gen.make_workload("c5")
+    H = wl.hidden_dim
+    x = gen.host_hidden(wl.seed, t0_tok, ntok, H)
+    w = gen.host_wgate(wl.seed, wl.L, H, wl.E, wl.wgate_scale)
+    barrier.wait()
+    t0 = time.perf_counter()
+    orc.topk(orc.gate_logits(x, w), wl.k)
+    results.put((ntok, time.perf_counter() - t0))
+
+
+def gate_cpu_baseline_all_cores(wl, ntok_per_core):
+    """gate_cpu_baseline on every host core: token ranges over spawned processes, timed
+    from a common start barrier to the last worker's end."""
+    import multiprocessing as mp
+    import oracle
+    oracle.get()
+    try:
+        ncores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        ncores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(ncores + 1)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_gate_cpu_worker,
+                         args=(i * ntok_per_core, ntok_per_core, barrier, results))
+             for i in range(ncores)]
+    for pr in procs:
+        pr.start()
+    try:
+        barrier.wait(timeout=600)
+        t0 = time.perf_counter()
+        got = [results.get(timeout=600) for _ in procs]
+        wall = time.perf_counter() - t0
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+    tokens = sum(t for t, _ in got)
+    return {"value": wl.L * tokens / wall, "unit": UNIT, "cores": ncores, "kind": "oracle",
+            "sample": f"gate logits (fp64 sums) + top-k of the first {tokens} tokens x {wl.L} "
+                      f"layers, {ntok_per_core} per process on {ncores} host cores, one pass, "
+                      f"{wall:.1f} s wall"}
+
+
 def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
     """Same metric through the public API with host buffers: per step the logits go
     host -> device in request chunks on a copy stream, overlapped with the path on
@@ -625,6 +677,56 @@ def cpu_baseline(wl, nreq):
     return {"value": wl.L * b.T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {nreq} requests ({b.T} tokens x {wl.L} layers), one pass, "
                       f"{dt:.1f} s, single thread"}
+
+
+def _cpu_worker(cfg, r0, r1, barrier, results):
+    """One host core's share of the all-cores oracle run: its requests' inputs are made
+    first (untimed), then every worker starts the oracle pass at the same barrier."""
+    import gen
+    import oracle
+    orc = oracle.get()
+    wl = gen.make_workload(cfg)
+    b = wl.batch(r0, r1)
+    logits = gen.host_logits(wl, b.tok_key, b.tok_dom)
+    barrier.wait()
+    t0 = time.perf_counter()
+    oracle_pass(orc, wl, b, logits)
+    results.put((b.T, time.perf_counter() - t0))
+
+
+def cpu_baseline_all_cores(cfg, wl, nreq_per_core):
+    """The oracle on every host core: request ranges split over spawned processes (the
+    oracle itself is single-threaded and unchanged), timed from a common start barrier to
+    the last worker's end."""
+    import multiprocessing as mp
+    import oracle
+    oracle.get()  # built once here, so the workers only load it
+    try:
+        ncores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        ncores = os.cpu_count() or 1
+    ncores = max(1, min(ncores, wl.R // max(nreq_per_core, 1)))
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(ncores + 1)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_cpu_worker,
+                         args=(cfg, i * nreq_per_core, (i + 1) * nreq_per_core, barrier, results))
+             for i in range(ncores)]
+    for pr in procs:
+        pr.start()
+    try:
+        barrier.wait(timeout=600)
+        t0 = time.perf_counter()
+        got = [results.get(timeout=600) for _ in procs]
+        wall = time.perf_counter() - t0
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+    tokens = sum(t for t, _ in got)
+    return {"value": wl.L * tokens / wall, "unit": UNIT, "cores": ncores, "kind": "oracle",
+            "sample": f"first {ncores * nreq_per_core} requests ({tokens} tokens x {wl.L} layers), "
+                      f"{nreq_per_core} per process on {ncores} host cores, one pass, "
+                      f"{wall:.1f} s wall"}
 
 
 def main(argv=None):
