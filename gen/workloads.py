@@ -337,3 +337,22 @@ def make_custom(E: int, k: int, L: int, lengths, *, B: int = 16, mask=None, ndom
                     bias_mask=bias_mask, mask=mask, D=D, tau=tau, centroids=centroids,
                     loads0=loads0, live=live, G=G, group_of=group_of, idf=idf,
                     slot_of_block=slot_of_block, nslots=nslots)
+
+
+def calib_signatures(N: int, dim: int, ndom: int = 4, seed: int = 0x4B4D):
+    """Seeded stand-in for the signatures of N calibration prompts (input construction,
+    not the method): each prompt draws a domain; each domain has a nonnegative profile
+    (1, or 3 on a random 3/16 of the coordinates); counts are Poisson around 4x the
+    profile; each row is scaled to unit L2 norm.  Returns (fp32 [N][dim], domain [N])."""
+    rs = np.random.RandomState(seed & 0xFFFFFFFF)
+    prof = 1.0 + 2.0 * (rs.random_sample((ndom, dim)) < 3.0 / 16.0)
+    dom = rs.randint(0, ndom, size=N)
+    counts = rs.poisson(4.0 * prof[dom]).astype(np.float64)
+    counts[counts.sum(axis=1) == 0, 0] = 1.0
+    sig = counts / np.linalg.norm(counts, axis=1, keepdims=True)
+    return sig.astype(np.float32), dom.astype(np.int32)
+
+
+def kmeans_seed_rows(N: int, D: int, seed: int = 0x5EED) -> np.ndarray:
+    """D distinct row indices, the initial centroids of a K-means fit (seeded choice)."""
+    return np.random.RandomState(seed & 0xFFFFFFFF).choice(N, size=D, replace=False)

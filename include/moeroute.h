@@ -229,6 +229,40 @@ MOER_API moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, 
                                     float* logits, uint8_t* topk, uint8_t* blk_cnt, int32_t* affinity,
                                     void* ws, size_t ws_bytes, moer_stream_t stream);
 
+/* Calibration (not on the per-request path): balanced K-means of N
+ * calibration signatures into D decoder centroids.  [ELDR] section "Key idea
+ * / structure / operation": offline, the calibration prompts' signatures are
+ * split into D clusters, one per decode worker, by K-means with a balance
+ * constraint solved by the Hungarian method, so that locality alone cannot
+ * pile requests onto one decoder.
+ *   Cluster d holds floor(N/D) points, plus one for d < N mod D.  Starting
+ *   from init_centroids, each step assigns the points to clusters at the least
+ *   total squared Euclidean distance under those sizes (exactly: a min-cost
+ *   transportation problem, solved in fp64), then moves every centroid to the
+ *   mean of its points (no renormalisation).  The fit stops after the first
+ *   step whose assignment equals the previous one (no update follows it) or
+ *   after max_iter steps.
+ * Limits: 1 <= D <= 32, D <= N <= 2^20, 1 <= dim <= 65536, 1 <= max_iter <= 1000.
+ * sig        [N][dim] fp32, device, finite (e.g. moer_route's signatures).
+ * init_centroids [D][dim] fp32, device (the caller's seeding).
+ * centroids  [D][dim] fp32 out (usable as moer_route's centroids).
+ * assign     [N] int32 out: the cluster of each signature.
+ * info       [3] int32 out or NULL: assignment steps run, negative cycles
+ *            cancelled, 1 if a step stopped at its cancellation bound (then
+ *            the status word also records MOER_ETIMEOUT).
+ * objective  [1] fp64 out or NULL: sum of squared distances of the points to
+ *            their returned centroids.
+ * ws         at least moer_kmeans_workspace_bytes(N, dim, D) bytes, 256-byte
+ *            aligned (status word, fp64 distances and centroids, previous
+ *            assignment).  Launches 3 * max_iter + 3 kernels; steps after
+ *            convergence return at once.
+ */
+MOER_API size_t moer_kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D);
+MOER_API moer_status moer_kmeans_balanced(const float* sig, int32_t N, int32_t dim, int32_t D,
+                                          const float* init_centroids, int32_t max_iter, float* centroids,
+                                          int32_t* assign, int32_t* info, double* objective, void* ws,
+                                          size_t ws_bytes, moer_stream_t stream);
+
 /* Calibration helper (not on the per-request path): smoothed idf over R
  * calibration requests.  [ELDR] section "Key idea / structure / operation"
  * (idf reweighting fit offline on calibration prompts; formula not printed).

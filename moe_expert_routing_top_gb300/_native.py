@@ -58,6 +58,8 @@ def _load():
         "moer_idf_fit": ([dp, vp, i32, vp, vp], ctypes.c_int),
         "moer_gate_workspace_bytes": ([dp, i32], sz),
         "moer_gate_topk": ([dp, vp, i64, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "moer_kmeans_workspace_bytes": ([i32, i32, i32], sz),
+        "moer_kmeans_balanced": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_ws_status": ([vp, vp], ctypes.c_int),
         "moer_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "moer_version": ([], ctypes.c_int32),
@@ -72,7 +74,8 @@ def _load():
 LIB = _load()
 EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_noalloc",
            "moer_block_stitch", "moer_affinity_load",
-           "moer_route", "moer_idf_fit", "moer_gate_workspace_bytes", "moer_gate_topk", "moer_ws_status",
+           "moer_route", "moer_idf_fit", "moer_gate_workspace_bytes", "moer_gate_topk",
+           "moer_kmeans_workspace_bytes", "moer_kmeans_balanced", "moer_ws_status",
            "moer_status_str", "moer_version")
 
 
@@ -142,6 +145,17 @@ def moer_route(dims, req_cnt, R, idf, centroids, D, tau, loads, live, sig, dist,
 def moer_idf_fit(dims, req_cnt, R, idf, stream=None) -> None:
     _check("moer_idf_fit", LIB.moer_idf_fit(ctypes.byref(dims), _ptr(req_cnt), int(R), _ptr(idf),
                                             _stream(stream)))
+
+
+def moer_kmeans_workspace_bytes(N: int, dim: int, D: int) -> int:
+    return int(LIB.moer_kmeans_workspace_bytes(int(N), int(dim), int(D)))
+
+
+def moer_kmeans_balanced(sig, N, dim, D, init_centroids, max_iter, centroids, assign, info, objective,
+                         ws, ws_bytes, stream=None) -> None:
+    _check("moer_kmeans_balanced", LIB.moer_kmeans_balanced(
+        _ptr(sig), int(N), int(dim), int(D), _ptr(init_centroids), int(max_iter), _ptr(centroids),
+        _ptr(assign), _ptr(info), _ptr(objective), _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
 def moer_gate_workspace_bytes(dims, H: int) -> int:

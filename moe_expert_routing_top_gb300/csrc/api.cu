@@ -6,6 +6,10 @@
 #include "common.cuh"
 
 namespace moer {
+size_t kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D);
+moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, const float* init, int32_t max_iter,
+                          float* centroids, int32_t* assign, int32_t* info, double* objective, void* ws,
+                          cudaStream_t st);
 size_t k1_scratch_bytes(const moer_dims* d, int64_t T);
 moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64_t T,
                                   const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
@@ -225,6 +229,28 @@ moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, int64_t T
   if (hist)
     s = block_counts_launch(d, topk, false, T, blk_tab, nblk, blk_cnt, reinterpret_cast<uint32_t*>(ws), st);
   return s;
+}
+
+size_t moer_kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D) {
+  if (N < 1 || dim < 1 || D < 1) return WS_HEADER;
+  return moer::kmeans_workspace_bytes(N, dim, D);
+}
+
+moer_status moer_kmeans_balanced(const float* sig, int32_t N, int32_t dim, int32_t D, const float* init_centroids,
+                                 int32_t max_iter, float* centroids, int32_t* assign, int32_t* info,
+                                 double* objective, void* ws, size_t ws_bytes, moer_stream_t stream) {
+  if (D < 1 || D > 32 || N < D || N > (1 << 20) || dim < 1 || dim > 65536) return MOER_ERANGE;
+  if (max_iter < 1 || max_iter > 1000) return MOER_ERANGE;
+  if (sig == nullptr || init_centroids == nullptr || centroids == nullptr || assign == nullptr)
+    return MOER_EINVAL;
+  if (!aligned(sig, 4) || !aligned(init_centroids, 4) || !aligned(centroids, 4) || !aligned(assign, 4))
+    return MOER_EINVAL;
+  if ((info != nullptr && !aligned(info, 4)) || (objective != nullptr && !aligned(objective, 8)))
+    return MOER_EINVAL;
+  if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
+  if (ws_bytes < moer_kmeans_workspace_bytes(N, dim, D)) return MOER_ENOMEM;
+  return moer::kmeans_launch(sig, N, dim, D, init_centroids, max_iter, centroids, assign, info, objective, ws,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 moer_status moer_ws_status(void* ws, moer_stream_t stream) {
