@@ -282,6 +282,10 @@ def run_gpu(args):
     sh = stream.cuda_stream
     if args.config == "c5":
         return run_gate_main(args, ws, rank, local, device, dist, stream)
+    if args.kmeans_only:
+        if rank == 0:
+            print(json.dumps({"kmeans_fit": measure_kmeans(args, device, stream, rank)}), flush=True)
+        return 0
 
     wl = gen.make_workload(args.config, R=args.requests)
     b = wl.batch()
@@ -341,6 +345,7 @@ def run_gpu(args):
         cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests)
 
     logits_gb = logits.numel() * 4 / 1e9
+    kmeans = measure_kmeans(args, device, stream, rank) if args.kmeans else None
     gate = None
     if args.gate:
         del logits, rs
@@ -372,6 +377,8 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "cpu_baseline_1core": cpu1,
         }
+        if kmeans is not None:
+            line["kmeans_fit"] = kmeans
         if gate is not None:
             line["gate_path"] = {key: gate[key] for key in
                                  ("workload", "value", "unit", "ms_per_step", "steps", "roofline",
@@ -608,6 +615,55 @@ def gate_cpu_baseline_all_cores(wl, ntok_per_core):
                       f"{wall:.1f} s wall"}
 
 
+def measure_kmeans(args, device, stream, rank):
+    """The calibration fit (balanced K-means of 1,000 signatures of 12 x 128 dims into 16
+    decoders), timed with CUDA events after one untimed fit, beside the oracle's fit of
+    the same inputs on one host core."""
+    import torch
+    import gen
+    from moe_expert_routing_top_gb300 import _native as nat
+    N, dim, D, max_iter = 1000, 12 * 128, 16, 100
+    S, _ = gen.calib_signatures(N, dim, ndom=24)
+    C0 = S[gen.kmeans_seed_rows(N, D)]
+    ds = torch.from_numpy(S).to(device)
+    dc0 = torch.from_numpy(np.ascontiguousarray(C0)).to(device)
+    cent = torch.empty((D, dim), dtype=torch.float32, device=device)
+    assign = torch.empty(N, dtype=torch.int32, device=device)
+    info = torch.zeros(3, dtype=torch.int32, device=device)
+    obj = torch.zeros(1, dtype=torch.float64, device=device)
+    wsb = nat.moer_kmeans_workspace_bytes(N, dim, D)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+
+    def fit():
+        nat.moer_kmeans_balanced(ds, N, dim, D, dc0, max_iter, cent, assign, info, obj, ws, wsb,
+                                 stream)
+
+    fit()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(args.kmeans_reps, 1)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fit()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if nat.moer_ws_status(ws, stream) != 0:
+        raise RuntimeError("device-side status after the K-means fit is not OK")
+    inf = info.cpu().tolist()
+    out = {"workload": f"balanced K-means, N={N} signatures, dim={dim}, D={D}, max_iter={max_iter}",
+           "ms": statistics.median(times), "steps": inf[0], "cycles_cancelled": inf[1],
+           "launches": 3 * max_iter + 3, "objective": float(obj.item())}
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import kmeans as km
+        t0 = time.perf_counter()
+        _, a_o, steps_o, obj_o = km.balanced_kmeans(S, C0.astype(np.float64), max_iter)
+        out["cpu_baseline"] = {"ms": (time.perf_counter() - t0) * 1e3, "cores": 1, "kind": "oracle",
+                               "sample": "the same fit (scipy Hungarian assignment per step)"}
+        out["matches_oracle"] = bool(np.array_equal(assign.cpu().numpy(), a_o) and steps_o == inf[0])
+    return out
+
+
 def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
     """Same metric through the public API with host buffers: per step the logits go
     host -> device in request chunks on a copy stream, overlapped with the path on
@@ -751,6 +807,12 @@ def main(argv=None):
                     help="also measure the gate path (moer_gate_topk first) into gate_path")
     ap.add_argument("--no-gate", dest="gate", action="store_false")
     ap.add_argument("--gate-steps", type=int, default=10)
+    ap.add_argument("--kmeans", dest="kmeans", action="store_true", default=True,
+                    help="also time the calibration fit (balanced K-means) into kmeans_fit")
+    ap.add_argument("--no-kmeans", dest="kmeans", action="store_false")
+    ap.add_argument("--kmeans-reps", type=int, default=5)
+    ap.add_argument("--kmeans-only", action="store_true",
+                    help="time only the calibration fit (one JSON object, for profiling)")
     ap.add_argument("--cpu-tokens", type=int, default=512,
                     help="gate path: tokens in the oracle's CPU-baseline sample")
     args = ap.parse_args(argv)

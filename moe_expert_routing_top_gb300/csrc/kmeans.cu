@@ -20,10 +20,11 @@
 //     min over points p in u of cost[p][v] - cost[p][u] (moving p from u to v).
 //     A cycle moves one point out of and one into every cluster on it, so the
 //     sizes stay put; with no negative cycle left the assignment is optimal
-//     (min-cost flow optimality).  Edge minima come from shared-memory 64-bit
-//     atomicMin on order-preserving keys; one warp runs Bellman-Ford over the
-//     D <= 32 nodes and extracts a cycle from the predecessor graph.  Later
-//     steps start next to the optimum, so few cycles remain.
+//     (min-cost flow optimality).  Edge minima are scans of per-cluster member
+//     lists (a few threads per edge, shuffle-reduced).  Each pass first applies
+//     every disjoint negative 2-cycle (pairwise swap) it finds; only when none
+//     is left does one warp run Bellman-Ford over the D <= 32 nodes and cancel
+//     a longer cycle read off the predecessor graph.
 //   * Means: one thread per (centroid, coordinate), points in index order.
 //   * Every kernel of a step returns at once after convergence, so the host
 //     launches max_iter steps without reading anything back.
@@ -44,7 +45,7 @@ struct KmState {
 };
 
 struct KmLayout {
-  size_t state, cost, cent, prev, total;
+  size_t state, cost, cent, prev, mem, pos, total;
 };
 
 static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
@@ -54,21 +55,13 @@ static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
   l.cost = l.state + 256;
   l.cent = l.cost + r256((size_t)N * D * sizeof(double));
   l.prev = l.cent + r256((size_t)D * dim * sizeof(double));
-  l.total = l.prev + r256((size_t)N * sizeof(int32_t));
+  l.mem = l.prev + r256((size_t)N * sizeof(int32_t));
+  l.pos = l.mem + r256((size_t)N * sizeof(int32_t));
+  l.total = l.pos + r256((size_t)N * sizeof(int32_t));
   return l;
 }
 
 __device__ __forceinline__ int km_cap(int d, int N, int D) { return N / D + (d < N % D ? 1 : 0); }
-
-// Order-preserving map of a double onto an unsigned 64-bit key.
-__device__ __forceinline__ unsigned long long dkey(double x) {
-  const unsigned long long b = (unsigned long long)__double_as_longlong(x);
-  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
-}
-__device__ __forceinline__ double dval(unsigned long long k) {
-  const unsigned long long b = (k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
-  return __longlong_as_double((long long)b);
-}
 
 __global__ void km_init_kernel(const float* __restrict__ init, double* __restrict__ cent, int64_t n) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -95,34 +88,53 @@ __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ 
   }
 }
 
+// Lexicographic (value, point) minimum, for edge minima that do not depend on
+// the order in which the points are visited.
+__device__ __forceinline__ void vmin(double& v, int& p, double v2, int p2) {
+  if (v2 < v || (v2 == v && p2 < p)) {
+    v = v2;
+    p = p2;
+  }
+}
+
 // One balanced assignment step (single CTA).  `a` holds the result; `prev` the
-// previous step's assignment.
+// previous step's assignment; `mem` / `pos` the per-cluster member lists
+// (cluster u's members at mem[off_u .. off_u + cap_u), pos[p] = p's slot).
 __global__ void __launch_bounds__(KM_THREADS, 1)
     km_assign_kernel(const double* __restrict__ cost, int32_t N, int32_t D, int32_t* __restrict__ a,
-                     int32_t* __restrict__ prev, KmState* state, int32_t max_cancel, uint32_t* status) {
-  __shared__ unsigned long long wkey[KM_MAXD * KM_MAXD];
+                     int32_t* __restrict__ prev, int32_t* __restrict__ mem, int32_t* __restrict__ pos,
+                     KmState* state, int32_t max_pass, uint32_t* status) {
+  __shared__ double wval[KM_MAXD * KM_MAXD];
   __shared__ int widx[KM_MAXD * KM_MAXD];
-  __shared__ int cnt[KM_MAXD];
-  __shared__ int cyc[KM_MAXD + 1];
-  __shared__ int ncyc;
+  __shared__ int off[KM_MAXD + 1], fill[KM_MAXD];
+  __shared__ int mv_pt[KM_MAXD], mv_from[KM_MAXD], mv_to[KM_MAXD], freed[KM_MAXD];
+  __shared__ int nmv;
   __shared__ int s_pred[KM_MAXD];
   __shared__ double red[KM_THREADS / 32];
   __shared__ int s_first;
   if (state->converged) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) s_first = (state->steps == 0);
+  if (tid == 0) {
+    s_first = (state->steps == 0);
+    off[0] = 0;
+    for (int d = 0; d < D; ++d) {
+      off[d + 1] = off[d] + km_cap(d, N, D);
+      fill[d] = 0;
+    }
+  }
   __syncthreads();
   const bool first = s_first != 0;
 
   // 1. a feasible start: the previous assignment, or greedy nearest-with-room
   if (first) {
     if (tid == 0) {
+      int cnt[KM_MAXD];
       for (int d = 0; d < D; ++d) cnt[d] = 0;
       for (int i = 0; i < N; ++i) {
         int best = -1;
         double bc = 0.0;
         for (int d = 0; d < D; ++d) {
-          if (cnt[d] >= km_cap(d, N, D)) continue;
+          if (cnt[d] >= off[d + 1] - off[d]) continue;
           const double c = cost[(size_t)i * D + d];
           if (best < 0 || c < bc) {
             best = d;
@@ -136,7 +148,15 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   } else {
     for (int i = tid; i < N; i += KM_THREADS) a[i] = prev[i];
   }
-  // 2. tolerance: cycles must gain more than 1e-12 of the largest cost
+  __syncthreads();
+  // member lists (slot order within a cluster does not matter)
+  for (int i = tid; i < N; i += KM_THREADS) {
+    const int u = a[i];
+    const int slot = off[u] + atomicAdd(&fill[u], 1);
+    mem[slot] = i;
+    pos[i] = slot;
+  }
+  // 2. tolerance: a move must gain more than 1e-12 of the largest cost
   double mx = 0.0;
   for (int64_t q = tid; q < (int64_t)N * D; q += KM_THREADS) mx = fmax(mx, fabs(cost[q]));
 #pragma unroll
@@ -152,32 +172,57 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   __syncthreads();
   const double eps = 1e-12 * red[0] + 1e-300;
 
-  // 3. cancel negative cycles
+  // threads per edge (a power of two <= 32, so an edge's threads share a warp)
+  const int npairs = D * D;
+  int tpp = 32;
+  while (tpp > 1 && tpp * npairs > KM_THREADS) tpp >>= 1;
+
+  // 3. improve until no negative cycle is left
   int done = 0;
-  for (int it = 0; it < max_cancel; ++it) {
-    for (int q = tid; q < D * D; q += KM_THREADS) {
-      wkey[q] = ~0ull;
-      widx[q] = INT_MAX;
+  for (int pass = 0; pass < max_pass; ++pass) {
+    // edge minima: W[u][v] = min over members p of u of cost[p][v] - cost[p][u]
+    {
+      const int q = tid / tpp, sub = tid % tpp;
+      const int u = q / D, v = q - (q / D) * D;
+      double best = INFINITY;
+      int bp = INT_MAX;
+      if (q < npairs && u != v) {
+        for (int k = off[u] + sub; k < off[u + 1]; k += tpp) {
+          const int p = mem[k];
+          vmin(best, bp, cost[(size_t)p * D + v] - cost[(size_t)p * D + u], p);
+        }
+      }
+      for (int o = tpp >> 1; o > 0; o >>= 1) {
+        const double ob = __shfl_xor_sync(FULL, best, o);
+        const int op = __shfl_xor_sync(FULL, bp, o);
+        vmin(best, bp, ob, op);
+      }
+      if (q < npairs && sub == 0) {
+        wval[q] = best;
+        widx[q] = bp;
+      }
     }
     __syncthreads();
-    for (int p = tid; p < N; p += KM_THREADS) {
-      const int u = a[p];
-      const double cu = cost[(size_t)p * D + u];
-      for (int v = 0; v < D; ++v)
-        if (v != u) atomicMin(&wkey[u * D + v], dkey(cost[(size_t)p * D + v] - cu));
+    // disjoint pairwise swaps first (negative 2-cycles), first fit in (u, v) order
+    if (tid == 0) {
+      unsigned used = 0u;
+      int n = 0;
+      for (int u = 0; u < D; ++u)
+        for (int v = u + 1; v < D; ++v) {
+          if ((used >> u) & 1u || (used >> v) & 1u) continue;
+          if (wval[u * D + v] + wval[v * D + u] < -eps) {
+            used |= (1u << u) | (1u << v);
+            mv_pt[n] = widx[u * D + v], mv_from[n] = u, mv_to[n] = v, ++n;
+            mv_pt[n] = widx[v * D + u], mv_from[n] = v, mv_to[n] = u, ++n;
+          }
+        }
+      nmv = n;
     }
     __syncthreads();
-    for (int p = tid; p < N; p += KM_THREADS) {
-      const int u = a[p];
-      const double cu = cost[(size_t)p * D + u];
-      for (int v = 0; v < D; ++v)
-        if (v != u && dkey(cost[(size_t)p * D + v] - cu) == wkey[u * D + v]) atomicMin(&widx[u * D + v], p);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // Bellman-Ford from a virtual source (0-weight edges to every node);
-      // lane v owns node v.  Rounds are synchronous: every lane reads the old
-      // distances through shuffles that all 32 lanes execute.
+    if (nmv == 0 && warp == 0) {
+      // no swap left: Bellman-Ford from a virtual source (0-weight edges to
+      // every node) for a longer negative cycle; lane v owns node v, rounds
+      // are synchronous (old distances through shuffles all lanes execute)
       double dist = 0.0;
       int pred = -1;
       for (int round = 0; round < 2 * (D + 1); ++round) {
@@ -186,18 +231,17 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
         for (int u = 0; u < D; ++u) {
           const double du = __shfl_sync(FULL, dist, u);
           if (lane < D && u != lane) {
-            const unsigned long long k = wkey[u * D + lane];
-            if (k != ~0ull) {
-              const double cand = du + dval(k);
-              if (cand < best) {
-                best = cand;
-                from = u;
-              }
+            const double cand = du + wval[u * D + lane];
+            if (cand < best) {
+              best = cand;
+              from = u;
             }
           }
         }
+        const bool changed = best < dist;
         dist = best;
         pred = from;
+        if (!__any_sync(FULL, changed)) break;
       }
       if (lane < D) s_pred[lane] = pred;
       __syncwarp();
@@ -212,39 +256,39 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
       }
       const unsigned on = __ballot_sync(FULL, alive);
       const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
-      if (lane == 0) {
-        ncyc = 0;
-        if (on) {
-          // nodes listed backwards (cyc[q + 1] is the predecessor of cyc[q])
-          int y = start, n = 0;
-          double w = 0.0;
-          bool ok = true;
-          do {
-            const int py = s_pred[y];
-            if (py < 0 || widx[py * D + y] >= N) {  // cannot happen on a cycle; checked anyway
-              ok = false;
-              break;
-            }
-            cyc[n++] = y;
-            w += dval(wkey[py * D + y]);
-            y = py;
-          } while (y != start && n <= D);
-          if (ok && y == start && w < -eps) ncyc = n;
-        }
+      if (lane == 0 && on) {
+        // walk the cycle backwards (edges pred[y] -> y)
+        int y = start, n = 0;
+        double w = 0.0;
+        bool ok = true;
+        do {
+          const int py = s_pred[y];
+          if (py < 0 || widx[py * D + y] >= N) {  // cannot happen on a cycle; checked anyway
+            ok = false;
+            break;
+          }
+          mv_pt[n] = widx[py * D + y], mv_from[n] = py, mv_to[n] = y, ++n;
+          w += wval[py * D + y];
+          y = py;
+        } while (y != start && n < D);
+        nmv = (ok && y == start && w < -eps) ? n : 0;
       }
     }
     __syncthreads();
-    if (ncyc == 0) {
+    if (nmv == 0) {
       done = 1;
       break;
     }
     if (tid == 0) {
-      // move, along each edge pred[y] -> y, the point that realises it
-      // (points are distinct: each leaves a different cluster)
-      for (int q = 0; q < ncyc; ++q) {
-        const int y = cyc[q];
-        const int py = cyc[(q + 1) % ncyc];  // cycle listed backwards: cyc[q+1] = pred of cyc[q]
-        a[widx[py * D + y]] = y;
+      // every cluster on the moves loses one point and gains one: the incoming
+      // point takes the outgoing point's slot (points are distinct: each move
+      // leaves a different cluster)
+      for (int m = 0; m < nmv; ++m) freed[mv_from[m]] = pos[mv_pt[m]];
+      for (int m = 0; m < nmv; ++m) {
+        const int pt = mv_pt[m], slot = freed[mv_to[m]];
+        a[pt] = mv_to[m];
+        mem[slot] = pt;
+        pos[pt] = slot;
       }
       state->cancelled += 1;
     }
@@ -324,6 +368,8 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
   double* cost = reinterpret_cast<double*>(w + l.cost);
   double* cent = reinterpret_cast<double*>(w + l.cent);
   int32_t* prev = reinterpret_cast<int32_t*>(w + l.prev);
+  int32_t* mem = reinterpret_cast<int32_t*>(w + l.mem);
+  int32_t* pos = reinterpret_cast<int32_t*>(w + l.pos);
   uint32_t* status = reinterpret_cast<uint32_t*>(w);
   if (cudaMemsetAsync(state, 0, sizeof(KmState), st) != cudaSuccess) return MOER_ECUDA;
   const int64_t nc = (int64_t)D * dim;
@@ -332,7 +378,7 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
   const dim3 ug((unsigned)((dim + 255) / 256), (unsigned)D);
   for (int it = 0; it < max_iter; ++it) {
     km_cost_kernel<<<(unsigned)N, 256, 0, st>>>(sig, dim, D, cent, cost, state, 0);
-    km_assign_kernel<<<1, KM_THREADS, 0, st>>>(cost, N, D, assign, prev, state, max_cancel, status);
+    km_assign_kernel<<<1, KM_THREADS, 0, st>>>(cost, N, D, assign, prev, mem, pos, state, max_cancel, status);
     km_update_kernel<<<ug, 256, 0, st>>>(sig, N, dim, D, assign, cent, state);
   }
   km_cost_kernel<<<(unsigned)N, 256, 0, st>>>(sig, dim, D, cent, cost, state, 1);
