@@ -345,6 +345,18 @@ def run_gpu(args):
         cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests)
 
     logits_gb = logits.numel() * 4 / 1e9
+    # GRACE replication plan from this step's loads (per layer, after moer_affinity_load)
+    rp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(10)]
+    for a, z in rp_ev:
+        a.record(stream)
+        rs.replication_plan()
+        z.record(stream)
+    torch.cuda.synchronize()
+    if rs.status() != 0:
+        raise RuntimeError("device-side status after the replication plan is not OK")
+    replication = {"ms": statistics.median(x.elapsed_time(y) for x, y in rp_ev), "layers": wl.L,
+                   "groups": wl.G, "replicas_per_layer": rs.n_rep.cpu().tolist()}
     kmeans = measure_kmeans(args, device, stream, rank) if args.kmeans else None
     gate = None
     if args.gate:
@@ -377,6 +389,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "cpu_baseline_1core": cpu1,
         }
+        line["replication_plan"] = replication
         if kmeans is not None:
             line["kmeans_fit"] = kmeans
         if gate is not None:

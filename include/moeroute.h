@@ -229,6 +229,33 @@ MOER_API moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, 
                                     float* logits, uint8_t* topk, uint8_t* blk_cnt, int32_t* affinity,
                                     void* ws, size_t ws_bytes, moer_stream_t stream);
 
+/* Replication planning per MoE layer.  [GRACE-MoE] section 4.2 (expert
+ * replication: only the hot experts of the most loaded group are copied, the
+ * replica count follows the load skew) and section 4.3 (predicted load after
+ * replication, W' = W - W_r + W_p).  Each of the G expert groups sits on one
+ * GPU.  Per layer l:
+ *   src[l]   the most loaded group (ties: lower index);
+ *   n_rep[l] min(max(1, floor(W_max * G / sum_g W_g)), G - 1), or 0 when G = 1
+ *            or the layer has no load;
+ *   hot[l][e] 1 for the source group's experts, in descending load (ties:
+ *            lower id), up to and including the one that takes the
+ *            cumulative load past W_max * n / (1 + n) (exact integer test);
+ *   dst[l][r] for r < n_rep: the n least-loaded other groups (ties: lower
+ *            index), in that order; -1 beyond;
+ *   w_pred[l][g] predicted load: the hot load H is split evenly over the
+ *            original and its copies (source: W_max - H n / (1 + n), each
+ *            replica group: W_g + H / (1 + n), fp64), other groups W_g.
+ * W        [L][E] int64 expert loads (moer_affinity_load's W_expert), >= 0.
+ * group_of [L][E] int32 group of each expert, in [0, G).
+ * Limits: 1 <= G <= 64.  An entry out of range leaves its layer unplanned
+ * (n_rep 0) and records MOER_EDATA in the workspace status word.
+ * ws       at least 256 bytes, 256-byte aligned (the status word).
+ */
+MOER_API moer_status moer_replication_plan(const moer_dims* d, const int64_t* W, const int32_t* group_of,
+                                           int32_t G, int32_t* n_rep, int32_t* src, uint8_t* hot,
+                                           int32_t* dst, double* w_pred, void* ws, size_t ws_bytes,
+                                           moer_stream_t stream);
+
 /* Calibration (not on the per-request path): balanced K-means of N
  * calibration signatures into D decoder centroids.  [ELDR] section "Key idea
  * / structure / operation": offline, the calibration prompts' signatures are

@@ -58,6 +58,7 @@ def _load():
         "moer_idf_fit": ([dp, vp, i32, vp, vp], ctypes.c_int),
         "moer_gate_workspace_bytes": ([dp, i32], sz),
         "moer_gate_topk": ([dp, vp, i64, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "moer_replication_plan": ([dp, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_kmeans_workspace_bytes": ([i32, i32, i32], sz),
         "moer_kmeans_balanced": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_ws_status": ([vp, vp], ctypes.c_int),
@@ -75,7 +76,8 @@ LIB = _load()
 EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_noalloc",
            "moer_block_stitch", "moer_affinity_load",
            "moer_route", "moer_idf_fit", "moer_gate_workspace_bytes", "moer_gate_topk",
-           "moer_kmeans_workspace_bytes", "moer_kmeans_balanced", "moer_ws_status",
+           "moer_replication_plan", "moer_kmeans_workspace_bytes", "moer_kmeans_balanced",
+           "moer_ws_status",
            "moer_status_str", "moer_version")
 
 
@@ -145,6 +147,13 @@ def moer_route(dims, req_cnt, R, idf, centroids, D, tau, loads, live, sig, dist,
 def moer_idf_fit(dims, req_cnt, R, idf, stream=None) -> None:
     _check("moer_idf_fit", LIB.moer_idf_fit(ctypes.byref(dims), _ptr(req_cnt), int(R), _ptr(idf),
                                             _stream(stream)))
+
+
+def moer_replication_plan(dims, W, group_of, G, n_rep, src, hot, dst, w_pred, ws, ws_bytes,
+                          stream=None) -> None:
+    _check("moer_replication_plan", LIB.moer_replication_plan(
+        ctypes.byref(dims), _ptr(W), _ptr(group_of), int(G), _ptr(n_rep), _ptr(src), _ptr(hot),
+        _ptr(dst), _ptr(w_pred), _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
 def moer_kmeans_workspace_bytes(N: int, dim: int, D: int) -> int:

@@ -6,6 +6,9 @@
 #include "common.cuh"
 
 namespace moer {
+moer_status replication_plan_launch(const moer_dims* d, const int64_t* W, const int32_t* group_of, int32_t G,
+                                    int32_t* n_rep, int32_t* src, uint8_t* hot, int32_t* dst, double* w_pred,
+                                    uint32_t* status, cudaStream_t st);
 size_t kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D);
 moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, const float* init, int32_t max_iter,
                           float* centroids, int32_t* assign, int32_t* info, double* objective, void* ws,
@@ -229,6 +232,24 @@ moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, int64_t T
   if (hist)
     s = block_counts_launch(d, topk, false, T, blk_tab, nblk, blk_cnt, reinterpret_cast<uint32_t*>(ws), st);
   return s;
+}
+
+moer_status moer_replication_plan(const moer_dims* d, const int64_t* W, const int32_t* group_of, int32_t G,
+                                  int32_t* n_rep, int32_t* src, uint8_t* hot, int32_t* dst, double* w_pred,
+                                  void* ws, size_t ws_bytes, moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (G < 1 || G > 64) return MOER_ERANGE;
+  if (W == nullptr || group_of == nullptr || n_rep == nullptr || src == nullptr || hot == nullptr ||
+      dst == nullptr || w_pred == nullptr)
+    return MOER_EINVAL;
+  if (!aligned(W, 8) || !aligned(w_pred, 8) || !aligned(group_of, 4) || !aligned(n_rep, 4) || !aligned(src, 4) ||
+      !aligned(dst, 4))
+    return MOER_EINVAL;
+  if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
+  if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
+  return moer::replication_plan_launch(d, W, group_of, G, n_rep, src, hot, dst, w_pred,
+                                       reinterpret_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t moer_kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D) {

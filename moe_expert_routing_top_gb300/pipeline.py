@@ -75,6 +75,11 @@ class RoutingStats:
         self.Wg = torch.empty((L, G), dtype=torch.int64, device=dev)
         self.rho_g = torch.empty(L, dtype=torch.float64, device=dev)
         self.rho_e = torch.empty(L, dtype=torch.float64, device=dev)
+        self.n_rep = torch.empty(L, dtype=i32, device=dev)
+        self.rep_src = torch.empty(L, dtype=i32, device=dev)
+        self.hot = torch.empty((L, E), dtype=torch.uint8, device=dev)
+        self.rep_dst = torch.empty((L, G), dtype=i32, device=dev)
+        self.w_pred = torch.empty((L, G), dtype=torch.float64, device=dev)
         self.cache = (torch.zeros((nslots, self.m, E), dtype=torch.uint8, device=dev)
                       if nslots > 0 else None)
         self.nslots = nslots
@@ -134,6 +139,12 @@ class RoutingStats:
     def affinity_load(self):
         nat.moer_affinity_load(self.dims, self.affinity, self.group_of, self.G, self.W, self.Wg,
                                self.rho_g, self.rho_e, self.stream)
+
+    def replication_plan(self):
+        """GRACE replication plan per layer from the current loads (after affinity_load)."""
+        nat.moer_replication_plan(self.dims, self.W, self.group_of, self.G, self.n_rep, self.rep_src,
+                                  self.hot, self.rep_dst, self.w_pred, self.ws, self.ws_bytes,
+                                  self.stream)
 
     def route(self, R, write_sig=True):
         nat.moer_route(self.dims, self.req_cnt, R, self.idf, self.centroids, self.D, self.tau,

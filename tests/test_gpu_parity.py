@@ -9,6 +9,7 @@ import pytest
 
 import gen
 import oracle
+from oracle import replication as rp
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +73,11 @@ def test_path_parity(env, cfg, R, nchunks):
         W, Wg, rg, re = orc.loads(tka, wl.E, wl.group_of, wl.G)
         assert np.array_equal(gu.host(rs.W), W) and np.array_equal(gu.host(rs.Wg), Wg)
         assert np.array_equal(gu.host(rs.rho_g), rg) and np.array_equal(gu.host(rs.rho_e), re)
+        rs.replication_plan()
+        pn, psrc, phot, pdst, pwp = rp.plan(W, wl.group_of, wl.G)
+        assert np.array_equal(gu.host(rs.n_rep), pn) and np.array_equal(gu.host(rs.rep_src), psrc)
+        assert np.array_equal(gu.host(rs.hot), phot) and np.array_equal(gu.host(rs.rep_dst), pdst)
+        assert np.array_equal(gu.host(rs.w_pred), pwp), "replication plan"
         sig, dist = orc.sig_dist(rc, wl.idf, wl.centroids)
         gu.assert_close(gu.host(rs.sig[:b.R]), sig, "signature")
         gu.assert_close(gu.host(rs.dist[:b.R]), dist, "distance")
