@@ -357,6 +357,7 @@ def run_gpu(args):
         raise RuntimeError("device-side status after the replication plan is not OK")
     replication = {"ms": statistics.median(x.elapsed_time(y) for x, y in rp_ev), "layers": wl.L,
                    "groups": wl.G, "replicas_per_layer": rs.n_rep.cpu().tolist()}
+    mask_sel = measure_mask_select(args, wl, b, bd, rs, device, stream, rank)
     kmeans = measure_kmeans(args, device, stream, rank) if args.kmeans else None
     gate = None
     if args.gate:
@@ -390,6 +391,7 @@ def run_gpu(args):
             "cpu_baseline_1core": cpu1,
         }
         line["replication_plan"] = replication
+        line["mask_select"] = mask_sel
         if kmeans is not None:
             line["kmeans_fit"] = kmeans
         if gate is not None:
@@ -626,6 +628,47 @@ def gate_cpu_baseline_all_cores(wl, ntok_per_core):
             "sample": f"gate logits (fp64 sums) + top-k of the first {tokens} tokens x {wl.L} "
                       f"layers, {ntok_per_core} per process on {ncores} host cores, one pass, "
                       f"{wall:.1f} s wall"}
+
+
+def measure_mask_select(args, wl, b, bd, rs, device, stream, rank):
+    """Greedy layer-mask selection (12 of the 48 layers) over the whole batch's top-k ids
+    from the step just timed, with CUDA events; the oracle on the first 16 requests."""
+    import torch
+    from moe_expert_routing_top_gb300 import _native as nat
+    m = 12
+    dims = nat.make_dims(wl.E, wl.k, wl.L, [], wl.B)
+    topk = rs.topk_for(b.T)
+    off = torch.from_numpy(np.asarray(b.req_off, dtype=np.int32)).to(device)
+    mask = torch.empty(m, dtype=torch.int32, device=device)
+    qual = torch.empty(m, dtype=torch.float64, device=device)
+    wsb = nat.moer_mask_select_workspace_bytes(dims, b.R)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+    times = []
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        nat.moer_mask_select(dims, topk, b.T, off, b.R, None, m, mask, qual, ws, wsb, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if nat.moer_ws_status(ws, stream) != 0:
+        raise RuntimeError("device-side status after the mask selection is not OK")
+    out = {"workload": f"greedy mask, {m} of {wl.L} layers, {b.R} requests ({b.T} tokens)",
+           "ms": statistics.median(times[1:]), "mask_in_order": mask.cpu().tolist(),
+           "quality": qual.cpu().tolist()}
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        from oracle import mask_select as ms
+        nreq = 16
+        bs, logits = cpu_sample(wl, nreq)
+        tk = oracle.get().topk(logits, wl.k)
+        t0 = time.perf_counter()
+        ms.greedy_mask(tk, bs.req_off, wl.E, m)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"ms_per_request": dt * 1e3 / nreq, "cores": 1, "kind": "oracle",
+                               "sample": f"first {nreq} requests ({bs.T} tokens), {dt:.1f} s"}
+        out["gpu_ms_per_request"] = out["ms"] / b.R
+    return out
 
 
 def measure_kmeans(args, device, stream, rank):

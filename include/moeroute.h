@@ -256,6 +256,33 @@ MOER_API moer_status moer_replication_plan(const moer_dims* d, const int64_t* W,
                                            int32_t* dst, double* w_pred, void* ws, size_t ws_bytes,
                                            moer_stream_t stream);
 
+/* Calibration (not on the per-request path): greedy choice of the signature's
+ * layer mask.  [ELDR] section "Key idea / structure / operation": the
+ * signature keeps only the MoE layers with the highest signature quality,
+ * chosen greedily offline.  The pages do not print the quality objective; the
+ * one here is a labelled proxy: each calibration request is split into its
+ * first half (tokens [0, floor(len/2))) and its second half, and quality(M)
+ * is the mean over the R requests of the cosine between the two halves'
+ * count.idf signatures over the layers in M (0 if either is zero).  m times,
+ * the layer outside M with the largest quality(M + {l}) is added (ties: the
+ * lower layer).  Sums in fp64.
+ * topk     [L][T][k] uint8 (moer_topk_signature's output over the calibration
+ *          batch); d->E, d->k, d->L give its shape (d->mask is not used).
+ * req_off  [R + 1] int32 token offsets of the requests (0 = req_off[0] <= ...
+ *          <= req_off[R] = T); a malformed request or an id >= E is skipped
+ *          and recorded as MOER_EDATA.
+ * idf      [L][E] fp32 per-layer idf, or NULL for 1.
+ * mask_out [m] int32: the layers in the order chosen (sort them for a mask).
+ * quality_out [m] fp64 or NULL: quality after each addition.
+ * Limits: 1 <= m <= L, R >= 1.
+ * ws       at least moer_mask_select_workspace_bytes(d, R) bytes, 256-byte
+ *          aligned (status word, per (request, layer) sums, running sums).
+ */
+MOER_API size_t moer_mask_select_workspace_bytes(const moer_dims* d, int32_t R);
+MOER_API moer_status moer_mask_select(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off,
+                                      int32_t R, const float* idf, int32_t m, int32_t* mask_out,
+                                      double* quality_out, void* ws, size_t ws_bytes, moer_stream_t stream);
+
 /* Calibration (not on the per-request path): balanced K-means of N
  * calibration signatures into D decoder centroids.  [ELDR] section "Key idea
  * / structure / operation": offline, the calibration prompts' signatures are

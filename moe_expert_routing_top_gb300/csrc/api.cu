@@ -6,6 +6,10 @@
 #include "common.cuh"
 
 namespace moer {
+size_t mask_select_workspace_bytes(int32_t L, int32_t R);
+moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off, int32_t R,
+                               const float* idf, int32_t m, int32_t* mask_out, double* quality_out, void* ws,
+                               cudaStream_t st);
 moer_status replication_plan_launch(const moer_dims* d, const int64_t* W, const int32_t* group_of, int32_t G,
                                     int32_t* n_rep, int32_t* src, uint8_t* hot, int32_t* dst, double* w_pred,
                                     uint32_t* status, cudaStream_t st);
@@ -250,6 +254,27 @@ moer_status moer_replication_plan(const moer_dims* d, const int64_t* W, const in
   if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
   return moer::replication_plan_launch(d, W, group_of, G, n_rep, src, hot, dst, w_pred,
                                        reinterpret_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moer_mask_select_workspace_bytes(const moer_dims* d, int32_t R) {
+  if (d == nullptr || d->L < 1 || R < 1) return WS_HEADER;
+  return moer::mask_select_workspace_bytes(d->L, R);
+}
+
+moer_status moer_mask_select(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off, int32_t R,
+                             const float* idf, int32_t m, int32_t* mask_out, double* quality_out, void* ws,
+                             size_t ws_bytes, moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (R < 1 || T < 1 || m < 1 || m > d->L) return MOER_ERANGE;
+  if (topk == nullptr || req_off == nullptr || mask_out == nullptr) return MOER_EINVAL;
+  if (!aligned(req_off, 4) || !aligned(mask_out, 4) || (idf != nullptr && !aligned(idf, 4)) ||
+      (quality_out != nullptr && !aligned(quality_out, 8)))
+    return MOER_EINVAL;
+  if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
+  if (ws_bytes < moer_mask_select_workspace_bytes(d, R)) return MOER_ENOMEM;
+  return moer::mask_select_launch(d, topk, T, req_off, R, idf, m, mask_out, quality_out, ws,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t moer_kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D) {

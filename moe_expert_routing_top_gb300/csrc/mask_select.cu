@@ -1,0 +1,158 @@
+// mask_select.cu -- moer_mask_select: greedy choice of the signature's layer mask.
+//
+// ELDR, section "Key idea / structure / operation": the signature keeps only
+// the subset of MoE layers with the highest signature quality, chosen
+// greedily on the calibration prompts.  The pages do not print the quality
+// objective (the paper relates prefill signatures to decode-time expert reuse,
+// which needs decode traces); the objective here is a labelled proxy: each
+// calibration prompt is split into its first half (tokens [0, floor(len/2)))
+// and its second half, and quality(M) is the mean over all requests of the
+// cosine between the two halves' count.idf signatures restricted to the layers
+// in M (0 when either is the zero vector).  Greedy: starting from the empty
+// set, m times add the layer with the largest quality(M + {l}) (ties: the
+// lower layer).
+//
+// Design: the cosine over a layer set only needs, per (request, layer), the
+// three sums s11 = sum_e w1^2, s22 = sum_e w2^2, s12 = sum_e w1 w2 (w = count *
+// idf): quality(M) = mean_r S12 / sqrt(S11 S22) with S = sum over l in M.
+//   * mask_stats_kernel: one CTA per (request, layer); the two halves' ids go
+//     into shared-memory histograms, then the three sums in fp64.
+//   * mask_greedy_kernel: one CTA; per step one warp per candidate layer, the
+//     lanes over the requests (running sums of the chosen layers + the
+//     candidate's), a warp reduction, and the argmax; then the chosen layer's
+//     sums are added to every request's running sums.
+#include "common.cuh"
+
+namespace moer {
+
+constexpr int MS_STATS_THREADS = 128;
+constexpr int MS_GREEDY_THREADS = 1024;
+
+__global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint8_t* __restrict__ topk, int64_t T,
+                                                                      int k, int E, int L,
+                                                                      const int32_t* __restrict__ req_off,
+                                                                      const float* __restrict__ idf,
+                                                                      double* __restrict__ stats, uint32_t* status) {
+  __shared__ int c1[256], c2[256];
+  __shared__ double red[3][MS_STATS_THREADS / 32];
+  const int r = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t t0 = req_off[r], t1 = req_off[r + 1];
+  double* out = stats + ((size_t)r * L + l) * 3;
+  if (t0 < 0 || t1 < t0 || t1 > T) {
+    if (tid == 0) {
+      out[0] = out[1] = out[2] = 0.0;
+      if (l == 0) atomicOr(status, WS_BIT_EDATA);
+    }
+    return;
+  }
+  for (int e = tid; e < E; e += MS_STATS_THREADS) c1[e] = c2[e] = 0;
+  __syncthreads();
+  const int64_t mid = t0 + (t1 - t0) / 2;
+  const uint8_t* row = topk + (size_t)l * T * k;
+  for (int64_t q = t0 * k + tid; q < t1 * k; q += MS_STATS_THREADS) {
+    const int e = row[q];
+    if (e < E) atomicAdd(q < mid * k ? &c1[e] : &c2[e], 1);
+    else atomicOr(status, WS_BIT_EDATA);  // an id outside [0, E) is skipped and reported
+  }
+  __syncthreads();
+  double a = 0.0, b = 0.0, c = 0.0;
+  for (int e = tid; e < E; e += MS_STATS_THREADS) {
+    const double w = idf != nullptr ? (double)idf[(size_t)l * E + e] : 1.0;
+    const double w1 = c1[e] * w, w2 = c2[e] * w;
+    a = fma(w1, w1, a);
+    b = fma(w2, w2, b);
+    c = fma(w1, w2, c);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(FULL, a, o);
+    b += __shfl_xor_sync(FULL, b, o);
+    c += __shfl_xor_sync(FULL, c, o);
+  }
+  if (lane == 0) {
+    red[0][warp] = a;
+    red[1][warp] = b;
+    red[2][warp] = c;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double s[3] = {0.0, 0.0, 0.0};
+    for (int w = 0; w < MS_STATS_THREADS / 32; ++w)
+      for (int j = 0; j < 3; ++j) s[j] += red[j][w];
+    out[0] = s[0];
+    out[1] = s[1];
+    out[2] = s[2];
+  }
+}
+
+__device__ __forceinline__ double ms_cos(double s11, double s22, double s12) {
+  return (s11 > 0.0 && s22 > 0.0) ? s12 / sqrt(s11 * s22) : 0.0;
+}
+
+// run [R][3] running sums of the chosen layers (zeroed by the host).
+__global__ void __launch_bounds__(MS_GREEDY_THREADS, 1)
+    mask_greedy_kernel(const double* __restrict__ stats, int R, int L, int m, double* __restrict__ run,
+                       int32_t* __restrict__ mask_out, double* __restrict__ quality_out) {
+  __shared__ double qual[256];
+  __shared__ unsigned char taken[256];
+  __shared__ int s_best;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int l = tid; l < L; l += MS_GREEDY_THREADS) taken[l] = 0;
+  __syncthreads();
+  for (int step = 0; step < m; ++step) {
+    for (int l = warp; l < L; l += MS_GREEDY_THREADS / 32) {
+      double acc = 0.0;
+      if (!taken[l]) {
+        for (int r = lane; r < R; r += 32) {
+          const double* s = stats + ((size_t)r * L + l) * 3;
+          const double* u = run + (size_t)r * 3;
+          acc += ms_cos(u[0] + s[0], u[1] + s[1], u[2] + s[2]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
+      if (lane == 0) qual[l] = acc / (double)R;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int best = -1;
+      for (int l = 0; l < L; ++l)
+        if (!taken[l] && (best < 0 || qual[l] > qual[best])) best = l;
+      taken[best] = 1;
+      s_best = best;
+      mask_out[step] = best;
+      if (quality_out != nullptr) quality_out[step] = qual[best];
+    }
+    __syncthreads();
+    const int best = s_best;
+    for (int r = tid; r < R; r += MS_GREEDY_THREADS) {
+      const double* s = stats + ((size_t)r * L + best) * 3;
+      double* u = run + (size_t)r * 3;
+      u[0] += s[0];
+      u[1] += s[1];
+      u[2] += s[2];
+    }
+    __syncthreads();
+  }
+}
+
+size_t mask_select_workspace_bytes(int32_t L, int32_t R) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  return WS_HEADER + r256((size_t)R * L * 3 * sizeof(double)) + r256((size_t)R * 3 * sizeof(double));
+}
+
+moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off, int32_t R,
+                               const float* idf, int32_t m, int32_t* mask_out, double* quality_out, void* ws,
+                               cudaStream_t st) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  char* w = static_cast<char*>(ws);
+  double* stats = reinterpret_cast<double*>(w + WS_HEADER);
+  double* run = reinterpret_cast<double*>(w + WS_HEADER + r256((size_t)R * d->L * 3 * sizeof(double)));
+  if (cudaMemsetAsync(run, 0, (size_t)R * 3 * sizeof(double), st) != cudaSuccess) return MOER_ECUDA;
+  mask_stats_kernel<<<dim3((unsigned)R, (unsigned)d->L), MS_STATS_THREADS, 0, st>>>(
+      topk, T, d->k, d->E, d->L, req_off, idf, stats, reinterpret_cast<uint32_t*>(ws));
+  mask_greedy_kernel<<<1, MS_GREEDY_THREADS, 0, st>>>(stats, R, d->L, m, run, mask_out, quality_out);
+  return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
+}
+
+}  // namespace moer
