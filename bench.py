@@ -527,23 +527,26 @@ def run_gate_e2e(args, wl, b, rs, hidden, w_gate, stream, device, dist):
     pinned = torch.empty((b.T, H), dtype=torch.int16, pin_memory=True)
     pinned.copy_(hidden)  # untimed: the host copy of the same inputs
     offs = np.concatenate([[0], np.cumsum([x.T for x in batches])]).astype(int)
-    copy_stream = torch.cuda.Stream(device)
+    copy_streams = [torch.cuda.Stream(device) for _ in range(max(args.e2e_copy_streams, 1))]
     maxT = max(x.T for x in batches)
     dev_bufs = [torch.empty((maxT, H), dtype=torch.int16, device=device) for _ in range(2)]
     bds = [pipeline.BatchDev.from_host(bb, device=device) for bb in batches]
     choice_host = torch.empty(wl.R, dtype=torch.int32, pin_memory=True)
 
     def one_step():
-        copied = [torch.cuda.Event() for _ in range(nch)]
         freed = [torch.cuda.Event() for _ in range(nch)]
         for i, bb in enumerate(batches):
             dst = dev_bufs[i % 2][:bb.T]
-            with torch.cuda.stream(copy_stream):
-                if i >= 2:
-                    copy_stream.wait_event(freed[i - 2])
-                dst.copy_(pinned[offs[i]:offs[i + 1]], non_blocking=True)
-                copied[i].record(copy_stream)
-            stream.wait_event(copied[i])
+            cuts = np.linspace(0, bb.T, len(copy_streams) + 1).astype(int)
+            for j, cs in enumerate(copy_streams):  # contiguous row ranges over the copy streams
+                with torch.cuda.stream(cs):
+                    if i >= 2:
+                        cs.wait_event(freed[i - 2])
+                    a, z = int(cuts[j]), int(cuts[j + 1])
+                    dst[a:z].copy_(pinned[offs[i] + a:offs[i] + z], non_blocking=True)
+                    done = torch.cuda.Event()
+                    done.record(cs)
+                stream.wait_event(done)
             rs.gate_step(dst, w_gate, bds[i])
             freed[i].record(stream)
             r0 = int(bounds[i])
@@ -563,6 +566,7 @@ def run_gate_e2e(args, wl, b, rs, hidden, w_gate, stream, device, dist):
     units = sum_over_ranks(dist, wl.L * b.T, device)
     return {"value": units / dt, "unit": UNIT, "h2d_bytes_per_step": int(b.T * H * 2),
             "d2h_bytes_per_step": int(wl.R * 4), "ms_per_step": dt * 1e3, "chunks": nch,
+            "copy_streams": len(copy_streams), "h2d_gbs": b.T * H * 2 / dt / 1e9,
             "steps": args.e2e_steps}
 
 
@@ -736,7 +740,7 @@ def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
     for bb in batches:
         chunk_views.append((off, bb.T))
         off += bb.T
-    copy_stream = torch.cuda.Stream(device)
+    copy_streams = [torch.cuda.Stream(device) for _ in range(max(args.e2e_copy_streams, 1))]
     dev_bufs = [torch.empty((wl.L, max(x.T for x in batches), wl.E), dtype=torch.float32,
                             device=device) for _ in range(2)]
     bds = [pipeline.BatchDev.from_host(bb, device=device) for bb in batches]
@@ -745,18 +749,20 @@ def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
     d2h = wl.R * 4
 
     def one_step():
-        copied = [torch.cuda.Event() for _ in range(nch)]
         freed = [torch.cuda.Event() for _ in range(nch)]
         for i, (o, t) in enumerate(chunk_views):
             buf = dev_bufs[i % 2]
-            with torch.cuda.stream(copy_stream):
-                if i >= 2:
-                    copy_stream.wait_event(freed[i - 2])
-                dst = buf[:, :t]
-                for l in range(wl.L):  # [L][T][E]: one contiguous row range per layer
-                    dst[l].copy_(pinned[l, o:o + t], non_blocking=True)
-                copied[i].record(copy_stream)
-            stream.wait_event(copied[i])
+            dst = buf[:, :t]
+            # [L][T][E]: one contiguous row range per layer, spread over the copy streams
+            for j, cs in enumerate(copy_streams):
+                with torch.cuda.stream(cs):
+                    if i >= 2:
+                        cs.wait_event(freed[i - 2])
+                    for l in range(j, wl.L, len(copy_streams)):
+                        dst[l].copy_(pinned[l, o:o + t], non_blocking=True)
+                    done = torch.cuda.Event()
+                    done.record(cs)
+                stream.wait_event(done)
             rs.step(dst, bds[i])
             freed[i].record(stream)
             r0 = int(bounds[i])
@@ -776,7 +782,7 @@ def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
     units = sum_over_ranks(dist, wl.L * b.T, device)
     return {"value": units / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3, "chunks": nch,
-            "steps": args.e2e_steps}
+            "copy_streams": len(copy_streams), "h2d_gbs": h2d / dt / 1e9, "steps": args.e2e_steps}
 
 
 def cpu_baseline(wl, nreq):
@@ -859,6 +865,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="copy streams for the host-to-device copies (1 measured as fast as 2-8)")
     ap.add_argument("--gate", dest="gate", action="store_true", default=True,
                     help="also measure the gate path (moer_gate_topk first) into gate_path")
     ap.add_argument("--no-gate", dest="gate", action="store_false")
