@@ -5,9 +5,11 @@
 // and each layer of the selected mask, how many of the block's tokens picked
 // each expert in their top-k.
 //
-// A segmented histogram over the block table: one warp per (KV block, mask
-// layer) pair reads the block's top-k ids (contiguous uint8, len * k bytes),
-// counts them into a private shared-memory row of packed 8-bit counters (four
+// A segmented histogram over the block table: a persistent grid of warps walks
+// the KV blocks; per block the warp reads the block's top-k ids of up to eight
+// mask layers at once (contiguous uint8, len * k bytes per layer, as 4-byte
+// words when k is a multiple of 4), counts them into private shared-memory
+// rows of packed 8-bit counters (four
 // experts per 32-bit word; a count never exceeds B <= 255) and writes the row
 // out with coalesced 32-bit stores.  No global atomics, no pre-zeroing.  The
 // block table is validated on the fly: a block whose length is outside
@@ -30,38 +32,80 @@ struct BcParams {
   int16_t layer_row[256];  // ids row-block of mask layer i
 };
 
+constexpr int BC_MC = 8;  // mask layers counted together (their loads in flight at once)
+
 __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __grid_constant__ BcParams p) {
-  extern __shared__ uint32_t bc_smem[];  // [BC_WARPS][E / 4]
+  extern __shared__ uint32_t bc_smem[];  // [BC_WARPS][BC_MC][E / 4]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wpb = p.E / 4;
-  uint32_t* cnt = bc_smem + warp * wpb;
-  const int64_t pair = (int64_t)blockIdx.x * BC_WARPS + warp;
-  if (pair >= (int64_t)p.nblk * p.m) return;
-  const int b = (int)(pair / p.m), i = (int)(pair - (int64_t)b * p.m);
-  const int t0 = p.blk_tab[2 * b], ln = p.blk_tab[2 * b + 1];
-  bool ok = ln >= 1 && ln <= p.B && t0 >= 0 && (int64_t)t0 + ln <= p.T;
-  if (b == 0) {
-    ok = ok && t0 == 0;
-  } else {
-    const int pt0 = p.blk_tab[2 * (b - 1)], pln = p.blk_tab[2 * (b - 1) + 1];
-    ok = ok && (int64_t)pt0 + pln == (int64_t)t0;
+  uint32_t* cnt = bc_smem + warp * BC_MC * wpb;
+  const int64_t stride = (int64_t)gridDim.x * BC_WARPS;
+  // 4-byte loads when every block's id row starts on a 4-byte boundary
+  const bool vec = (p.k % 4) == 0;
+  // persistent warps, one KV block at a time, all mask layers of the block
+  for (int64_t bb = (int64_t)blockIdx.x * BC_WARPS + warp; bb < p.nblk; bb += stride) {
+    const int b = (int)bb;
+    const int t0 = p.blk_tab[2 * b], ln = p.blk_tab[2 * b + 1];
+    bool ok = ln >= 1 && ln <= p.B && t0 >= 0 && (int64_t)t0 + ln <= p.T;
+    if (b == 0) {
+      ok = ok && t0 == 0;
+    } else {
+      const int pt0 = p.blk_tab[2 * (b - 1)], pln = p.blk_tab[2 * (b - 1) + 1];
+      ok = ok && (int64_t)pt0 + pln == (int64_t)t0;
+    }
+    if (b == p.nblk - 1) ok = ok && (int64_t)t0 + ln == p.T;
+    if (!ok) {
+      if (lane == 0) atomicOr(p.status, WS_BIT_EDATA);
+      continue;
+    }
+    const int n = ln * p.k;
+    for (int i0 = 0; i0 < p.m; i0 += BC_MC) {
+      const int nl = min(BC_MC, p.m - i0);
+      for (int w = lane; w < nl * wpb; w += 32) cnt[w] = 0u;
+      __syncwarp();
+      if (vec) {
+        const int nw = n >> 2;
+        for (int q0 = 0; q0 < nw; q0 += 32) {
+          const int q = q0 + lane;
+          uint32_t v[BC_MC];
+#pragma unroll
+          for (int ii = 0; ii < BC_MC; ++ii) {
+            v[ii] = 0u;
+            if (ii < nl && q < nw) {
+              const uint8_t* src = p.ids + (int64_t)p.layer_row[i0 + ii] * p.layer_stride + (int64_t)t0 * p.k;
+              v[ii] = reinterpret_cast<const uint32_t*>(src)[q];
+            }
+          }
+#pragma unroll
+          for (int ii = 0; ii < BC_MC; ++ii) {
+            if (ii < nl && q < nw) {
+              uint32_t* c = cnt + ii * wpb;
+#pragma unroll
+              for (int by = 0; by < 4; ++by) {
+                const int e = (v[ii] >> (8 * by)) & 0xFF;
+                atomicAdd(&c[e >> 2], 1u << ((e & 3) * 8));
+              }
+            }
+          }
+        }
+      } else {
+        for (int ii = 0; ii < nl; ++ii) {
+          const uint8_t* src = p.ids + (int64_t)p.layer_row[i0 + ii] * p.layer_stride + (int64_t)t0 * p.k;
+          uint32_t* c = cnt + ii * wpb;
+          for (int j = lane; j < n; j += 32) {
+            const int e = src[j];
+            atomicAdd(&c[e >> 2], 1u << ((e & 3) * 8));
+          }
+        }
+      }
+      __syncwarp();
+      for (int ii = 0; ii < nl; ++ii) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.blk_cnt + ((size_t)b * p.m + i0 + ii) * p.E);
+        for (int w = lane; w < wpb; w += 32) dst[w] = cnt[ii * wpb + w];
+      }
+      __syncwarp();
+    }
   }
-  if (b == p.nblk - 1) ok = ok && (int64_t)t0 + ln == p.T;
-  if (!ok) {
-    if (lane == 0 && i == 0) atomicOr(p.status, WS_BIT_EDATA);
-    return;
-  }
-  for (int w = lane; w < wpb; w += 32) cnt[w] = 0u;
-  __syncwarp();
-  const uint8_t* src = p.ids + (int64_t)p.layer_row[i] * p.layer_stride + (int64_t)t0 * p.k;
-  const int n = ln * p.k;
-  for (int j = lane; j < n; j += 32) {
-    const int e = src[j];
-    atomicAdd(&cnt[e >> 2], 1u << ((e & 3) * 8));
-  }
-  __syncwarp();
-  uint32_t* dst = reinterpret_cast<uint32_t*>(p.blk_cnt + ((size_t)b * p.m + i) * p.E);
-  for (int w = lane; w < wpb; w += 32) dst[w] = cnt[w];
 }
 
 // ids: either the caller's [L][T][k] top-k (mask_only = false: row block of
@@ -83,10 +127,11 @@ moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mas
   p.status = status;
   for (int i = 0; i < 256; ++i) p.layer_row[i] = 0;
   for (int i = 0; i < d->m; ++i) p.layer_row[i] = (int16_t)(mask_only ? i : d->mask[i]);
-  const int64_t pairs = (int64_t)nblk * d->m;
-  const int64_t grid = (pairs + BC_WARPS - 1) / BC_WARPS;
-  if (grid <= 0) return MOER_OK;
-  block_counts_kernel<<<(unsigned)grid, BC_WARPS * 32, BC_WARPS * (d->E / 4) * sizeof(uint32_t), st>>>(p);
+  if (nblk <= 0 || d->m <= 0) return MOER_OK;
+  const int sms = device_sm_count();
+  if (sms <= 0) return MOER_ECUDA;
+  const int64_t grid = min64(((int64_t)nblk + BC_WARPS - 1) / BC_WARPS, (int64_t)sms * 8);
+  block_counts_kernel<<<(unsigned)grid, BC_WARPS * 32, BC_WARPS * BC_MC * (d->E / 4) * sizeof(uint32_t), st>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
