@@ -358,6 +358,7 @@ def run_gpu(args):
     replication = {"ms": statistics.median(x.elapsed_time(y) for x, y in rp_ev), "layers": wl.L,
                    "groups": wl.G, "replicas_per_layer": rs.n_rep.cpu().tolist()}
     mask_sel = measure_mask_select(args, wl, b, bd, rs, device, stream, rank)
+    spectral = measure_spectral(args, wl, rs, device, stream, rank)
     kmeans = measure_kmeans(args, device, stream, rank) if args.kmeans else None
     gate = None
     if args.gate:
@@ -392,6 +393,7 @@ def run_gpu(args):
         }
         line["replication_plan"] = replication
         line["mask_select"] = mask_sel
+        line["spectral_groups"] = spectral
         if kmeans is not None:
             line["kmeans_fit"] = kmeans
         if gate is not None:
@@ -672,6 +674,44 @@ def measure_mask_select(args, wl, b, bd, rs, device, stream, rank):
         out["cpu_baseline"] = {"ms_per_request": dt * 1e3 / nreq, "cores": 1, "kind": "oracle",
                                "sample": f"first {nreq} requests ({bs.T} tokens), {dt:.1f} s"}
         out["gpu_ms_per_request"] = out["ms"] / b.R
+    return out
+
+
+def measure_spectral(args, wl, rs, device, stream, rank):
+    """Spectral grouping of the step's 48 co-activation matrices into 8 groups (17 size
+    tolerances each, knee), with CUDA events; the oracle per layer on the first 4 layers."""
+    import torch
+    from moe_expert_routing_top_gb300 import _native as nat
+    G = wl.G
+    dims = nat.make_dims(wl.E, wl.k, wl.L, [], wl.B)
+    g = torch.empty((wl.L, wl.E), dtype=torch.int32, device=device)
+    k = torch.empty(wl.L, dtype=torch.int32, device=device)
+    uc = torch.empty((wl.L, 17), dtype=torch.float64, device=device)
+    sc = torch.empty((wl.L, 17), dtype=torch.float64, device=device)
+    wsb = nat.moer_spectral_workspace_bytes(dims, G)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+    times = []
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        nat.moer_spectral_groups(dims, rs.affinity, G, g, k, uc, sc, ws, wsb, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if nat.moer_ws_status(ws, stream) != 0:
+        raise RuntimeError("device-side status after the spectral grouping is not OK")
+    out = {"workload": f"spectral grouping, {wl.L} layers, E={wl.E} into G={G}, 17 size tolerances",
+           "ms": statistics.median(times[1:]), "knee_j": k.cpu().tolist()}
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import grouping as gp
+        A = rs.affinity.cpu().numpy()
+        t0 = time.perf_counter()
+        for l in range(4):
+            gp.group_layer(A[l], G)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"ms_per_layer": dt * 1e3 / 4, "cores": 1, "kind": "oracle",
+                               "sample": "4 layers (numpy eigh + scipy Hungarian per step)"}
+        out["gpu_ms_per_layer"] = out["ms"] / wl.L
     return out
 
 

@@ -229,6 +229,38 @@ MOER_API moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, 
                                     float* logits, uint8_t* topk, uint8_t* blk_cnt, int32_t* affinity,
                                     void* ws, size_t ws_bytes, moer_stream_t stream);
 
+/* Expert grouping per MoE layer.  [GRACE-MoE] section 4.1: spectral
+ * clustering of the co-activation matrix puts experts that are selected
+ * together on the same GPU; the group sizes are held within
+ * [E_bar - delta, E_bar + delta], delta = E_bar * r, with r at the knee of
+ * the affinity utilisation U(r) (the size deviation S(r) beside it).  For G
+ * groups, per layer, in fp64:
+ *   M = D^-1/2 A D^-1/2 (A: co-activation off the diagonal, D: its row sums);
+ *   embedding: eigenvectors of M's G largest eigenvalues, rows scaled to unit
+ *   length; for r = j/16 (j = 0..16) group sizes in [max(1, floor(E(16-j)/16G)),
+ *   min(E, ceil(E(16+j)/16G))]: K-means on the embedding under those bounds
+ *   (seeds: largest degree, then farthest from the seeds so far; exact bounded
+ *   assignment each step, centroids to the means, at most 100 steps);
+ *   U(r) = affinity inside groups / affinity off the diagonal, S(r) = std of
+ *   the sizes / (E/G); the knee of U over r (both scaled to [0, 1]: the point
+ *   farthest above the chord from r = 0 to r = 1, ties to smaller r, r = 0
+ *   when none is above) picks the groups.
+ * affinity [L][E][E] int32 (moer_topk_signature's co-activation).
+ * group_of [L][E] int32 out: the group of each expert (usable as the group
+ *          map of moer_affinity_load and moer_replication_plan).
+ * knee     [L] int32 out: j of the chosen r = j/16.
+ * u_curve, s_curve [L][17] fp64 out: U and S at every grid point.
+ * Limits: E <= 128, 2 <= G <= 31, G <= E.
+ * ws       at least moer_spectral_workspace_bytes(d, G) bytes, 256-byte aligned
+ *          (status word, eigenvectors, embedding, degrees, groups per grid
+ *          point).  A Jacobi sweep or an assignment that hits its bound
+ *          records MOER_ETIMEOUT.
+ */
+MOER_API size_t moer_spectral_workspace_bytes(const moer_dims* d, int32_t G);
+MOER_API moer_status moer_spectral_groups(const moer_dims* d, const int32_t* affinity, int32_t G,
+                                          int32_t* group_of, int32_t* knee, double* u_curve, double* s_curve,
+                                          void* ws, size_t ws_bytes, moer_stream_t stream);
+
 /* Replication planning per MoE layer.  [GRACE-MoE] section 4.2 (expert
  * replication: only the hot experts of the most loaded group are copied, the
  * replica count follows the load skew) and section 4.3 (predicted load after

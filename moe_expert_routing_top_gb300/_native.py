@@ -58,6 +58,8 @@ def _load():
         "moer_idf_fit": ([dp, vp, i32, vp, vp], ctypes.c_int),
         "moer_gate_workspace_bytes": ([dp, i32], sz),
         "moer_gate_topk": ([dp, vp, i64, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "moer_spectral_workspace_bytes": ([dp, i32], sz),
+        "moer_spectral_groups": ([dp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_mask_select_workspace_bytes": ([dp, i32], sz),
         "moer_mask_select": ([dp, vp, i64, vp, i32, vp, i32, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_replication_plan": ([dp, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
@@ -79,7 +81,8 @@ EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_n
            "moer_block_stitch", "moer_affinity_load",
            "moer_route", "moer_idf_fit", "moer_gate_workspace_bytes", "moer_gate_topk",
            "moer_replication_plan", "moer_kmeans_workspace_bytes", "moer_kmeans_balanced",
-           "moer_mask_select_workspace_bytes", "moer_mask_select",
+           "moer_mask_select_workspace_bytes", "moer_mask_select", "moer_spectral_workspace_bytes",
+           "moer_spectral_groups",
            "moer_ws_status",
            "moer_status_str", "moer_version")
 
@@ -150,6 +153,17 @@ def moer_route(dims, req_cnt, R, idf, centroids, D, tau, loads, live, sig, dist,
 def moer_idf_fit(dims, req_cnt, R, idf, stream=None) -> None:
     _check("moer_idf_fit", LIB.moer_idf_fit(ctypes.byref(dims), _ptr(req_cnt), int(R), _ptr(idf),
                                             _stream(stream)))
+
+
+def moer_spectral_workspace_bytes(dims, G: int) -> int:
+    return int(LIB.moer_spectral_workspace_bytes(ctypes.byref(dims), int(G)))
+
+
+def moer_spectral_groups(dims, affinity, G, group_of, knee, u_curve, s_curve, ws, ws_bytes,
+                         stream=None) -> None:
+    _check("moer_spectral_groups", LIB.moer_spectral_groups(
+        ctypes.byref(dims), _ptr(affinity), int(G), _ptr(group_of), _ptr(knee), _ptr(u_curve),
+        _ptr(s_curve), _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
 def moer_mask_select_workspace_bytes(dims, R: int) -> int:

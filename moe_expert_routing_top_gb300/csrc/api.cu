@@ -6,6 +6,9 @@
 #include "common.cuh"
 
 namespace moer {
+size_t spectral_workspace_bytes(int L, int E, int G);
+moer_status spectral_launch(const moer_dims* d, const int32_t* affinity, int32_t G, int32_t* group_of,
+                            int32_t* knee, double* u_curve, double* s_curve, void* ws, cudaStream_t st);
 size_t mask_select_workspace_bytes(int32_t L, int32_t R);
 moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off, int32_t R,
                                const float* idf, int32_t m, int32_t* mask_out, double* quality_out, void* ws,
@@ -275,6 +278,28 @@ moer_status moer_mask_select(const moer_dims* d, const uint8_t* topk, int64_t T,
   if (ws_bytes < moer_mask_select_workspace_bytes(d, R)) return MOER_ENOMEM;
   return moer::mask_select_launch(d, topk, T, req_off, R, idf, m, mask_out, quality_out, ws,
                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moer_spectral_workspace_bytes(const moer_dims* d, int32_t G) {
+  if (d == nullptr || d->L < 1 || d->E < 1 || G < 1) return WS_HEADER;
+  return moer::spectral_workspace_bytes(d->L, d->E, G);
+}
+
+moer_status moer_spectral_groups(const moer_dims* d, const int32_t* affinity, int32_t G, int32_t* group_of,
+                                 int32_t* knee, double* u_curve, double* s_curve, void* ws, size_t ws_bytes,
+                                 moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (d->E > 128 || G < 2 || G > 31 || G > d->E) return MOER_ERANGE;
+  if (affinity == nullptr || group_of == nullptr || knee == nullptr || u_curve == nullptr || s_curve == nullptr)
+    return MOER_EINVAL;
+  if (!aligned(affinity, 4) || !aligned(group_of, 4) || !aligned(knee, 4) || !aligned(u_curve, 8) ||
+      !aligned(s_curve, 8))
+    return MOER_EINVAL;
+  if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
+  if (ws_bytes < moer_spectral_workspace_bytes(d, G)) return MOER_ENOMEM;
+  return moer::spectral_launch(d, affinity, G, group_of, knee, u_curve, s_curve, ws,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t moer_kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D) {
