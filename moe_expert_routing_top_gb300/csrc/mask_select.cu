@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint
   __shared__ double red[3][MS_STATS_THREADS / 32];
   const int r = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t0 = req_off[r], t1 = req_off[r + 1];
-  double* out = stats + ((size_t)r * L + l) * 3;
+  const int R = gridDim.x;
+  double* out = stats + ((size_t)l * R + r) * 3;  // layer-major: the greedy's lanes read consecutive requests
   if (t0 < 0 || t1 < t0 || t1 > T) {
     if (tid == 0) {
       out[0] = out[1] = out[2] = 0.0;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(MS_GREEDY_THREADS, 1)
       double acc = 0.0;
       if (!taken[l]) {
         for (int r = lane; r < R; r += 32) {
-          const double* s = stats + ((size_t)r * L + l) * 3;
+          const double* s = stats + ((size_t)l * R + r) * 3;
           const double* u = run + (size_t)r * 3;
           acc += ms_cos(u[0] + s[0], u[1] + s[1], u[2] + s[2]);
         }
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(MS_GREEDY_THREADS, 1)
     __syncthreads();
     const int best = s_best;
     for (int r = tid; r < R; r += MS_GREEDY_THREADS) {
-      const double* s = stats + ((size_t)r * L + best) * 3;
+      const double* s = stats + ((size_t)best * R + r) * 3;
       double* u = run + (size_t)r * 3;
       u[0] += s[0];
       u[1] += s[1];

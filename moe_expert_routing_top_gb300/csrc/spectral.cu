@@ -23,9 +23,15 @@
 // Design (GB300):
 //   * spec_embed_kernel, one CTA per layer: M lives in shared memory (fp64,
 //     128 KB at E = 128); parallel cyclic Jacobi with the round-robin pairing,
-//     E/2 disjoint rotations per round (rows, then columns and the eigenvector
-//     matrix in global memory), until the off-diagonal mass is below 1e-30 of
-//     the total; the G largest diagonal entries pick the columns.
+//     E/2 disjoint rotations per round (rows, then columns with the pairs
+//     fastest so a warp touches 32 different columns, and the eigenvector
+//     matrix, kept transposed in global memory so its update is coalesced),
+//     until the off-diagonal mass is below 1e-30 of the total; the G largest
+//     diagonal entries pick the columns.  A full solve rather than an
+//     iteration on the top-G subspace: the co-activation spectra of real
+//     layers are nearly degenerate just below the leading eigenvalues, where
+//     subspace iteration needs 10^4 - 10^5 steps, while Jacobi's accuracy
+//     (backward stable) only needs the gap at the G-th eigenvalue.
 //   * spec_group_kernel, one CTA per (grid point, layer): the size-bounded
 //     assignment is a transportation problem with lower and upper bounds; one
 //     warp keeps a feasible assignment and cancels negative cycles of the
@@ -133,16 +139,21 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
         M[q * E + j] = s * mp + c * mq;
       }
       __syncthreads();
-      for (int w = tid; w < (E / 2) * E; w += nt) {  // columns p, q, and the eigenvectors
-        const int i = w / E, j = w - i * E;
+      for (int w = tid; w < (E / 2) * E; w += nt) {  // columns p, q: pairs fastest (distinct banks)
+        const int i = w % (E / 2), j = w / (E / 2);
         const int p = pp[i], q = qq[i];
         const double c = cs[i], s = sn[i];
         const double mp = M[j * E + p], mq = M[j * E + q];
         M[j * E + p] = c * mp - s * mq;
         M[j * E + q] = s * mp + c * mq;
-        const double vp = Vl[(size_t)j * E + p], vq = Vl[(size_t)j * E + q];
-        Vl[(size_t)j * E + p] = c * vp - s * vq;
-        Vl[(size_t)j * E + q] = s * vp + c * vq;
+      }
+      for (int w = tid; w < (E / 2) * E; w += nt) {  // eigenvectors, stored transposed: rows p, q
+        const int i = w / E, j = w - i * E;
+        const int p = pp[i], q = qq[i];
+        const double c = cs[i], s = sn[i];
+        const double vp = Vl[(size_t)p * E + j], vq = Vl[(size_t)q * E + j];
+        Vl[(size_t)p * E + j] = c * vp - s * vq;
+        Vl[(size_t)q * E + j] = s * vp + c * vq;
       }
       __syncthreads();
     }
@@ -156,8 +167,8 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
       const double lb = M[b * E + b];
       rank += (lb > la || (lb == la && b < a)) ? 1 : 0;
     }
-    if (rank < G)
-      for (int e = 0; e < E; ++e) U[(size_t)e * G + rank] = Vl[(size_t)e * E + a];
+    if (rank < G)  // eigenvector a is row a of the transposed matrix
+      for (int e = 0; e < E; ++e) U[(size_t)e * G + rank] = Vl[(size_t)a * E + e];
   }
   __syncthreads();
   for (int e = tid; e < E; e += nt) {  // unit rows
