@@ -17,16 +17,17 @@
 // idf): quality(M) = mean_r S12 / sqrt(S11 S22) with S = sum over l in M.
 //   * mask_stats_kernel: one CTA per (request, layer); the two halves' ids go
 //     into shared-memory histograms, then the three sums in fp64.
-//   * mask_greedy_kernel: one CTA; per step one warp per candidate layer, the
-//     lanes over the requests (running sums of the chosen layers + the
-//     candidate's), a warp reduction, and the argmax; then the chosen layer's
-//     sums are added to every request's running sums.
+//   * per greedy step, mask_eval_kernel (one CTA per candidate layer, threads
+//     over the requests: running sums of the chosen layers + the candidate's,
+//     fp64 cosines, a block reduction) and mask_pick_kernel (the argmax, then
+//     the chosen layer's sums added to every request's running sums).  The fp64
+//     square roots and divisions are spread over L SMs instead of one.
 #include "common.cuh"
 
 namespace moer {
 
 constexpr int MS_STATS_THREADS = 128;
-constexpr int MS_GREEDY_THREADS = 1024;
+constexpr int MS_EVAL_THREADS = 256;
 
 __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint8_t* __restrict__ topk, int64_t T,
                                                                       int k, int E, int L,
@@ -90,56 +91,72 @@ __device__ __forceinline__ double ms_cos(double s11, double s22, double s12) {
   return (s11 > 0.0 && s22 > 0.0) ? s12 / sqrt(s11 * s22) : 0.0;
 }
 
-// run [R][3] running sums of the chosen layers (zeroed by the host).
-__global__ void __launch_bounds__(MS_GREEDY_THREADS, 1)
-    mask_greedy_kernel(const double* __restrict__ stats, int R, int L, int m, double* __restrict__ run,
-                       int32_t* __restrict__ mask_out, double* __restrict__ quality_out) {
-  __shared__ double qual[256];
-  __shared__ unsigned char taken[256];
-  __shared__ int s_best;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int l = tid; l < L; l += MS_GREEDY_THREADS) taken[l] = 0;
-  __syncthreads();
-  for (int step = 0; step < m; ++step) {
-    for (int l = warp; l < L; l += MS_GREEDY_THREADS / 32) {
-      double acc = 0.0;
-      if (!taken[l]) {
-        for (int r = lane; r < R; r += 32) {
-          const double* s = stats + ((size_t)l * R + r) * 3;
-          const double* u = run + (size_t)r * 3;
-          acc += ms_cos(u[0] + s[0], u[1] + s[1], u[2] + s[2]);
-        }
-      }
+// One greedy step, part 1: CTA l evaluates quality(M + {l}) for a layer l not
+// chosen yet -- the mean over requests of the cosine from the running sums of
+// the chosen layers plus layer l's sums.  run [R][3] is zeroed by the host.
+__global__ void __launch_bounds__(MS_EVAL_THREADS) mask_eval_kernel(const double* __restrict__ stats, int R,
+                                                                    const double* __restrict__ run,
+                                                                    const unsigned char* __restrict__ taken,
+                                                                    double* __restrict__ qual) {
+  __shared__ double red[MS_EVAL_THREADS / 32];
+  const int l = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (taken[l]) {  // never picked again
+    if (tid == 0) qual[l] = -INFINITY;
+    return;
+  }
+  double acc = 0.0;
+  for (int r = tid; r < R; r += MS_EVAL_THREADS) {
+    const double* s = stats + ((size_t)l * R + r) * 3;
+    const double* u = run + (size_t)r * 3;
+    acc += ms_cos(u[0] + s[0], u[1] + s[1], u[2] + s[2]);
+  }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
-      if (lane == 0) qual[l] = acc / (double)R;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int best = -1;
-      for (int l = 0; l < L; ++l)
-        if (!taken[l] && (best < 0 || qual[l] > qual[best])) best = l;
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    double sum = 0.0;
+    for (int w = 0; w < MS_EVAL_THREADS / 32; ++w) sum += red[w];
+    qual[l] = sum / (double)R;
+  }
+}
+
+// Part 2: the best layer not chosen yet (ties: the lower layer; chosen layers
+// read -inf) joins the mask -- every CTA finds the same one from the read-only
+// qualities, CTA 0 records it -- and its sums join every request's running sums.
+__global__ void __launch_bounds__(MS_EVAL_THREADS) mask_pick_kernel(const double* __restrict__ stats, int R, int L,
+                                                                    double* __restrict__ run,
+                                                                    unsigned char* __restrict__ taken,
+                                                                    const double* __restrict__ qual, int step,
+                                                                    int32_t* __restrict__ mask_out,
+                                                                    double* __restrict__ quality_out) {
+  __shared__ int s_best;
+  if (threadIdx.x == 0) {
+    int best = 0;
+    for (int l = 1; l < L; ++l)
+      if (qual[l] > qual[best]) best = l;
+    s_best = best;
+    if (blockIdx.x == 0) {
       taken[best] = 1;
-      s_best = best;
       mask_out[step] = best;
       if (quality_out != nullptr) quality_out[step] = qual[best];
     }
-    __syncthreads();
-    const int best = s_best;
-    for (int r = tid; r < R; r += MS_GREEDY_THREADS) {
-      const double* s = stats + ((size_t)best * R + r) * 3;
-      double* u = run + (size_t)r * 3;
-      u[0] += s[0];
-      u[1] += s[1];
-      u[2] += s[2];
-    }
-    __syncthreads();
+  }
+  __syncthreads();
+  const int best = s_best;
+  for (int r = blockIdx.x * MS_EVAL_THREADS + threadIdx.x; r < R; r += gridDim.x * MS_EVAL_THREADS) {
+    const double* s = stats + ((size_t)best * R + r) * 3;
+    double* u = run + (size_t)r * 3;
+    u[0] += s[0];
+    u[1] += s[1];
+    u[2] += s[2];
   }
 }
 
 size_t mask_select_workspace_bytes(int32_t L, int32_t R) {
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
-  return WS_HEADER + r256((size_t)R * L * 3 * sizeof(double)) + r256((size_t)R * 3 * sizeof(double));
+  return WS_HEADER + r256((size_t)R * L * 3 * sizeof(double)) + r256((size_t)R * 3 * sizeof(double)) +
+         r256((size_t)L * sizeof(double)) + r256((size_t)L);
 }
 
 moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off, int32_t R,
@@ -149,10 +166,18 @@ moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t 
   char* w = static_cast<char*>(ws);
   double* stats = reinterpret_cast<double*>(w + WS_HEADER);
   double* run = reinterpret_cast<double*>(w + WS_HEADER + r256((size_t)R * d->L * 3 * sizeof(double)));
+  double* qual = reinterpret_cast<double*>(reinterpret_cast<char*>(run) + r256((size_t)R * 3 * sizeof(double)));
+  unsigned char* taken = reinterpret_cast<unsigned char*>(qual) + r256((size_t)d->L * sizeof(double));
   if (cudaMemsetAsync(run, 0, (size_t)R * 3 * sizeof(double), st) != cudaSuccess) return MOER_ECUDA;
+  if (cudaMemsetAsync(taken, 0, (size_t)d->L, st) != cudaSuccess) return MOER_ECUDA;
   mask_stats_kernel<<<dim3((unsigned)R, (unsigned)d->L), MS_STATS_THREADS, 0, st>>>(
       topk, T, d->k, d->E, d->L, req_off, idf, stats, reinterpret_cast<uint32_t*>(ws));
-  mask_greedy_kernel<<<1, MS_GREEDY_THREADS, 0, st>>>(stats, R, d->L, m, run, mask_out, quality_out);
+  const unsigned pick_grid = (unsigned)min64(((int64_t)R + MS_EVAL_THREADS - 1) / MS_EVAL_THREADS, 64);
+  for (int step = 0; step < m; ++step) {
+    mask_eval_kernel<<<d->L, MS_EVAL_THREADS, 0, st>>>(stats, R, run, taken, qual);
+    mask_pick_kernel<<<pick_grid, MS_EVAL_THREADS, 0, st>>>(stats, R, d->L, run, taken, qual, step, mask_out,
+                                                            quality_out);
+  }
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
