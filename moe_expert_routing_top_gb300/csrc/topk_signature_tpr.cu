@@ -9,9 +9,9 @@
 // Figure 2(a) (per-layer expert co-activation).
 //
 // Design (GB300):
-//   * Persistent grid, one CTA per SM: one producer warp and ten consumer
+//   * Persistent grid, one CTA per SM: one producer warp and twelve consumer
 //     warps.  Work items are (layer, 32-token tile); tile n of the CTA goes to
-//     consumer warp n % 10 and to that warp's own ring stage (one
+//     consumer warp n % 12 and to that warp's own ring stage (one
 //     cp.async.bulk copy of 32 contiguous logit rows, completing on an
 //     mbarrier).  Stages are never shared between consumer warps, so each
 //     warp meets its stages' barrier phases strictly in order.
@@ -32,10 +32,12 @@
 //     Rows that fail (ties, NaN, +-inf, zeros, negatives in the top k) are
 //     redone exactly by the whole warp with the ballot tie-breaking path.
 //   * Co-activation: each lane adds its row's k(k-1)/2 rank-ordered pairs to
-//     a shared-memory E x E int32 tile of directed counts with shared atomics
-//     (28 adds per row at k = 8 instead of the 64 of the full k x k block);
-//     the consumer warps fold the tile into the symmetric co-activation,
-//     diagonal included, and add it to global memory at each layer change.
+//     a shared-memory tile of directed counts with shared atomics (28 adds per
+//     row at k = 8 instead of the 64 of the full k x k block), 16 bits per
+//     count so the tile takes 32 KB and the ring 192 KB; the consumer warps
+//     fold the tile into the symmetric co-activation, diagonal included, and
+//     add it to global memory at each layer change and at least every 2047
+//     tiles (65504 rows), before any count could overflow.
 //   * The top-k ids go out as 8 (or 6) bytes per row; the per-KV-block
 //     counts are computed from them by block_counts.cu.
 #include <climits>
@@ -50,10 +52,13 @@ namespace moer {
 #define MOER_TPR_LPR 1
 #endif
 #ifndef MOER_TPR_CW
-#define MOER_TPR_CW 10
+#define MOER_TPR_CW 12
 #endif
 #ifndef MOER_TPR_STAGE_KB
-#define MOER_TPR_STAGE_KB 160
+#define MOER_TPR_STAGE_KB 192
+#endif
+#ifndef MOER_TPR_FOLD_ROWS
+#define MOER_TPR_FOLD_ROWS 65535  // rows between folds of the 16-bit co-activation tile
 #endif
 
 template <int E>
@@ -75,7 +80,12 @@ struct TprGeo {
   static constexpr size_t STAGE_BYTES = (size_t)TT * E * 4;
   static constexpr size_t OFF_ROWS = 0;
   static constexpr size_t OFF_AFF = OFF_ROWS + STAGES * STAGE_BYTES;
-  static constexpr size_t AFF_WORDS = (size_t)E * E;
+  // directed pair counts, 16 bits each, two per word (D[a][b] is half (b & 1)
+  // of word (a E + b) / 2); the tile is folded into global memory at least
+  // every FT tiles, so no count passes 65535 (a count grows once per row at most)
+  static constexpr size_t AFF_WORDS = (size_t)E * E / 2;
+  static constexpr int FT = MOER_TPR_FOLD_ROWS / TT;
+  static_assert(MOER_TPR_FOLD_ROWS <= 65535, "16-bit counts: at most 65535 rows between folds");
   static constexpr size_t OFF_RSUM = OFF_AFF + AFF_WORDS * 4;  // E row sums used by the flush
   static constexpr size_t OFF_BAR = OFF_RSUM + (size_t)E * 4;
   static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8;
@@ -253,22 +263,25 @@ __device__ void tpr_producer(const K1Params& p, char* smem, int64_t i0, int64_t 
 }
 
 // -------------------------------------------------------------- consumers
+// Directed pair count D[a][b]: 16-bit half (b & 1) of word (a E + b) / 2.
+__device__ __forceinline__ uint32_t aff_get(const uint32_t* aff, int c) { return (aff[c >> 1] >> ((c & 1) << 4)) & 0xFFFFu; }
+
 // The shared tile holds directed pair counts D[a][b] = # rows of this CTA's
-// current layer in which expert a ranks above expert b.  Co-activation is
-// symmetric: A[a][b] = D[a][b] + D[b][a] for a != b, and, every row holding
-// k distinct experts, the diagonal (the expert's load) is its off-diagonal
-// row sum divided by k - 1.  Adds the tile to layer `layer` of the global
-// co-activation and clears it.  All consumer threads call this (it holds a
-// barrier); `skip` leaves the tile alone (a consumer warp timed out).
+// current layer (since the last fold) in which expert a ranks above expert b.
+// Co-activation is symmetric: A[a][b] = D[a][b] + D[b][a] for a != b, and,
+// every row holding k distinct experts, the diagonal (the expert's load) is
+// its off-diagonal row sum divided by k - 1.  Adds the tile to layer `layer`
+// of the global co-activation and clears it.  All consumer threads call this
+// (it holds a barrier); `skip` leaves the tile alone (a consumer warp timed out).
 template <int E, int K>
-__device__ void tpr_flush_aff(const K1Params& p, int* aff, int* rsum, int layer, bool skip) {
+__device__ void tpr_flush_aff(const K1Params& p, uint32_t* aff, int* rsum, int layer, bool skip) {
   using G = TprGeo<E>;
   int32_t* dst = p.affinity + (size_t)layer * E * E;
   if (!skip) {
     for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) {
       const int a = c / E, b = c % E;
       if (a < b) {
-        const int v = aff[a * E + b] + aff[b * E + a];
+        const int v = (int)(aff_get(aff, a * E + b) + aff_get(aff, b * E + a));
         if (v != 0) {
           atomicAdd(&dst[a * E + b], v);
           atomicAdd(&dst[b * E + a], v);
@@ -287,7 +300,7 @@ __device__ void tpr_flush_aff(const K1Params& p, int* aff, int* rsum, int layer,
         rsum[a] = 0;
       }
     }
-    for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) aff[c] = 0;
+    for (int c = threadIdx.x; c < (int)G::AFF_WORDS; c += G::CTHREADS) aff[c] = 0u;
   }
 }
 
@@ -300,14 +313,20 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rrow = lane / LPR, h = lane % LPR, rot = lane & 7;
   const float* rows = reinterpret_cast<const float*>(smem + G::OFF_ROWS);
-  int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
+  uint32_t* aff = reinterpret_cast<uint32_t*>(smem + G::OFF_AFF);
   int* rsum = reinterpret_cast<int*>(smem + G::OFF_RSUM);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   uint64_t* empty = full + G::STAGES;
   const bool aff_on = p.affinity != nullptr;
   const int64_t N = i1 - i0;
-  const int l_first = (int)(i0 / p.ntiles), l_last = (int)((i1 - 1) / p.ntiles);
-  int cur = l_first;
+  // fold epochs: (layer, tile / FT), numbered l * epl + tile / FT, monotone in the item
+  const int epl = (p.ntiles + G::FT - 1) / G::FT;
+  auto epoch_of = [&](int64_t item) {
+    const int li = (int)(item / p.ntiles);
+    return (int64_t)li * epl + (item - (int64_t)li * p.ntiles) / G::FT;
+  };
+  const int64_t ep_last = epoch_of(i1 - 1);
+  int64_t cur = epoch_of(i0);
   bool dead = false;
   int l = (int)((i0 + warp) / p.ntiles);
   int tile = (int)((i0 + warp) - (int64_t)l * p.ntiles);
@@ -319,13 +338,14 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
         ++l;
       }
     }
-    while (aff_on && cur < l) {
+    const int64_t ep = (int64_t)l * epl + tile / G::FT;
+    while (aff_on && cur < ep) {
       named_bar(1, G::CTHREADS);
-      tpr_flush_aff<E, K>(p, aff, rsum, cur, dead);
+      tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
       named_bar(1, G::CTHREADS);
       ++cur;
     }
-    cur = l;
+    cur = ep;
     if (dead) continue;
     const int s = G::stage_of(n);
     if (!mbar_wait(&full[s], (uint32_t)((n / G::STAGES) & 1), p.status)) {
@@ -383,14 +403,22 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
         }
       }
       if (aff_on) {
-        // directed pairs (rank i above rank j): k(k-1)/2 adds per row; with
-        // two lanes per row, lane h takes the ranks i with i % 2 == h
+        // directed pairs (rank i above rank j): k(k-1)/2 adds per row into the
+        // packed 16-bit counts; with two lanes per row, lane h takes the ranks
+        // i with i % 2 == h
+        int wj[K];
+        uint32_t sj[K];
+#pragma unroll
+        for (int j = 1; j < K; ++j) {
+          wj[j] = idx[j] >> 1;
+          sj[j] = 1u << ((idx[j] & 1) << 4);
+        }
 #pragma unroll
         for (int i = 0; i < K - 1; ++i) {
           if (i % LPR == h) {
-            int* ra = aff + idx[i] * E;
+            uint32_t* ra = aff + idx[i] * (E / 2);
 #pragma unroll
-            for (int j = i + 1; j < K; ++j) atomicAdd(ra + idx[j], 1);
+            for (int j = i + 1; j < K; ++j) atomicAdd(ra + wj[j], sj[j]);
           }
         }
       }
@@ -408,7 +436,10 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
           const int q = base + lane;
           const int ia = __shfl_sync(FULL, e, q < K * K ? q / K : 0);
           const int ib = __shfl_sync(FULL, e, q < K * K ? q % K : 0);
-          if (q < K * K && q / K < q % K) atomicAdd(&aff[ia * E + ib], 1);
+          if (q < K * K && q / K < q % K) {
+            const int c = ia * E + ib;
+            atomicAdd(&aff[c >> 1], 1u << ((c & 1) << 4));
+          }
         }
       }
     }
@@ -416,14 +447,14 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     if (lane == 0) mbar_arrive(&empty[s]);
   }
   if (aff_on) {
-    while (cur < l_last) {
+    while (cur < ep_last) {
       named_bar(1, G::CTHREADS);
-      tpr_flush_aff<E, K>(p, aff, rsum, cur, dead);
+      tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
       named_bar(1, G::CTHREADS);
       ++cur;
     }
     named_bar(1, G::CTHREADS);
-    tpr_flush_aff<E, K>(p, aff, rsum, cur, dead);
+    tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
   }
 }
 
@@ -435,8 +466,8 @@ __global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __g
   const int64_t i1 = ((int64_t)blockIdx.x + 1) * p.nitems / gridDim.x;
   if (i1 <= i0) return;
   if (p.affinity != nullptr) {
-    int* aff = reinterpret_cast<int*>(smem + G::OFF_AFF);
-    for (size_t w = threadIdx.x; w < G::AFF_WORDS + E; w += G::THREADS) aff[w] = 0;  // tile and row sums
+    uint32_t* aff = reinterpret_cast<uint32_t*>(smem + G::OFF_AFF);
+    for (size_t w = threadIdx.x; w < G::AFF_WORDS + E; w += G::THREADS) aff[w] = 0u;  // tile and row sums
   }
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   if (threadIdx.x == 0) {
