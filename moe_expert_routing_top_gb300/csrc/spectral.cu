@@ -26,7 +26,9 @@
 //     E/2 disjoint rotations per round (rows, then columns with the pairs
 //     fastest so a warp touches 32 different columns, and the eigenvector
 //     matrix, kept transposed in global memory so its update is coalesced),
-//     until the off-diagonal mass is below 1e-30 of the total; the G largest
+//     until a sweep finds every off-diagonal entry negligible against its
+//     diagonal pair (|a_pq| <= 1e-15 sqrt|a_pp a_qq|: threshold Jacobi, which
+//     stops at the rounding floor instead of chasing it); the G largest
 //     diagonal entries pick the columns.  A full solve rather than an
 //     iteration on the top-G subspace: the co-activation spectra of real
 //     layers are nearly degenerate just below the leading eigenvalues, where
@@ -55,18 +57,6 @@ constexpr int SP_MAX_STEPS = 100;
 
 __device__ __forceinline__ int sp_seq(int j, int r, int E) { return j == 0 ? 0 : ((j - 1 + r) % (E - 1)) + 1; }
 
-__device__ double sp_block_sum(double v, double* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  double s = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-  return s;
-}
-
 __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     spec_embed_kernel(const int32_t* __restrict__ affinity, int E, int G, double* __restrict__ V,
                       double* __restrict__ Uo, double* __restrict__ deg_out) {
@@ -90,39 +80,32 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     inv[a] = d > 0 ? 1.0 / sqrt((double)d) : 0.0;
   }
   __syncthreads();
-  double f = 0.0;
   for (int q = tid; q < E * E; q += nt) {
     const int a = q / E, b = q - a * E;
     const int32_t x = A[q] > 0 ? A[q] : 0;
-    const double m = (a == b) ? 0.0 : inv[a] * (double)x * inv[b];
-    M[q] = m;
+    M[q] = (a == b) ? 0.0 : inv[a] * (double)x * inv[b];
     Vl[q] = (a == b) ? 1.0 : 0.0;
-    f += m * m;
   }
-  const double fro2 = sp_block_sum(f, red);
+  __syncthreads();
+  // threshold Jacobi: a rotation is skipped when |a_pq| <= 1e-15 sqrt(|a_pp a_qq|)
+  // (negligible against the diagonal); the solve ends after a sweep that rotates nothing
   for (int sweep = 0; sweep < SP_MAX_SWEEPS; ++sweep) {
-    double o = 0.0;
-    for (int q = tid; q < E * E; q += nt) {
-      const int a = q / E, b = q - a * E;
-      if (a != b) o += M[q] * M[q];
-    }
-    const double off = sp_block_sum(o, red);
-    if (tid == 0) s_done = off <= 1e-30 * fro2;
+    if (tid == 0) s_done = 1;
     __syncthreads();
-    if (s_done) break;
     for (int r = 0; r < E - 1; ++r) {
       if (tid < E / 2) {
         const int p = sp_seq(tid, r, E), q = sp_seq(E - 1 - tid, r, E);
-        const double apq = M[p * E + q];
+        const double apq = M[p * E + q], app = M[p * E + p], aqq = M[q * E + q];
         double c = 1.0, s = 0.0;
-        if (fabs(apq) > 1e-300) {
-          const double th = (M[q * E + q] - M[p * E + p]) / (2.0 * apq);
+        if (fabs(apq) > 1e-15 * sqrt(fabs(app * aqq)) && fabs(apq) > 1e-300) {
+          const double th = (aqq - app) / (2.0 * apq);
           double t;
           if (fabs(th) > 1e150) t = 1.0 / (2.0 * th);
           else if (th == 0.0) t = 1.0;
           else t = (th > 0.0 ? 1.0 : -1.0) / (fabs(th) + sqrt(th * th + 1.0));
           c = 1.0 / sqrt(1.0 + t * t);
           s = t * c;
+          s_done = 0;
         }
         pp[tid] = p;
         qq[tid] = q;
@@ -157,6 +140,9 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
       }
       __syncthreads();
     }
+    const bool stop = s_done != 0;  // read by every thread before thread 0 resets it
+    __syncthreads();
+    if (stop) break;
   }
   // the G largest eigenvalues (ties: lower index) pick the embedding's columns
   double* U = Uo + (size_t)l * E * G;
