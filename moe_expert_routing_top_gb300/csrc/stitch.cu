@@ -7,70 +7,98 @@
 // signature.  Full computed blocks are inserted first; then each request's
 // counts are the sum over its cached prefix blocks and its computed blocks.
 //
-// Both kernels move 32-bit words of packed 8-bit counts (four experts per
-// word); a request's record of m*E counts is handled by one CTA whose threads
-// own consecutive words, so every load and store is coalesced.
+// Both kernels move 16-byte words of packed 8-bit counts (sixteen experts per
+// word; 4-byte words when a record or buffer is not 16-byte aligned): the
+// insert copies one block record per warp, and a request's record of m*E
+// counts is summed by one CTA whose threads own consecutive words, so every
+// load and store is coalesced.
 #include "common.cuh"
 
 namespace moer {
 
-__global__ void stitch_insert(const uint32_t* __restrict__ blk_w, const int32_t* __restrict__ blk_tab,
-                              int nblk, int B, const int32_t* __restrict__ insert_slot,
-                              uint32_t* __restrict__ cache_w, int nslots, int rec_words,
-                              uint32_t* status) {
-  const int64_t total = (int64_t)nblk * rec_words;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int b = (int)(i / rec_words);
-    const int w = (int)(i - (int64_t)b * rec_words);
+// One warp per KV block: the slot is checked once, the record is copied with
+// 16-byte (V = uint4) or 4-byte (V = uint32_t) words.
+template <typename V>
+__global__ void stitch_insert(const V* __restrict__ blk_w, const int32_t* __restrict__ blk_tab, int nblk, int B,
+                              const int32_t* __restrict__ insert_slot, V* __restrict__ cache_w, int nslots,
+                              int rec_v, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblk; b += stride) {
     const int slot = insert_slot[b];
     if (slot < 0 || blk_tab[2 * b + 1] != B) continue;
     if (slot >= nslots) {
-      if (status != nullptr && w == 0) atomicOr(status, WS_BIT_EDATA);
+      if (status != nullptr && lane == 0) atomicOr(status, WS_BIT_EDATA);
       continue;
     }
-    cache_w[(size_t)slot * rec_words + w] = blk_w[(size_t)b * rec_words + w];
+    const V* src = blk_w + (size_t)b * rec_v;
+    V* dst = cache_w + (size_t)slot * rec_v;
+    for (int w = lane; w < rec_v; w += 32) dst[w] = src[w];
   }
 }
 
-__global__ void stitch_sum(const uint32_t* __restrict__ blk_w, int nblk,
-                           const int32_t* __restrict__ req_blk_off,
-                           const int32_t* __restrict__ cache_idx,
-                           const int32_t* __restrict__ req_cache_off,
-                           const uint32_t* __restrict__ cache_w, int nslots, int rec_words,
-                           int32_t* __restrict__ req_cnt, uint32_t* status) {
+__device__ __forceinline__ void acc4(uint32_t (&a)[4], uint32_t v) {
+  a[0] += v & 0xFFu;
+  a[1] += (v >> 8) & 0xFFu;
+  a[2] += (v >> 16) & 0xFFu;
+  a[3] += v >> 24;
+}
+__device__ __forceinline__ void accv(uint32_t (&a)[4], uint32_t v) { acc4(a, v); }
+__device__ __forceinline__ void accv(uint32_t (&a)[16], uint4 v) {
+  uint32_t* q = a;
+  acc4(*reinterpret_cast<uint32_t(*)[4]>(q), v.x);
+  acc4(*reinterpret_cast<uint32_t(*)[4]>(q + 4), v.y);
+  acc4(*reinterpret_cast<uint32_t(*)[4]>(q + 8), v.z);
+  acc4(*reinterpret_cast<uint32_t(*)[4]>(q + 12), v.w);
+}
+
+// One CTA per request: thread w owns word w of the record (16 or 4 bytes of
+// packed 8-bit counts) and sums it over the request's cached and computed
+// blocks, four block loads in flight at a time.
+template <typename V, int NB>
+__global__ void stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t* __restrict__ req_blk_off,
+                           const int32_t* __restrict__ cache_idx, const int32_t* __restrict__ req_cache_off,
+                           const V* __restrict__ cache_w, int nslots, int rec_v, int32_t* __restrict__ req_cnt,
+                           uint32_t* status) {
   const int r = blockIdx.x;
   const int b0 = req_blk_off[r], b1 = req_blk_off[r + 1];
   const int c0 = cache_w ? req_cache_off[r] : 0, c1 = cache_w ? req_cache_off[r + 1] : 0;
   const bool bad_blocks = b0 < 0 || b1 < b0 || b1 > nblk;
   if (bad_blocks && threadIdx.x == 0 && status != nullptr) atomicOr(status, WS_BIT_EDATA);
-  for (int w = threadIdx.x; w < rec_words; w += blockDim.x) {
-    uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  for (int w = threadIdx.x; w < rec_v; w += blockDim.x) {
+    uint32_t a[NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) a[i] = 0u;
     for (int c = c0; c < c1; ++c) {
       const int slot = cache_idx[c];
       if (slot < 0 || slot >= nslots) {
         if (status != nullptr && w == 0) atomicOr(status, WS_BIT_EDATA);
         continue;
       }
-      const uint32_t v = cache_w[(size_t)slot * rec_words + w];
-      a0 += v & 0xFFu;
-      a1 += (v >> 8) & 0xFFu;
-      a2 += (v >> 16) & 0xFFu;
-      a3 += v >> 24;
+      accv(a, cache_w[(size_t)slot * rec_v + w]);
     }
-    if (!bad_blocks)
-      for (int b = b0; b < b1; ++b) {
-        const uint32_t v = blk_w[(size_t)b * rec_words + w];
-        a0 += v & 0xFFu;
-        a1 += (v >> 8) & 0xFFu;
-        a2 += (v >> 16) & 0xFFu;
-        a3 += v >> 24;
+    if (!bad_blocks) {
+      int b = b0;
+      for (; b + 4 <= b1; b += 4) {
+        const V v0 = blk_w[(size_t)b * rec_v + w], v1 = blk_w[(size_t)(b + 1) * rec_v + w];
+        const V v2 = blk_w[(size_t)(b + 2) * rec_v + w], v3 = blk_w[(size_t)(b + 3) * rec_v + w];
+        accv(a, v0);
+        accv(a, v1);
+        accv(a, v2);
+        accv(a, v3);
       }
-    int32_t* dst = req_cnt + (size_t)r * rec_words * 4 + (size_t)w * 4;
-    dst[0] = (int32_t)a0;
-    dst[1] = (int32_t)a1;
-    dst[2] = (int32_t)a2;
-    dst[3] = (int32_t)a3;
+      for (; b < b1; ++b) accv(a, blk_w[(size_t)b * rec_v + w]);
+    }
+    int32_t* dst = req_cnt + (size_t)r * rec_v * NB + (size_t)w * NB;
+    if constexpr (NB == 16) {
+      int4* d4 = reinterpret_cast<int4*>(dst);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        d4[i] = make_int4((int)a[4 * i], (int)a[4 * i + 1], (int)a[4 * i + 2], (int)a[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < NB; ++i) dst[i] = (int32_t)a[i];
+    }
   }
 }
 
@@ -79,20 +107,38 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
                                 const int32_t* cache_idx, const int32_t* req_cache_off,
                                 uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
                                 int32_t* req_cnt, uint32_t* status, cudaStream_t st) {
-  const int rec_words = d->m * d->E / 4;
+  const int rec_bytes = d->m * d->E;
+  auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  // 16-byte words when every record, cache slot and request row stays 16-byte aligned
+  const bool v16 = rec_bytes % 16 == 0 && a16(blk_cnt) && (cache == nullptr || a16(cache)) && a16(req_cnt);
+  const int sms = device_sm_count();
+  if (sms <= 0) return MOER_ECUDA;
   if (cache != nullptr && insert_slot != nullptr && nblk > 0) {
-    const int64_t total = (int64_t)nblk * rec_words;
-    const int blocks = (int)min64((total + 255) / 256, 8192);
-    stitch_insert<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), blk_tab, nblk,
-                                          d->block, insert_slot, reinterpret_cast<uint32_t*>(cache),
-                                          nslots, rec_words, status);
+    const int grid = (int)min64(((int64_t)nblk + 7) / 8, (int64_t)sms * 8);
+    if (v16)
+      stitch_insert<uint4><<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(blk_cnt), blk_tab, nblk, d->block,
+                                                 insert_slot, reinterpret_cast<uint4*>(cache), nslots,
+                                                 rec_bytes / 16, status);
+    else
+      stitch_insert<uint32_t><<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), blk_tab, nblk,
+                                                    d->block, insert_slot, reinterpret_cast<uint32_t*>(cache),
+                                                    nslots, rec_bytes / 4, status);
     if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
   }
-  const int threads = rec_words >= 256 ? 256 : ((rec_words + 31) / 32) * 32;
-  stitch_sum<<<R, threads, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), nblk, req_blk_off,
-                                    cache_idx, req_cache_off,
-                                    reinterpret_cast<const uint32_t*>(cache), nslots, rec_words,
-                                    req_cnt, status);
+  if (v16) {
+    const int rec_v = rec_bytes / 16;
+    const int threads = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
+    stitch_sum<uint4, 16><<<R, threads, 0, st>>>(reinterpret_cast<const uint4*>(blk_cnt), nblk, req_blk_off,
+                                                 cache_idx, req_cache_off, reinterpret_cast<const uint4*>(cache),
+                                                 nslots, rec_v, req_cnt, status);
+  } else {
+    const int rec_v = rec_bytes / 4;
+    const int threads = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
+    stitch_sum<uint32_t, 4><<<R, threads, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), nblk, req_blk_off,
+                                                   cache_idx, req_cache_off,
+                                                   reinterpret_cast<const uint32_t*>(cache), nslots, rec_v,
+                                                   req_cnt, status);
+  }
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
