@@ -94,3 +94,66 @@ def test_workspace_size_covers_calls(nat):
     r = nat.moer_workspace_bytes(d, 0, 0, 14000, 16)
     both = nat.moer_workspace_bytes(d, 1305533, 82065, 14000, 16)
     assert both == max(t, r) and t >= 256 + 4 * (1305533 // 64)
+
+
+def test_gate_arguments(nat):
+    d = nat.make_dims(128, 8, 4, [0], 16)
+    g = nat.moer_gate_topk
+    ws = nat.moer_gate_workspace_bytes(d, 256)
+    assert _code(g, nat.make_dims(64, 8, 4, [0], 16), 64, 128, 256, 64, None, 0, None, 64, None, None, 256, ws, 0) == 3
+    assert _code(g, nat.make_dims(128, 7, 4, [0], 16), 64, 128, 256, 64, None, 0, None, 64, None, None, 256, ws, 0) == 3
+    assert _code(g, d, 64, 128, 100, 64, None, 0, None, 64, None, None, 256, ws, 0) == 3        # H % 64
+    assert _code(g, d, None, 128, 256, 64, None, 0, None, 64, None, None, 256, ws, 0) == 1     # no hidden
+    assert _code(g, d, 64, 128, 256, 64, None, 0, None, None, None, None, 256, ws, 0) == 1     # no top-k
+    assert _code(g, d, BADPTR, 128, 256, 64, None, 0, None, 64, None, None, 256, ws, 0) == 1   # misaligned
+    assert _code(g, d, 64, 128, 256, 64, None, 0, None, 64, None, None, 256, ws - 256, 0) == 5
+    g(d, 64, 0, 256, 64, None, 0, None, 64, None, None, 256, ws, 0)                            # T = 0: no-op
+
+
+def test_kmeans_arguments(nat):
+    k = nat.moer_kmeans_balanced
+    ws = nat.moer_kmeans_workspace_bytes(100, 32, 4)
+    assert ws > 256
+    assert _code(k, 64, 100, 32, 0, 64, 10, 64, 64, None, None, 256, ws, 0) == 3    # D = 0
+    assert _code(k, 64, 100, 32, 33, 64, 10, 64, 64, None, None, 256, ws, 0) == 3   # D > 32
+    assert _code(k, 64, 3, 32, 4, 64, 10, 64, 64, None, None, 256, ws, 0) == 3      # N < D
+    assert _code(k, 64, 100, 0, 4, 64, 10, 64, 64, None, None, 256, ws, 0) == 3     # dim = 0
+    assert _code(k, 64, 100, 32, 4, 64, 0, 64, 64, None, None, 256, ws, 0) == 3     # max_iter = 0
+    assert _code(k, None, 100, 32, 4, 64, 10, 64, 64, None, None, 256, ws, 0) == 1  # no signatures
+    assert _code(k, 64, 100, 32, 4, 64, 10, 64, 64, None, BADPTR, 256, ws, 0) == 1  # misaligned objective
+    assert _code(k, 64, 100, 32, 4, 64, 10, 64, 64, None, None, 256, ws - 8, 0) == 5
+
+
+def test_replication_arguments(nat):
+    d = nat.make_dims(128, 8, 4, [0], 16)
+    r = nat.moer_replication_plan
+    assert _code(r, d, 64, 64, 0, 64, 64, 64, 64, 64, 256, 256, 0) == 3      # G = 0
+    assert _code(r, d, 64, 64, 65, 64, 64, 64, 64, 64, 256, 256, 0) == 3     # G > 64
+    assert _code(r, d, None, 64, 8, 64, 64, 64, 64, 64, 256, 256, 0) == 1    # no loads
+    assert _code(r, d, BADPTR, 64, 8, 64, 64, 64, 64, 64, 256, 256, 0) == 1  # misaligned loads
+    assert _code(r, d, 64, 64, 8, 64, 64, 64, 64, 64, 256, 128, 0) == 5      # workspace
+
+
+def test_mask_select_arguments(nat):
+    d = nat.make_dims(128, 8, 4, [], 16)
+    m = nat.moer_mask_select
+    ws = nat.moer_mask_select_workspace_bytes(d, 10)
+    assert _code(m, d, 64, 100, 64, 10, None, 0, 64, None, 256, ws, 0) == 3     # m = 0
+    assert _code(m, d, 64, 100, 64, 10, None, 5, 64, None, 256, ws, 0) == 3     # m > L
+    assert _code(m, d, 64, 100, 64, 0, None, 2, 64, None, 256, ws, 0) == 3      # R = 0
+    assert _code(m, d, None, 100, 64, 10, None, 2, 64, None, 256, ws, 0) == 1   # no top-k
+    assert _code(m, d, 64, 100, 64, 10, None, 2, 64, None, 256, ws - 8, 0) == 5
+
+
+def test_spectral_arguments(nat):
+    s = nat.moer_spectral_groups
+    d = nat.make_dims(128, 8, 4, [], 16)
+    ws = nat.moer_spectral_workspace_bytes(d, 8)
+    big = nat.make_dims(256, 8, 4, [], 16)
+    assert _code(s, big, 64, 8, 64, 64, 64, 64, 256, ws, 0) == 3     # E > 128
+    assert _code(s, d, 64, 1, 64, 64, 64, 64, 256, ws, 0) == 3       # G < 2
+    assert _code(s, d, 64, 32, 64, 64, 64, 64, 256, ws, 0) == 3      # G > 31
+    assert _code(s, nat.make_dims(16, 8, 4, [], 16), 64, 17, 64, 64, 64, 64, 256, ws, 0) == 3  # G > E
+    assert _code(s, d, None, 8, 64, 64, 64, 64, 256, ws, 0) == 1     # no co-activation
+    assert _code(s, d, 64, 8, 64, 64, BADPTR, 64, 256, ws, 0) == 1   # misaligned curve
+    assert _code(s, d, 64, 8, 64, 64, 64, 64, 256, ws - 8, 0) == 5
