@@ -2,13 +2,15 @@
 // moer_topk_signature, shared by its host dispatch and both kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace moer {
 
 struct K1Params {
-  const float* logits;  // [L][T][E]
+  CUtensorMap tm_logits;  // the logits as a 3-D tiled map (thread-per-row kernel only)
+  const float* logits;    // [L][T][E]
   int64_t T;
   int E, k, L;
   uint8_t* ids;          // top-k ids out, or NULL: the caller's [L][T][k], or

@@ -9,35 +9,37 @@
 // Figure 2(a) (per-layer expert co-activation).
 //
 // Design (GB300):
-//   * Persistent grid, one CTA per SM: one producer warp and twelve consumer
-//     warps.  Work items are (layer, 32-token tile); tile n of the CTA goes to
-//     consumer warp n % 12 and to that warp's own ring stage (one
-//     cp.async.bulk copy of 32 contiguous logit rows, completing on an
-//     mbarrier).  Stages are never shared between consumer warps, so each
-//     warp meets its stages' barrier phases strictly in order.
-//   * One consumer lane per token row (two lanes per row is a build option:
-//     the halves are then merged across the lane pair with shuffles).  A lane
-//     reads its row from shared memory in 16-byte units whose order is
-//     XOR-rotated by (lane & 7), which makes every LDS.128 conflict-free, and
-//     folds it 8 values at a time into a sorted top-8 held in registers: an
-//     optimal 19-comparator sorting network per chunk, then a bitonic
-//     split/merge with the running top-8 (the split's losers, folded with
-//     3-input maxima, give the 9th-ranked key).  Keys are the float's upper
-//     24 bits (signed-int order equals value order for positive floats) with
-//     the value's position in the lane's read order in the low 8 bits, so
-//     keys are unique and min/max networks apply.
+//   * Persistent grid, one CTA per SM, sixteen warps, no producer warp.  Work
+//     items are (layer, 32-token tile); tile n of the CTA goes to warp n % 16.
+//     A tile is fetched in column slices (32 rows x 32 experts, 4 KB) by 3-D
+//     TMA tensor copies ([L][T][E] logits, rows past T zero-filled) into two
+//     slice buffers that the warp owns: as soon as the warp has folded a
+//     slice, its lane 0 issues the copy of the slice two ahead into the same
+//     buffer, so each copy lands while the other buffer is being folded.
+//     With one whole-tile stage per warp instead, a warp sat idle a quarter of
+//     its time waiting for its own refill.
+//   * One lane per token row.  A lane reads its row's slice from shared memory
+//     in 16-byte units whose order is XOR-rotated by (lane & 7), which makes
+//     every LDS.128 conflict-free, and folds it 8 values at a time into a
+//     sorted top-8 held in registers: an optimal 19-comparator sorting network
+//     per chunk, then a bitonic split/merge with the running top-8 (the
+//     split's losers, folded with 3-input maxima, give the 9th-ranked key).
+//     Keys are the float's upper 24 bits (signed-int order equals value order
+//     for positive floats) with the value's position in the lane's read order
+//     in the low 8 bits, so keys are unique and min/max networks apply.
 //   * A row's result is certified when its k leading keys are positive and
 //     finite and the k+1 leading keys are pairwise distinct in their upper
 //     24 bits (then truncation cannot have changed membership or order).
 //     Rows that fail (ties, NaN, +-inf, zeros, negatives in the top k) are
-//     redone exactly by the whole warp with the ballot tie-breaking path.
+//     redone exactly by the whole warp, from global memory, with the ballot
+//     tie-breaking path.
 //   * Co-activation: each lane adds its row's k(k-1)/2 rank-ordered pairs to
 //     a shared-memory tile of directed counts with shared atomics (28 adds per
-//     row at k = 8 instead of the 64 of the full k x k block), 16 bits per
-//     count so the tile takes 32 KB and the ring 192 KB; the consumer warps
-//     fold the tile into the symmetric co-activation, diagonal included, and
-//     add it to global memory at each layer change and at least every 2047
-//     tiles (65504 rows), before any count could overflow.
+//     row at k = 8 instead of the 64 of the full k x k block), 32 bits per
+//     count (66 KB with the bank padding; a 16-bit tile of half the size,
+//     folded every 65,535 rows, is a build option and costs more per add);
+//     the warps fold the tile into the symmetric co-activation, diagonal
+//     included, and add it to global memory at each layer change.
 //   * The top-k ids go out as 8 (or 6) bytes per row; the per-KV-block
 //     counts are computed from them by block_counts.cu.
 #include <climits>
@@ -48,14 +50,14 @@
 namespace moer {
 
 // Geometry (compile-time tunables with the measured defaults).
-#ifndef MOER_TPR_LPR
-#define MOER_TPR_LPR 1
-#endif
 #ifndef MOER_TPR_CW
-#define MOER_TPR_CW 12
+#define MOER_TPR_CW 16  // warps per CTA
 #endif
-#ifndef MOER_TPR_STAGE_KB
-#define MOER_TPR_STAGE_KB 192
+#ifndef MOER_TPR_RING
+#define MOER_TPR_RING 2  // slice buffers per warp
+#endif
+#ifndef MOER_TPR_AFF32
+#define MOER_TPR_AFF32 1  // 32-bit co-activation counts (else 16-bit, two per word)
 #endif
 #ifndef MOER_TPR_FOLD_ROWS
 #define MOER_TPR_FOLD_ROWS 65535  // rows between folds of the 16-bit co-activation tile
@@ -63,32 +65,32 @@ namespace moer {
 
 template <int E>
 struct TprGeo {
-  static constexpr int LPR = MOER_TPR_LPR;  // lanes per row: each folds E / LPR values
-  static constexpr int TT = 32 / LPR;       // rows per tile (one tile per consumer warp)
-  static constexpr int CW = MOER_TPR_CW;    // consumer warps
-  static constexpr int STAGES = MOER_TPR_STAGE_KB * 1024 / (TT * E * 4);
-  // Each stage belongs to one consumer warp (STAGES / CW stages per warp), so
-  // a warp always waits on its stages' phases in order and can never pass a
-  // barrier one phase early.
-  static_assert(STAGES % CW == 0, "stages must divide evenly among consumer warps");
-  static constexpr int SPW = STAGES / CW;
-  // Ring stage of the CTA's n-th tile: warp n % CW, that warp's (n / CW)-th use.
-  __device__ static int stage_of(int64_t n) { return (int)(n % CW) + CW * (int)((n / CW) % SPW); }
-  // Phase (use count) of that stage: n / STAGES.
-  static constexpr int CTHREADS = CW * 32;
-  static constexpr int THREADS = CTHREADS + 32;
-  static constexpr size_t STAGE_BYTES = (size_t)TT * E * 4;
+  static constexpr int TT = 32;             // rows per tile: one per lane
+  static constexpr int SW = 32;             // experts per slice: 128-byte slice rows
+  static constexpr int Q = E / SW;          // slices per tile
+  static constexpr int R = MOER_TPR_RING;   // slice buffers per warp
+  static constexpr int CW = MOER_TPR_CW;
+  static constexpr int THREADS = CW * 32;
+  static_assert(E % SW == 0 && Q >= 1, "whole slices per row");
+  static_assert(R >= 2, "a warp needs a second slice buffer to overlap copy and compute");
+  static constexpr uint32_t SLICE_BYTES = (uint32_t)TT * SW * 4;
   static constexpr size_t OFF_ROWS = 0;
-  static constexpr size_t OFF_AFF = OFF_ROWS + STAGES * STAGE_BYTES;
-  // directed pair counts, 16 bits each, two per word (D[a][b] is half (b & 1)
-  // of word (a E + b) / 2); the tile is folded into global memory at least
-  // every FT tiles, so no count passes 65535 (a count grows once per row at most)
-  static constexpr size_t AFF_WORDS = (size_t)E * E / 2;
-  static constexpr int FT = MOER_TPR_FOLD_ROWS / TT;
+  static constexpr size_t OFF_AFF = OFF_ROWS + (size_t)CW * R * SLICE_BYTES;
+  // Directed pair counts D[a][b].  16-bit counts: half (b & 1) of word
+  // a RS + b / 2, folded into global memory at least every FT tiles so that no
+  // count passes 65535 (a count grows once per row at most).  32-bit counts:
+  // word a RS + b, folded at layer changes only.  A tile row has one word of
+  // padding, so the bank of a counter moves with its row as well as its
+  // column (without it the column alone picks the bank).
+  static constexpr bool W32 = MOER_TPR_AFF32 != 0;
+  static constexpr int RS = W32 ? E + 1 : E / 2 + 1;
+  static constexpr size_t AFF_WORDS = (size_t)E * RS;
+  static constexpr int FT = W32 ? (1 << 30) / TT : MOER_TPR_FOLD_ROWS / TT;
   static_assert(MOER_TPR_FOLD_ROWS <= 65535, "16-bit counts: at most 65535 rows between folds");
   static constexpr size_t OFF_RSUM = OFF_AFF + AFF_WORDS * 4;  // E row sums used by the flush
-  static constexpr size_t OFF_BAR = OFF_RSUM + (size_t)E * 4;
-  static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8;
+  static constexpr size_t OFF_BAR = (OFF_RSUM + (size_t)E * 4 + 7) / 8 * 8;
+  static constexpr size_t SMEM = OFF_BAR + (size_t)CW * R * 8;
+  static_assert(SMEM <= 232448, "fits the 227 KB of shared memory a CTA may use");
 };
 
 
@@ -143,51 +145,37 @@ __device__ __forceinline__ void merge8(int (&T)[8], const int (&U)[8], int& L9) 
   for (int i = 0; i < 8; ++i) T[i] = mrg[i];
 }
 
-// Top-8 keys (descending) of this lane's part of a row and, if WANT9, the
-// 9th key.  The part holds NV values starting at expert PART * NV; it is read
-// in 16-byte units whose order is XOR-rotated by (lane & 7).  The value at
-// read position p of part h gets the low key byte 255 - (h * NV + p); its
-// expert id is h * NV + (p ^ (4 * rot)) with rot the reading lane's rotation.
-// The key keeps the float's upper 24 bits: (bits >> 8) * 256 + byte, computed
-// as a multiply-high and a multiply-add by the run-time constants hi_mul =
-// 2^24 and lo_mul = 2^8.
-template <int NV, bool WANT9>
-__device__ __forceinline__ void part_top8(const float* part, int h, int rot, uint32_t hi_mul, uint32_t lo_mul,
-                                          int (&T)[8], int& L9) {
-  const char* base = reinterpret_cast<const char*>(part);
+// Folds one slice of this lane's row (SW values, experts col0 .. col0 + SW - 1)
+// into the running top-8 keys T (descending) and, if WANT9, the 9th key L9.
+// The slice row is read in 16-byte units whose order is XOR-rotated by
+// rot = (lane & 7).  The value at read position p of the row gets the low key
+// byte 255 - p; its expert id is p ^ (4 rot) (the rotation permutes the units
+// of each 128-byte slice row, and col0 is a multiple of 32).  The key keeps
+// the float's upper 24 bits: (bits >> 8) * 256 + byte, computed as a
+// multiply-high and a multiply-add by the run-time constants hi_mul = 2^24
+// and lo_mul = 2^8.  FIRST starts a row: the first chunk becomes T.
+template <int SW, bool WANT9, bool FIRST>
+__device__ __forceinline__ void slice_top8(const float* srow, int rot, int col0, uint32_t hi_mul,
+                                           uint32_t lo_mul, int (&T)[8], int& L9) {
+  const char* base = reinterpret_cast<const char*>(srow);
   const int r16 = rot * 16;
-  const int hb = h * NV;
-  L9 = INT_MIN;
+  if constexpr (FIRST) L9 = INT_MIN;
 #pragma unroll
-  for (int g = 0; g < NV / 8; ++g) {
+  for (int g = 0; g < SW / 8; ++g) {
     const float4 a = *reinterpret_cast<const float4*>(base + (((2 * g) * 16) ^ r16));
     const float4 b = *reinterpret_cast<const float4*>(base + (((2 * g + 1) * 16) ^ r16));
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     int c[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      c[j] = (int)(__umulhi(__float_as_uint(v[j]), hi_mul) * lo_mul + (uint32_t)(255 - hb - (8 * g + j)));
+      c[j] = (int)(__umulhi(__float_as_uint(v[j]), hi_mul) * lo_mul + (uint32_t)(255 - col0 - (8 * g + j)));
     sort8_desc(c);
-    if (g == 0) {
+    if (FIRST && g == 0) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) T[i] = c[i];
     } else {
       merge8<WANT9>(T, c, L9);
     }
-  }
-}
-
-// Merges the sorted top-8 of the lanes that share a row (xor butterfly over
-// LPR lanes); afterwards every lane of the row holds the row's top-8 and 9th.
-template <int LPR, bool WANT9>
-__device__ __forceinline__ void merge_lanes(int (&T)[8], int& L9) {
-#pragma unroll
-  for (int sh = 1; sh < LPR; sh <<= 1) {
-    int P[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) P[i] = __shfl_xor_sync(FULL, T[i], sh);
-    if constexpr (WANT9) L9 = max(L9, __shfl_xor_sync(FULL, L9, sh));
-    merge8<WANT9>(T, P, L9);
   }
 }
 
@@ -230,41 +218,36 @@ __device__ int row_topk_exact(const float* row, int k, int lane) {
   return myidx;
 }
 
-// --------------------------------------------------------------- producer
-template <int E>
-__device__ void tpr_producer(const K1Params& p, char* smem, int64_t i0, int64_t i1) {
-  using G = TprGeo<E>;
-  if ((threadIdx.x & 31) != 0) return;
-  float* rows = reinterpret_cast<float*>(smem + G::OFF_ROWS);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
-  uint64_t* empty = full + G::STAGES;
-  const int64_t N = i1 - i0;
-  // (layer, tile) of the next copy, advanced incrementally (no division per item)
-  int cl = (int)(i0 / p.ntiles), ct = (int)(i0 % p.ntiles);
-  int64_t n = 0;
-  for (; n < N; ++n) {
-    const int s = G::stage_of(n);
-    if (n >= G::STAGES && !mbar_wait(&empty[s], (uint32_t)((n / G::STAGES - 1) & 1), p.status)) break;
-    const int64_t tok0 = (int64_t)ct * G::TT;
-    const uint32_t bytes = (uint32_t)min64(G::TT, p.T - tok0) * E * 4u;
-    mbar_arrive_expect_tx(&full[s], bytes);
-    bulk_g2s(rows + (size_t)s * G::TT * E, p.logits + ((size_t)cl * p.T + tok0) * E, bytes, &full[s]);
-    if (++ct == p.ntiles) {
-      ct = 0;
-      ++cl;
-    }
-  }
-  if (n < N) {
-    // a consumer stopped answering: wait (bounded) for the copies still in
-    // flight into this CTA's shared memory before leaving
-    for (int64_t q = (n > G::STAGES ? n - G::STAGES : 0); q < n; ++q)
-      mbar_wait(&full[G::stage_of(q)], (uint32_t)((q / G::STAGES) & 1), nullptr);
-  }
+// ------------------------------------------------------------- slice copy
+// One tiled TMA copy of the 3-D logits map (x = expert, y = token, z = layer)
+// into shared memory, completing on `bar` as transaction bytes; rows past T
+// are zero-filled and counted.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // -------------------------------------------------------------- consumers
-// Directed pair count D[a][b]: 16-bit half (b & 1) of word (a E + b) / 2.
-__device__ __forceinline__ uint32_t aff_get(const uint32_t* aff, int c) { return (aff[c >> 1] >> ((c & 1) << 4)) & 0xFFFFu; }
+// Directed pair count D[a][b] in the shared tile.
+template <int E>
+__device__ __forceinline__ uint32_t aff_get(const uint32_t* aff, int a, int b) {
+  using G = TprGeo<E>;
+  if constexpr (G::W32) return aff[a * G::RS + b];
+  return (aff[a * G::RS + (b >> 1)] >> ((b & 1) << 4)) & 0xFFFFu;
+}
+
+// Adds one to D[a][b].
+template <int E>
+__device__ __forceinline__ void aff_add(uint32_t* aff, int a, int b) {
+  using G = TprGeo<E>;
+  if constexpr (G::W32)
+    atomicAdd(&aff[a * G::RS + b], 1u);
+  else
+    atomicAdd(&aff[a * G::RS + (b >> 1)], 1u << ((b & 1) << 4));
+}
 
 // The shared tile holds directed pair counts D[a][b] = # rows of this CTA's
 // current layer (since the last fold) in which expert a ranks above expert b.
@@ -278,10 +261,10 @@ __device__ void tpr_flush_aff(const K1Params& p, uint32_t* aff, int* rsum, int l
   using G = TprGeo<E>;
   int32_t* dst = p.affinity + (size_t)layer * E * E;
   if (!skip) {
-    for (int c = threadIdx.x; c < E * E; c += G::CTHREADS) {
+    for (int c = threadIdx.x; c < E * E; c += G::THREADS) {
       const int a = c / E, b = c % E;
       if (a < b) {
-        const int v = (int)(aff_get(aff, a * E + b) + aff_get(aff, b * E + a));
+        const int v = (int)(aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a));
         if (v != 0) {
           atomicAdd(&dst[a * E + b], v);
           atomicAdd(&dst[b * E + a], v);
@@ -291,32 +274,30 @@ __device__ void tpr_flush_aff(const K1Params& p, uint32_t* aff, int* rsum, int l
       }
     }
   }
-  named_bar(1, G::CTHREADS);
+  named_bar(1, G::THREADS);
   if (!skip) {
-    for (int a = threadIdx.x; a < E; a += G::CTHREADS) {
+    for (int a = threadIdx.x; a < E; a += G::THREADS) {
       const int v = rsum[a];
       if (v != 0) {
         atomicAdd(&dst[a * E + a], v / (K - 1));
         rsum[a] = 0;
       }
     }
-    for (int c = threadIdx.x; c < (int)G::AFF_WORDS; c += G::CTHREADS) aff[c] = 0u;
+    for (int c = threadIdx.x; c < (int)G::AFF_WORDS; c += G::THREADS) aff[c] = 0u;
   }
 }
 
 template <int E, int K>
 __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t i1) {
   using G = TprGeo<E>;
-  constexpr int LPR = G::LPR;
-  constexpr int NV = E / LPR;              // values folded by one lane
-  static_assert(LPR == 1 || LPR == 2, "rank split assumes one or two lanes per row");
+  constexpr int Q = G::Q, R = G::R, SW = G::SW;
+  constexpr int SLICE_FLOATS = G::TT * SW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rrow = lane / LPR, h = lane % LPR, rot = lane & 7;
-  const float* rows = reinterpret_cast<const float*>(smem + G::OFF_ROWS);
+  const int rot = lane & 7;
+  float* ring = reinterpret_cast<float*>(smem + G::OFF_ROWS) + (size_t)warp * R * SLICE_FLOATS;
   uint32_t* aff = reinterpret_cast<uint32_t*>(smem + G::OFF_AFF);
   int* rsum = reinterpret_cast<int*>(smem + G::OFF_RSUM);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
-  uint64_t* empty = full + G::STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR) + warp * R;
   const bool aff_on = p.affinity != nullptr;
   const int64_t N = i1 - i0;
   // fold epochs: (layer, tile / FT), numbered l * epl + tile / FT, monotone in the item
@@ -327,9 +308,34 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   };
   const int64_t ep_last = epoch_of(i1 - 1);
   int64_t cur = epoch_of(i0);
+  const int l0 = (int)((i0 + warp) / p.ntiles);
+  const int t0 = (int)((i0 + warp) - (int64_t)l0 * p.ntiles);
+  // Copy side (lane 0): the warp's slices in order, slice j = (its tile j / Q,
+  // experts SW (j % Q) ...), slice j into buffer j % R.
+  const int64_t nsl = (N > warp ? (N - warp + G::CW - 1) / G::CW : 0) * Q;
+  int64_t js = 0;  // next slice to copy
+  int cq = 0, cl = l0, ct = t0;
+  auto fetch = [&](int buf) {
+    mbar_arrive_expect_tx(&full[buf], G::SLICE_BYTES);
+    tma_load_3d(ring + (size_t)buf * SLICE_FLOATS, &p.tm_logits, cq * SW, ct * G::TT, cl, &full[buf]);
+    ++js;
+    if (++cq == Q) {
+      cq = 0;
+      ct += G::CW;
+      while (ct >= p.ntiles) {
+        ct -= p.ntiles;
+        ++cl;
+      }
+    }
+  };
+  if (lane == 0)
+    for (int r = 0; r < R && js < nsl; ++r) fetch(r);
+  // Fold side: slice jw is in buffer wb, phase parity wpar.
+  int64_t jw = 0;
+  int wb = 0;
+  uint32_t wpar = 0;
   bool dead = false;
-  int l = (int)((i0 + warp) / p.ntiles);
-  int tile = (int)((i0 + warp) - (int64_t)l * p.ntiles);
+  int l = l0, tile = t0;
   for (int64_t n = warp; n < N; n += G::CW) {
     if (n > warp) {
       tile += G::CW;
@@ -340,28 +346,41 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     }
     const int64_t ep = (int64_t)l * epl + tile / G::FT;
     while (aff_on && cur < ep) {
-      named_bar(1, G::CTHREADS);
+      named_bar(1, G::THREADS);
       tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
-      named_bar(1, G::CTHREADS);
+      named_bar(1, G::THREADS);
       ++cur;
     }
     cur = ep;
     if (dead) continue;
-    const int s = G::stage_of(n);
-    if (!mbar_wait(&full[s], (uint32_t)((n / G::STAGES) & 1), p.status)) {
-      dead = true;
-      continue;
-    }
     const int64_t tok0 = (int64_t)tile * G::TT;
     const int ntok = (int)min64(G::TT, p.T - tok0);
     const int slot = p.slot_of_layer[l];
     uint8_t* out = nullptr;
     if (p.ids != nullptr && (!p.ids_mask_only || slot >= 0))
       out = p.ids + ((size_t)(p.ids_mask_only ? slot : l) * p.T + tok0) * K;
-    const float* stage = rows + (size_t)s * G::TT * E;
     int Tk[8], L9;
-    part_top8<NV, (K == 8)>(stage + (size_t)rrow * E + h * NV, h, rot, p.key_hi_mul, p.key_lo_mul, Tk, L9);
-    merge_lanes<LPR, (K == 8)>(Tk, L9);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      if (!__all_sync(FULL, mbar_wait(&full[wb], wpar, p.status))) {
+        dead = true;
+        break;
+      }
+      const float* srow = ring + (size_t)wb * SLICE_FLOATS + lane * SW;
+      if (q == 0)
+        slice_top8<SW, (K == 8), true>(srow, rot, 0, p.key_hi_mul, p.key_lo_mul, Tk, L9);
+      else
+        slice_top8<SW, (K == 8), false>(srow, rot, q * SW, p.key_hi_mul, p.key_lo_mul, Tk, L9);
+      // every lane has read the buffer: refill it with the slice R ahead
+      __syncwarp();
+      if (lane == 0 && js < nsl) fetch(wb);
+      ++jw;
+      if (++wb == R) {
+        wb = 0;
+        wpar ^= 1u;
+      }
+    }
+    if (dead) continue;
     // certification of the truncated-key result
     const int nxt = (K == 8) ? L9 : Tk[K < 8 ? K : 7];
     bool bad = (Tk[K - 1] < 256) || (Tk[0] >= 0x7F800000);
@@ -371,64 +390,61 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
       const int b = (i + 1 < K) ? Tk[i + 1] : nxt;
       bad = bad || (b >= (a & (int)0xFFFFFF00));
     }
-    const bool live = rrow < ntok;
-    const unsigned redo = __ballot_sync(FULL, bad && live && h == 0);
-    // expert ids: position pos = 255 - low byte lies in part hp = pos / NV,
-    // read by lane (row lanes) | hp with rotation orot = that lane's & 7, so
-    // id = hp * NV + ((pos % NV) ^ 4 orot).  4 orot < NV leaves bit log2(NV)
-    // alone, hence id = pos ^ 4 orot = pos ^ xrow ^ 4 hp with the row's
-    // constant xrow = 4 ((lane & ~(LPR-1)) & 7) and 4 hp = (pos >> (log2(NV) - 2)) & 4.
-    static_assert(4 * 7 < NV && (NV & (NV - 1)) == 0, "id recovery assumes NV a power of two >= 32");
-    constexpr int HSH = (NV == 64) ? 4 : 3;
-    const int xrow = 4 * ((lane & ~(LPR - 1)) & 7);
+    const bool live = lane < ntok;
+    const unsigned redo = __ballot_sync(FULL, bad && live);
+    // expert ids: read position pos = 255 - low byte, id = pos ^ 4 (lane & 7)
+    const int xrow = 4 * rot;
     int idx[K];
 #pragma unroll
-    for (int i = 0; i < K; ++i) {
-      const int pos = (~Tk[i]) & 0xFF;
-      idx[i] = (LPR == 2) ? (pos ^ xrow ^ ((pos >> HSH) & 4)) : (pos ^ xrow);
-    }
+    for (int i = 0; i < K; ++i) idx[i] = ((~Tk[i]) & 0xFF) ^ xrow;
     if (live && !bad) {
-      if (out != nullptr && h == 0) {
+      if (out != nullptr) {
         if constexpr (K == 8) {
           const uint32_t lo = (uint32_t)idx[0] | ((uint32_t)idx[1] << 8) | ((uint32_t)idx[2] << 16) |
                               ((uint32_t)idx[3] << 24);
           const uint32_t hi = (uint32_t)idx[4] | ((uint32_t)idx[5] << 8) | ((uint32_t)idx[6] << 16) |
                               ((uint32_t)idx[7] << 24);
-          *reinterpret_cast<uint2*>(out + (size_t)rrow * 8) = make_uint2(lo, hi);
+          *reinterpret_cast<uint2*>(out + (size_t)lane * 8) = make_uint2(lo, hi);
         } else {
-          uint8_t* o = out + (size_t)rrow * K;
+          uint8_t* o = out + (size_t)lane * K;
 #pragma unroll
           for (int i = 0; i < K; i += 2)
             *reinterpret_cast<uint16_t*>(o + i) = (uint16_t)(idx[i] | (idx[i + 1] << 8));
         }
       }
       if (aff_on) {
-        // directed pairs (rank i above rank j): k(k-1)/2 adds per row into the
-        // packed 16-bit counts; with two lanes per row, lane h takes the ranks
-        // i with i % 2 == h
-        int wj[K];
-        uint32_t sj[K];
+        // directed pairs (rank i above rank j): k(k-1)/2 adds per row
+        if constexpr (G::W32) {
 #pragma unroll
-        for (int j = 1; j < K; ++j) {
-          wj[j] = idx[j] >> 1;
-          sj[j] = 1u << ((idx[j] & 1) << 4);
-        }
+          for (int i = 0; i < K - 1; ++i) {
+            uint32_t* ra = aff + idx[i] * G::RS;
 #pragma unroll
-        for (int i = 0; i < K - 1; ++i) {
-          if (i % LPR == h) {
-            uint32_t* ra = aff + idx[i] * (E / 2);
+            for (int j = i + 1; j < K; ++j) atomicAdd(ra + idx[j], 1u);
+          }
+        } else {
+          int wj[K];
+          uint32_t sj[K];
+#pragma unroll
+          for (int j = 1; j < K; ++j) {
+            wj[j] = idx[j] >> 1;
+            sj[j] = 1u << ((idx[j] & 1) << 4);
+          }
+#pragma unroll
+          for (int i = 0; i < K - 1; ++i) {
+            uint32_t* ra = aff + idx[i] * G::RS;
 #pragma unroll
             for (int j = i + 1; j < K; ++j) atomicAdd(ra + wj[j], sj[j]);
           }
         }
       }
     }
-    // rows the fast path could not certify: the whole warp redoes each exactly
+    // rows the fast path could not certify: the whole warp redoes each exactly,
+    // reading the row again from global memory (its slices are being refilled)
     unsigned todo = redo;
     while (todo) {
-      const int f = (__ffs(todo) - 1) / LPR;
+      const int f = __ffs(todo) - 1;
       todo &= todo - 1;
-      const int e = row_topk_exact<E>(stage + (size_t)f * E, K, lane);
+      const int e = row_topk_exact<E>(p.logits + ((size_t)l * p.T + tok0 + f) * E, K, lane);
       if (out != nullptr && lane < K) out[(size_t)f * K + lane] = (uint8_t)e;
       if (aff_on) {
 #pragma unroll
@@ -436,24 +452,24 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
           const int q = base + lane;
           const int ia = __shfl_sync(FULL, e, q < K * K ? q / K : 0);
           const int ib = __shfl_sync(FULL, e, q < K * K ? q % K : 0);
-          if (q < K * K && q / K < q % K) {
-            const int c = ia * E + ib;
-            atomicAdd(&aff[c >> 1], 1u << ((c & 1) << 4));
-          }
+          if (q < K * K && q / K < q % K) aff_add<E>(aff, ia, ib);
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (dead && lane == 0) {
+    // a copy stopped answering: wait (bounded) for this warp's copies still in
+    // flight into shared memory before leaving
+    for (int64_t j = jw; j < js; ++j) mbar_wait(&full[j % R], (uint32_t)((j / R) & 1), nullptr);
   }
   if (aff_on) {
     while (cur < ep_last) {
-      named_bar(1, G::CTHREADS);
+      named_bar(1, G::THREADS);
       tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
-      named_bar(1, G::CTHREADS);
+      named_bar(1, G::THREADS);
       ++cur;
     }
-    named_bar(1, G::CTHREADS);
+    named_bar(1, G::THREADS);
     tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
   }
 }
@@ -471,17 +487,11 @@ __global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __g
   }
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < G::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&full[G::STAGES + s], 1);
-    }
+    for (int s = 0; s < G::CW * G::R; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x >= G::CTHREADS)
-    tpr_producer<E>(p, smem, i0, i1);
-  else
-    tpr_consumer<E, K>(p, smem, i0, i1);
+  tpr_consumer<E, K>(p, smem, i0, i1);
 }
 
 template <int E, int K>
@@ -502,11 +512,53 @@ bool tpr_supported(int E, int k) { return (E == 128 || E == 64) && (k == 8 || k 
 
 int tpr_tile_tokens(int E) { return E == 128 ? TprGeo<128>::TT : TprGeo<64>::TT; }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tiled_encoder() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The logits [L][T][E] fp32 as a 3-D tensor map (x = expert, y = token,
+// z = layer) with boxes of one slice: SW experts x TT tokens x 1 layer.
+template <int E>
+bool logits_map(CUtensorMap* m, const float* logits, int64_t T, int L) {
+  using G = TprGeo<E>;
+  EncodeTiledFn enc = tiled_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)E, (cuuint64_t)T, (cuuint64_t)L};
+  const cuuint64_t strides[2] = {(cuuint64_t)E * 4, (cuuint64_t)T * E * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)G::SW, (cuuint32_t)G::TT, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(logits), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int E, int K>
+cudaError_t tpr_launch_mapped(const K1Params& p0, int grid, cudaStream_t st) {
+  K1Params p = p0;
+  if (!logits_map<E>(&p.tm_logits, p.logits, p.T, p.L)) return cudaErrorInvalidValue;
+  return tpr_launch<E, K>(p, grid, st);
+}
+}  // namespace
+
 cudaError_t tpr_run(int E, int k, const K1Params& p, int grid, cudaStream_t st) {
-  if (E == 128 && k == 8) return tpr_launch<128, 8>(p, grid, st);
-  if (E == 128 && k == 6) return tpr_launch<128, 6>(p, grid, st);
-  if (E == 64 && k == 8) return tpr_launch<64, 8>(p, grid, st);
-  return tpr_launch<64, 6>(p, grid, st);
+  if (E == 128 && k == 8) return tpr_launch_mapped<128, 8>(p, grid, st);
+  if (E == 128 && k == 6) return tpr_launch_mapped<128, 6>(p, grid, st);
+  if (E == 64 && k == 8) return tpr_launch_mapped<64, 8>(p, grid, st);
+  return tpr_launch_mapped<64, 6>(p, grid, st);
 }
 
 }  // namespace moer
