@@ -16,7 +16,8 @@
 // three sums s11 = sum_e w1^2, s22 = sum_e w2^2, s12 = sum_e w1 w2 (w = count *
 // idf): quality(M) = mean_r S12 / sqrt(S11 S22) with S = sum over l in M.
 //   * mask_stats_kernel: one CTA per (request, layer); the two halves' ids go
-//     into shared-memory histograms, then the three sums in fp64.
+//     into shared-memory histograms (at k = 8 one 8-byte load per token, four
+//     in flight per thread), then the three sums in fp64.
 //   * per greedy step, mask_eval_kernel (one CTA per candidate layer, threads
 //     over the requests: running sums of the chosen layers + the candidate's,
 //     fp64 cosines, a block reduction) and mask_pick_kernel (the argmax, then
@@ -27,6 +28,7 @@
 namespace moer {
 
 constexpr int MS_STATS_THREADS = 128;
+constexpr int MS_UNROLL = 4;  // token loads in flight per thread
 constexpr int MS_EVAL_THREADS = 256;
 
 __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint8_t* __restrict__ topk, int64_t T,
@@ -51,11 +53,49 @@ __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint
   __syncthreads();
   const int64_t mid = t0 + (t1 - t0) / 2;
   const uint8_t* row = topk + (size_t)l * T * k;
-  for (int64_t q = t0 * k + tid; q < t1 * k; q += MS_STATS_THREADS) {
-    const int e = row[q];
-    if (e < E) atomicAdd(q < mid * k ? &c1[e] : &c2[e], 1);
-    else atomicOr(status, WS_BIT_EDATA);  // an id outside [0, E) is skipped and reported
+  bool bad_id = false;
+  if (k == 8 && (reinterpret_cast<uintptr_t>(row) & 7u) == 0) {
+    // whole tokens: one 8-byte word of ids each, MS_UNROLL loads in flight per
+    // thread; a lane starts its token's ranks at (lane & 7), so the lanes of
+    // one add mostly hit different experts (ranks, not tokens, correlate)
+    const uint2* tok_ids = reinterpret_cast<const uint2*>(row);
+    const int rot = 8 * (lane & 3);
+    const bool swap = (lane & 4) != 0;
+    for (int64_t t = t0 + tid; t < t1; t += MS_STATS_THREADS * MS_UNROLL) {
+      uint2 v[MS_UNROLL];
+#pragma unroll
+      for (int u = 0; u < MS_UNROLL; ++u) {
+        const int64_t tu = t + (int64_t)u * MS_STATS_THREADS;
+        v[u] = tu < t1 ? tok_ids[tu] : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < MS_UNROLL; ++u) {
+        const int64_t tu = t + (int64_t)u * MS_STATS_THREADS;
+        if (tu < t1) {
+          int* c = tu < mid ? c1 : c2;
+          const uint32_t a = swap ? v[u].y : v[u].x, b = swap ? v[u].x : v[u].y;
+          const uint32_t lo = __funnelshift_r(a, b, rot), hi = __funnelshift_r(b, a, rot);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int e = (int)(((j < 4 ? lo : hi) >> (8 * (j & 3))) & 0xFFu);
+            if (e < E)
+              atomicAdd(&c[e], 1);
+            else
+              bad_id = true;
+          }
+        }
+      }
+    }
+  } else {
+    for (int64_t q = t0 * k + tid; q < t1 * k; q += MS_STATS_THREADS) {
+      const int e = row[q];
+      if (e < E)
+        atomicAdd(q < mid * k ? &c1[e] : &c2[e], 1);
+      else
+        bad_id = true;
+    }
   }
+  if (bad_id) atomicOr(status, WS_BIT_EDATA);  // an id outside [0, E) is skipped and reported
   __syncthreads();
   double a = 0.0, b = 0.0, c = 0.0;
   for (int e = tid; e < E; e += MS_STATS_THREADS) {

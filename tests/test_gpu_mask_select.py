@@ -118,3 +118,36 @@ def test_malformed_offsets_are_reported(env):
     nat.moer_mask_select(dims, torch.from_numpy(topk).cuda(), topk.shape[1], torch.from_numpy(bad).cuda(),
                          10, None, 2, mask, None, ws, wsb)
     assert nat.moer_ws_status(ws) == 6
+
+
+def test_k8_misaligned_view_and_bad_id(env):
+    torch, nat = env
+    topk, off = _synthetic(5, 6, 64, 8, 40)
+    L, T, k = topk.shape
+    R = len(off) - 1
+    dims = nat.make_dims(64, k, L, [], 16)
+    do = torch.from_numpy(off).cuda()
+
+    def run(dt):
+        mask = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+        qual = torch.zeros(4, dtype=torch.float64, device="cuda")
+        wsb = nat.moer_mask_select_workspace_bytes(dims, R)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        nat.moer_mask_select(dims, dt, T, do, R, None, 4, mask, qual, ws, wsb)
+        return mask.cpu().numpy(), qual.cpu().numpy(), nat.moer_ws_status(ws)
+
+    aligned_m, aligned_q, st = run(torch.from_numpy(topk).cuda())
+    assert st == 0
+    _compare(topk, off, 64, 4, None, aligned_m, aligned_q)
+    # the same ids one byte into a buffer: the 8-byte loads are not allowed there
+    buf = torch.zeros(topk.size + 8, dtype=torch.uint8, device="cuda")
+    buf[1:1 + topk.size] = torch.from_numpy(topk.reshape(-1)).cuda()
+    view = buf[1:1 + topk.size]
+    assert view.data_ptr() % 8 == 1
+    m2, q2, st2 = run(view)
+    assert st2 == 0 and np.array_equal(m2, aligned_m) and np.array_equal(q2, aligned_q)
+    # an id outside [0, E) is skipped and reported
+    bad = topk.copy()
+    bad[2, 5, 3] = 64
+    _, _, st3 = run(torch.from_numpy(bad).cuda())
+    assert st3 == 6
