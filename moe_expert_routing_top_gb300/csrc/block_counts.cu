@@ -144,22 +144,26 @@ namespace moer {
 // section 3 and section 4 / Figure 2(a): A_l[a][b] += #tokens whose top-k
 // at layer l holds both a and b.
 //
-// Persistent grid over (layer, 512-token chunk) items in layer-major order,
-// one thread per token row.  A row's k distinct ids, in rank order, add its
-// k(k-1)/2 rank-ordered pairs to a shared tile of directed counts
-// D[a][b] (= # rows where a ranks above b).  When the CTA's layer changes
+// Persistent grid over (layer, 2048-token chunk) items in layer-major order,
+// four token rows per thread with their id loads issued together.  A row's k
+// distinct ids, in rank order, add its k(k-1)/2 rank-ordered pairs to a
+// shared tile of directed counts D[a][b] (= # rows where a ranks above b).  When the CTA's layer changes
 // the tile is folded into the symmetric co-activation -- A[a][b] = D[a][b] +
 // D[b][a] off the diagonal, and A[a][a] = (sum over b != a of A[a][b]) /
 // (k - 1), since each row holding a holds k - 1 other experts -- and added to
 // global memory.  Needs k >= 2.
-constexpr int AI_CHUNK = 512;
 constexpr int AI_THREADS = 512;
+constexpr int AI_U = 4;                      // tokens per thread per item, loads in flight together
+constexpr int AI_CHUNK = AI_THREADS * AI_U;  // tokens per work item
 
+// The tile's rows are E + 1 words apart, so the bank of D[a][b] depends on a
+// as well as b.
 __device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* dst) {
+  const int rs = E + 1;
   for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
     const int a = c / E, b = c - a * E;
     if (a < b) {
-      const int v = tile[a * E + b] + tile[b * E + a];
+      const int v = tile[a * rs + b] + tile[b * rs + a];
       if (v != 0) {
         atomicAdd(&dst[a * E + b], v);
         atomicAdd(&dst[b * E + a], v);
@@ -176,7 +180,7 @@ __device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* 
       rsum[a] = 0;
     }
   }
-  for (int c = threadIdx.x; c < E * E; c += AI_THREADS) tile[c] = 0;
+  for (int c = threadIdx.x; c < E * rs; c += AI_THREADS) tile[c] = 0;
   __syncthreads();
 }
 
@@ -184,12 +188,13 @@ template <int K>
 __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t* __restrict__ ids, int64_t T,
                                                                   int E, int L, int nchunks,
                                                                   int32_t* __restrict__ affinity) {
-  extern __shared__ int ai_tile[];  // [E][E] directed counts, then [E] row sums
-  int* rsum = ai_tile + E * E;
+  extern __shared__ int ai_tile[];  // [E][E + 1] directed counts, then [E] row sums
+  const int rs = E + 1;
+  int* rsum = ai_tile + E * rs;
   const int64_t nitems = (int64_t)L * nchunks;
   const int64_t i0 = (int64_t)blockIdx.x * nitems / gridDim.x;
   const int64_t i1 = ((int64_t)blockIdx.x + 1) * nitems / gridDim.x;
-  for (int c = threadIdx.x; c < E * E + E; c += AI_THREADS) ai_tile[c] = 0;
+  for (int c = threadIdx.x; c < E * rs + E; c += AI_THREADS) ai_tile[c] = 0;
   __syncthreads();
   int cur = (int)(i0 / nchunks);
   for (int64_t it = i0; it < i1; ++it) {
@@ -199,30 +204,42 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
       affinity_ids_flush(ai_tile, rsum, E, K, affinity + (size_t)cur * E * E);
       cur = l;
     }
-    const int64_t t = (it - (int64_t)l * nchunks) * AI_CHUNK + threadIdx.x;
-    if (threadIdx.x < AI_CHUNK && t < T) {
-      const uint8_t* src = ids + ((size_t)l * T + t) * K;
-      int e[K];
-      if constexpr (K == 8) {
-        const uint2 w = *reinterpret_cast<const uint2*>(src);
+    const int64_t tb = (it - (int64_t)l * nchunks) * AI_CHUNK + threadIdx.x;
+    const uint8_t* lay = ids + (size_t)l * T * K;
+    uint32_t w[AI_U][(K + 3) / 4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          e[j] = (w.x >> (8 * j)) & 0xFF;
-          e[4 + j] = (w.y >> (8 * j)) & 0xFF;
-        }
-      } else {
+    for (int u = 0; u < AI_U; ++u) {
+      const int64_t t = tb + (int64_t)u * AI_THREADS;
+      if (t < T) {
+        if constexpr (K == 8) {
+          const uint2 v = *reinterpret_cast<const uint2*>(lay + (size_t)t * 8);
+          w[u][0] = v.x;
+          w[u][1] = v.y;
+        } else {
+          const uint8_t* src = lay + (size_t)t * K;
 #pragma unroll
-        for (int j = 0; j < K; j += 2) {
-          const uint32_t h = *reinterpret_cast<const uint16_t*>(src + j);
-          e[j] = h & 0xFF;
-          e[j + 1] = h >> 8;
+          for (int j = 0; j < K; j += 2) {
+            const uint32_t h = *reinterpret_cast<const uint16_t*>(src + j);
+            if (j % 4 == 0)
+              w[u][j / 4] = h;
+            else
+              w[u][j / 4] |= h << 16;
+          }
         }
       }
+    }
 #pragma unroll
-      for (int i = 0; i < K - 1; ++i) {
-        int* ra = ai_tile + e[i] * E;
+    for (int u = 0; u < AI_U; ++u) {
+      if (tb + (int64_t)u * AI_THREADS < T) {
+        int e[K];
 #pragma unroll
-        for (int j = i + 1; j < K; ++j) atomicAdd(ra + e[j], 1);
+        for (int j = 0; j < K; ++j) e[j] = (w[u][j / 4] >> (8 * (j % 4))) & 0xFF;
+#pragma unroll
+        for (int i = 0; i < K - 1; ++i) {
+          int* ra = ai_tile + e[i] * rs;
+#pragma unroll
+          for (int j = i + 1; j < K; ++j) atomicAdd(ra + e[j], 1);
+        }
       }
     }
   }
@@ -240,10 +257,10 @@ moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t 
   const int64_t nitems = (int64_t)d->L * nchunks;
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
-  const size_t smem = ((size_t)d->E * d->E + d->E) * sizeof(int);
+  const size_t smem = ((size_t)d->E * (d->E + 1) + d->E) * sizeof(int);
   static bool configured = false;
   if (!configured) {
-    const int most = (int)((128 * 128 + 128) * sizeof(int));
+    const int most = (int)((128 * 129 + 128) * sizeof(int));
     if (cudaFuncSetAttribute(affinity_ids_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
             cudaSuccess ||
         cudaFuncSetAttribute(affinity_ids_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
