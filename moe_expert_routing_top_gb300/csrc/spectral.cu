@@ -22,18 +22,16 @@
 //
 // Design (GB300):
 //   * spec_embed_kernel, one CTA per layer: M lives in shared memory (fp64,
-//     128 KB at E = 128); parallel cyclic Jacobi with the round-robin pairing,
-//     E/2 disjoint rotations per round (rows, then columns with the pairs
-//     fastest so a warp touches 32 different columns, and the eigenvector
-//     matrix, kept transposed in global memory so its update is coalesced),
-//     until a sweep finds every off-diagonal entry negligible against its
-//     diagonal pair (|a_pq| <= 1e-15 sqrt|a_pp a_qq|: threshold Jacobi, which
-//     stops at the rounding floor instead of chasing it); the G largest
-//     diagonal entries pick the columns.  A full solve rather than an
-//     iteration on the top-G subspace: the co-activation spectra of real
-//     layers are nearly degenerate just below the leading eigenvalues, where
-//     subspace iteration needs 10^4 - 10^5 steps, while Jacobi's accuracy
-//     (backward stable) only needs the gap at the G-th eigenvalue.
+//     128 KB at E = 128).  Householder reduction to tridiagonal form (the
+//     matrix-vector product eight threads per row, the rank-2 update over the
+//     whole trailing block), the G largest eigenvalues by Sturm-count
+//     multisection (a warp per eigenvalue, a lane per trial point), their
+//     eigenvectors by inverse iteration on the tridiagonal form, taken back
+//     through the reflections.  A full solve of the spectrum is not needed:
+//     only G eigenpairs are formed.  Subspace iteration on the top-G space is
+//     not an option either: the co-activation spectra of real layers are
+//     nearly degenerate just below the leading eigenvalues, where it needs
+//     10^4 - 10^5 steps.
 //   * spec_group_kernel, one CTA per (grid point, layer): the size-bounded
 //     assignment is a transportation problem with lower and upper bounds; one
 //     warp keeps a feasible assignment and cancels negative cycles of the
@@ -52,26 +50,70 @@ constexpr int SP_MAXG = 31;
 constexpr int SP_NGRID = 17;
 constexpr int SP_EMBED_THREADS = 1024;
 constexpr int SP_GROUP_THREADS = 256;
-constexpr int SP_MAX_SWEEPS = 40;
 constexpr int SP_MAX_STEPS = 100;
 
-__device__ __forceinline__ int sp_seq(int j, int r, int E) { return j == 0 ? 0 : ((j - 1 + r) % (E - 1)) + 1; }
 
+__device__ __forceinline__ double sp_warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int sp_sturm(const double* dg, const double* e2, int n, double x, double pivmin) {
+  // number of eigenvalues of the tridiagonal form below x (signs of the pivots
+  // of T - x I = L D L^T)
+  double q = dg[0] - x;
+  if (fabs(q) < pivmin) q = -pivmin;
+  int c = q < 0.0 ? 1 : 0;
+  for (int i = 1; i < n; ++i) {
+    q = (dg[i] - x) - e2[i] / q;
+    if (fabs(q) < pivmin) q = -pivmin;
+    c += q < 0.0 ? 1 : 0;
+  }
+  return c;
+}
+
+// Spectral embedding of one layer (CTA l), all in fp64:
+//   * M = D^-1/2 A D^-1/2 (A the co-activation without its diagonal, D its
+//     row sums) in shared memory, reduced to tridiagonal form T by E - 2
+//     Householder reflections H_k (x = column k below the diagonal,
+//     v = x - alpha e_1 with alpha = -sign(x_0) |x|, beta = 2 / v.v; the
+//     trailing block becomes A - v w^T - w v^T with p = beta A v,
+//     w = p - (beta v.p / 2) v).  v is kept in row k right of the diagonal.
+//   * The G largest eigenvalues of T by multisection: warp j brackets the
+//     (j+1)-th largest between Gershgorin bounds and narrows the bracket 33-fold
+//     per step with a Sturm count at 32 points (one per lane).
+//   * Their eigenvectors by inverse iteration on T (LU with partial pivoting,
+//     three solves from a fixed start vector, each re-orthogonalised against
+//     the vectors found before it whose eigenvalues lie within 1e-3 |T|),
+//     then taken back through the reflections: x = H_0 ... H_{E-3} y.
+//   Rows of the embedding are the G eigenvectors' components, scaled to unit
+//   length.  Only the G vectors are formed: fp64 divisions and square roots
+//   are slow on this part, and a full QL solve spent ~37 M clock cycles per
+//   layer in its sequential recurrence.
 __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
-    spec_embed_kernel(const int32_t* __restrict__ affinity, int E, int G, double* __restrict__ V,
-                      double* __restrict__ Uo, double* __restrict__ deg_out) {
+    spec_embed_kernel(const int32_t* __restrict__ affinity, int E, int G, double* __restrict__ Uo,
+                      double* __restrict__ deg_out) {
   extern __shared__ double sp_sm[];
-  double* M = sp_sm;                 // [E][E]
-  double* inv = M + E * E;           // [E]
-  double* cs = inv + E;              // [E/2]
-  double* sn = cs + E / 2;           // [E/2]
-  double* red = sn + E / 2;          // [32]
-  int* pp = reinterpret_cast<int*>(red + 32);
-  int* qq = pp + E / 2;
-  __shared__ int s_done;
+  const int n = E;
+  double* M = sp_sm;         // [E][E]
+  double* inv = M + E * E;   // [E] D^-1/2
+  double* vv = inv + E;      // [E] Householder vector
+  double* pw = vv + E;       // [E] p, then w; later e2[i] = sd[i-1]^2
+  double* dg = pw + E;       // [E] diagonal of T
+  double* sd = dg + E;       // [E] subdiagonal: sd[i] couples i and i + 1
+  double* bet = sd + E;      // [E] beta of reflection k (0: none needed)
+  double* lu0 = bet + E;     // [E] LU of T - lambda I: reciprocal pivots,
+  double* lu1 = lu0 + E;     // [E]   first and
+  double* lu2 = lu1 + E;     // [E]   second superdiagonal,
+  double* lmul = lu2 + E;    // [E]   multipliers
+  double* lam = lmul + E;    // [32] eigenvalues, largest first
+  double* red = lam + 32;    // [32]
+  double* Y = red + 32;      // [G][E] eigenvectors
+  int* lsw = reinterpret_cast<int*>(Y + (size_t)G * E);  // [E] row swaps of the LU
   const int l = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int32_t* A = affinity + (size_t)l * E * E;
-  double* Vl = V + (size_t)l * E * E;
   for (int a = tid; a < E; a += nt) {
     long long d = 0;
     for (int b = 0; b < E; ++b)
@@ -84,88 +126,198 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     const int a = q / E, b = q - a * E;
     const int32_t x = A[q] > 0 ? A[q] : 0;
     M[q] = (a == b) ? 0.0 : inv[a] * (double)x * inv[b];
-    Vl[q] = (a == b) ? 1.0 : 0.0;
   }
   __syncthreads();
-  // threshold Jacobi: a rotation is skipped when |a_pq| <= 1e-15 sqrt(|a_pp a_qq|)
-  // (negligible against the diagonal); the solve ends after a sweep that rotates nothing
-  for (int sweep = 0; sweep < SP_MAX_SWEEPS; ++sweep) {
-    if (tid == 0) s_done = 1;
-    __syncthreads();
-    for (int r = 0; r < E - 1; ++r) {
-      if (tid < E / 2) {
-        const int p = sp_seq(tid, r, E), q = sp_seq(E - 1 - tid, r, E);
-        const double apq = M[p * E + q], app = M[p * E + p], aqq = M[q * E + q];
-        double c = 1.0, s = 0.0;
-        if (fabs(apq) > 1e-15 * sqrt(fabs(app * aqq)) && fabs(apq) > 1e-300) {
-          const double th = (aqq - app) / (2.0 * apq);
-          double t;
-          if (fabs(th) > 1e150) t = 1.0 / (2.0 * th);
-          else if (th == 0.0) t = 1.0;
-          else t = (th > 0.0 ? 1.0 : -1.0) / (fabs(th) + sqrt(th * th + 1.0));
-          c = 1.0 / sqrt(1.0 + t * t);
-          s = t * c;
-          s_done = 0;
+  // ---- Householder reduction to tridiagonal form
+  for (int k = 0; k + 2 < n; ++k) {
+    const int m = n - k - 1;  // length of x = M[k+1 ..][k]
+    if (warp == 0) {
+      double s2 = 0.0;
+      for (int j = 1 + lane; j < m; j += 32) {
+        const double x = M[(k + 1 + j) * n + k];
+        s2 = fma(x, x, s2);
+      }
+      s2 = sp_warp_sum(s2);
+      if (lane == 0) {
+        const double x0 = M[(k + 1) * n + k];
+        if (s2 == 0.0) {  // already reduced
+          sd[k] = x0;
+          bet[k] = 0.0;
+        } else {
+          const double sig = fma(x0, x0, s2);
+          const double alpha = x0 > 0.0 ? -sqrt(sig) : sqrt(sig);
+          sd[k] = alpha;
+          bet[k] = 1.0 / (sig - alpha * x0);
+          red[0] = x0 - alpha;
         }
-        pp[tid] = p;
-        qq[tid] = q;
-        cs[tid] = c;
-        sn[tid] = s;
+        dg[k] = M[k * n + k];
       }
-      __syncthreads();
-      for (int w = tid; w < (E / 2) * E; w += nt) {  // rows p, q of every pair
-        const int i = w / E, j = w - i * E;
-        const int p = pp[i], q = qq[i];
-        const double c = cs[i], s = sn[i];
-        const double mp = M[p * E + j], mq = M[q * E + j];
-        M[p * E + j] = c * mp - s * mq;
-        M[q * E + j] = s * mp + c * mq;
-      }
-      __syncthreads();
-      for (int w = tid; w < (E / 2) * E; w += nt) {  // columns p, q: pairs fastest (distinct banks)
-        const int i = w % (E / 2), j = w / (E / 2);
-        const int p = pp[i], q = qq[i];
-        const double c = cs[i], s = sn[i];
-        const double mp = M[j * E + p], mq = M[j * E + q];
-        M[j * E + p] = c * mp - s * mq;
-        M[j * E + q] = s * mp + c * mq;
-      }
-      for (int w = tid; w < (E / 2) * E; w += nt) {  // eigenvectors, stored transposed: rows p, q
-        const int i = w / E, j = w - i * E;
-        const int p = pp[i], q = qq[i];
-        const double c = cs[i], s = sn[i];
-        const double vp = Vl[(size_t)p * E + j], vq = Vl[(size_t)q * E + j];
-        Vl[(size_t)p * E + j] = c * vp - s * vq;
-        Vl[(size_t)q * E + j] = s * vp + c * vq;
-      }
-      __syncthreads();
     }
-    const bool stop = s_done != 0;  // read by every thread before thread 0 resets it
     __syncthreads();
-    if (stop) break;
-  }
-  // the G largest eigenvalues (ties: lower index) pick the embedding's columns
-  double* U = Uo + (size_t)l * E * G;
-  for (int a = tid; a < E; a += nt) {
-    const double la = M[a * E + a];
-    int rank = 0;
-    for (int b = 0; b < E; ++b) {
-      const double lb = M[b * E + b];
-      rank += (lb > la || (lb == la && b < a)) ? 1 : 0;
+    const double beta = bet[k];
+    if (beta == 0.0) continue;
+    for (int j = tid; j < m; j += nt) vv[j] = j == 0 ? red[0] : M[(k + 1 + j) * n + k];
+    __syncthreads();
+    {  // p = beta A22 v, eight threads per row (nt / 8 >= m rows)
+      const int i = tid >> 3;
+      double acc = 0.0;
+      if (i < m) {
+        const double* row = M + (k + 1 + i) * n + (k + 1);
+        for (int j = tid & 7; j < m; j += 8) acc = fma(row[j], vv[j], acc);
+      }
+      acc += __shfl_xor_sync(FULL, acc, 1);
+      acc += __shfl_xor_sync(FULL, acc, 2);
+      acc += __shfl_xor_sync(FULL, acc, 4);
+      if (i < m && (tid & 7) == 0) pw[i] = beta * acc;
     }
-    if (rank < G)  // eigenvector a is row a of the transposed matrix
-      for (int e = 0; e < E; ++e) U[(size_t)e * G + rank] = Vl[(size_t)a * E + e];
+    __syncthreads();
+    if (warp == 0) {
+      double t = 0.0;
+      for (int j = lane; j < m; j += 32) t = fma(vv[j], pw[j], t);
+      t = sp_warp_sum(t);
+      if (lane == 0) red[1] = 0.5 * beta * t;
+    }
+    __syncthreads();
+    const double kc = red[1];
+    for (int j = tid; j < m; j += nt) pw[j] = fma(-kc, vv[j], pw[j]);
+    __syncthreads();
+    for (int q = tid; q < m * m; q += nt) {  // A22 -= v w^T + w v^T
+      const int i = q / m, j = q - i * m;
+      double* e = M + (k + 1 + i) * n + (k + 1 + j);
+      *e = *e - vv[i] * pw[j] - pw[i] * vv[j];
+    }
+    for (int j = tid; j < m; j += nt) M[k * n + (k + 1 + j)] = vv[j];  // v, for the eigenvectors
+    __syncthreads();
+  }
+  if (tid == 0) {
+    dg[n - 2] = M[(n - 2) * n + (n - 2)];
+    sd[n - 2] = M[(n - 1) * n + (n - 2)];
+    dg[n - 1] = M[(n - 1) * n + (n - 1)];
+    sd[n - 1] = 0.0;
+    double tn = 0.0;  // Gershgorin bound of T
+    for (int i = 0; i < n; ++i) tn = fmax(tn, fabs(dg[i]) + fabs(sd[i]) + (i > 0 ? fabs(sd[i - 1]) : 0.0));
+    red[2] = tn;
   }
   __syncthreads();
+  for (int i = tid; i < n; i += nt) pw[i] = i > 0 ? sd[i - 1] * sd[i - 1] : 0.0;
+  __syncthreads();
+  const double eps = 2.220446049250313e-16;
+  const double tn = red[2];
+  const double pivmin = eps * tn + 1e-300;
+  // ---- the G largest eigenvalues by multisection, warp j for the (j+1)-th
+  if (warp < G) {
+    const int j = n - 1 - warp;  // eigenvalues below it: j
+    double lo = -tn - pivmin, hi = tn + pivmin;
+    for (int it = 0; it < 64; ++it) {
+      const double x = lo + (hi - lo) * ((double)(lane + 1) / 33.0);
+      const int cnt = sp_sturm(dg, pw, n, x, pivmin);
+      const unsigned above = __ballot_sync(FULL, cnt > j);
+      if (above == 0u) {
+        lo = __shfl_sync(FULL, x, 31);
+      } else {
+        const int f = __ffs(above) - 1;
+        const double xf = __shfl_sync(FULL, x, f), xp = __shfl_sync(FULL, x, f > 0 ? f - 1 : 0);
+        hi = xf;
+        if (f > 0) lo = xp;
+      }
+      if (hi - lo <= 2.0 * eps * fmax(fabs(lo), fabs(hi)) + pivmin) break;
+    }
+    if (lane == 0) lam[warp] = 0.5 * (lo + hi);
+  }
+  __syncthreads();
+  // ---- inverse iteration, one eigenvector after another (warp 0)
+  if (warp == 0) {
+    for (int w = 0; w < G; ++w) {
+      const double lambda = lam[w];
+      if (lane == 0) {
+        double ca = dg[0] - lambda, cb = sd[0];
+        for (int i = 0; i + 1 < n; ++i) {
+          const double nc = sd[i], na = dg[i + 1] - lambda, nb = i + 2 < n ? sd[i + 1] : 0.0;
+          if (fabs(ca) >= fabs(nc) || fabs(nc) <= pivmin) {  // no swap; a pivot below pivmin is floored
+            const double piv = fabs(ca) > pivmin ? ca : (ca >= 0.0 ? pivmin : -pivmin);
+            const double r = 1.0 / piv;
+            lu0[i] = r;
+            lu1[i] = cb;
+            lu2[i] = 0.0;
+            lmul[i] = nc * r;
+            lsw[i] = 0;
+            ca = na - lmul[i] * cb;
+            cb = nb;
+          } else {
+            const double r = 1.0 / nc;
+            lu0[i] = r;
+            lu1[i] = na;
+            lu2[i] = nb;
+            lmul[i] = ca * r;
+            lsw[i] = 1;
+            ca = cb - lmul[i] * na;
+            cb = -lmul[i] * nb;
+          }
+        }
+        lu0[n - 1] = 1.0 / (fabs(ca) > pivmin ? ca : (ca >= 0.0 ? pivmin : -pivmin));
+      }
+      double* y = Y + (size_t)w * n;
+      for (int i = lane; i < n; i += 32) y[i] = (double)(((unsigned)i * 2654435761u) % 1000u) / 1000.0 - 0.499;
+      __syncwarp();
+      for (int it = 0; it < 3; ++it) {
+        if (lane == 0) {  // solve (T - lambda I) y' = y
+          for (int i = 0; i + 1 < n; ++i) {
+            if (lsw[i]) {
+              const double t = y[i];
+              y[i] = y[i + 1];
+              y[i + 1] = t;
+            }
+            y[i + 1] -= lmul[i] * y[i];
+          }
+          y[n - 1] *= lu0[n - 1];
+          y[n - 2] = (y[n - 2] - lu1[n - 2] * y[n - 1]) * lu0[n - 2];
+          for (int i = n - 3; i >= 0; --i) y[i] = (y[i] - lu1[i] * y[i + 1] - lu2[i] * y[i + 2]) * lu0[i];
+        }
+        __syncwarp();
+        for (int u = 0; u < w; ++u) {
+          if (fabs(lam[u] - lambda) > 1e-3 * tn) continue;
+          const double* z = Y + (size_t)u * n;
+          double t = 0.0;
+          for (int i = lane; i < n; i += 32) t = fma(z[i], y[i], t);
+          t = sp_warp_sum(t);
+          for (int i = lane; i < n; i += 32) y[i] = fma(-t, z[i], y[i]);
+          __syncwarp();
+        }
+        double s2 = 0.0;
+        for (int i = lane; i < n; i += 32) s2 = fma(y[i], y[i], s2);
+        s2 = sp_warp_sum(s2);
+        const double sc = s2 > 0.0 ? 1.0 / sqrt(s2) : 0.0;
+        for (int i = lane; i < n; i += 32) y[i] *= sc;
+        __syncwarp();
+      }
+    }
+  }
+  __syncthreads();
+  // ---- back through the reflections: y <- H_k y for k = E-3 .. 0, warp j for vector j
+  if (warp < G) {
+    double* y = Y + (size_t)warp * n;
+    for (int k = n - 3; k >= 0; --k) {
+      if (bet[k] == 0.0) continue;
+      const int m = n - k - 1;
+      const double* v = M + k * n + (k + 1);
+      double t = 0.0;
+      for (int j = lane; j < m; j += 32) t = fma(v[j], y[k + 1 + j], t);
+      const double f = bet[k] * sp_warp_sum(t);
+      for (int j = lane; j < m; j += 32) y[k + 1 + j] = fma(-f, v[j], y[k + 1 + j]);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  double* U = Uo + (size_t)l * E * G;
   for (int e = tid; e < E; e += nt) {  // unit rows
     double n2 = 0.0;
-    for (int g = 0; g < G; ++g) n2 += U[(size_t)e * G + g] * U[(size_t)e * G + g];
-    const double n = sqrt(n2);
-    for (int g = 0; g < G; ++g) U[(size_t)e * G + g] = n > 0.0 ? U[(size_t)e * G + g] / n : 0.0;
+    for (int g = 0; g < G; ++g) n2 = fma(Y[(size_t)g * n + e], Y[(size_t)g * n + e], n2);
+    const double sc = n2 > 0.0 ? 1.0 / sqrt(n2) : 0.0;
+    for (int g = 0; g < G; ++g) U[(size_t)e * G + g] = Y[(size_t)g * n + e] * sc;
   }
 }
 
-size_t spec_embed_smem(int E);
+size_t spec_embed_smem(int E, int G);
 
 // Size-bounded assignment by warp 0 (lanes 0..31): a = previous assignment or
 // greedy nearest-with-room at the first step, then negative cycles of the
@@ -472,14 +624,13 @@ size_t spec_group_smem(int E, int G) {
 }
 
 struct SpLayout {
-  size_t V, U, deg, groups, total;
+  size_t U, deg, groups, total;
 };
 
 static SpLayout sp_layout(int L, int E, int G) {
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
   SpLayout o;
-  o.V = WS_HEADER;
-  o.U = o.V + r256((size_t)L * E * E * sizeof(double));
+  o.U = WS_HEADER;
   o.deg = o.U + r256((size_t)L * E * G * sizeof(double));
   o.groups = o.deg + r256((size_t)L * E * sizeof(double));
   o.total = o.groups + r256((size_t)L * SP_NGRID * E * sizeof(int32_t));
@@ -493,26 +644,27 @@ moer_status spectral_launch(const moer_dims* d, const int32_t* affinity, int32_t
   const int L = d->L, E = d->E;
   const SpLayout o = sp_layout(L, E, G);
   char* w = static_cast<char*>(ws);
-  double* V = reinterpret_cast<double*>(w + o.V);
   double* U = reinterpret_cast<double*>(w + o.U);
   double* deg = reinterpret_cast<double*>(w + o.deg);
   int32_t* groups = reinterpret_cast<int32_t*>(w + o.groups);
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(spec_embed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)spec_embed_smem(SP_MAXE)) != cudaSuccess ||
+                             (int)spec_embed_smem(SP_MAXE, SP_MAXG)) != cudaSuccess ||
         cudaFuncSetAttribute(spec_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)spec_group_smem(SP_MAXE, SP_MAXG)) != cudaSuccess)
       return MOER_ECUDA;
     configured = true;
   }
-  spec_embed_kernel<<<L, SP_EMBED_THREADS, spec_embed_smem(E), st>>>(affinity, E, G, V, U, deg);
+  spec_embed_kernel<<<L, SP_EMBED_THREADS, spec_embed_smem(E, G), st>>>(affinity, E, G, U, deg);
   spec_group_kernel<<<dim3(SP_NGRID, L), SP_GROUP_THREADS, spec_group_smem(E, G), st>>>(
       affinity, E, G, U, deg, groups, u_curve, s_curve, reinterpret_cast<uint32_t*>(ws));
   spec_knee_kernel<<<L, 32, 0, st>>>(groups, u_curve, E, group_of, knee);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
-size_t spec_embed_smem(int E) { return ((size_t)E * E + E + E + 32) * sizeof(double) + (size_t)E * sizeof(int); }
+size_t spec_embed_smem(int E, int G) {
+  return ((size_t)E * E + 10 * (size_t)E + 64 + (size_t)G * E) * sizeof(double) + (size_t)E * sizeof(int);
+}
 
 }  // namespace moer

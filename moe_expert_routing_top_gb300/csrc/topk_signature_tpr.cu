@@ -255,7 +255,7 @@ __device__ __forceinline__ void aff_add(uint32_t* aff, int a, int b) {
 // every row holding k distinct experts, the diagonal (the expert's load) is
 // its off-diagonal row sum divided by k - 1.  Adds the tile to layer `layer`
 // of the global co-activation and clears it.  All consumer threads call this
-// (it holds a barrier); `skip` leaves the tile alone (a consumer warp timed out).
+// (it holds a barrier); `skip` leaves the tile alone (a warp timed out).
 template <int E, int K>
 __device__ void tpr_flush_aff(const K1Params& p, uint32_t* aff, int* rsum, int layer, bool skip) {
   using G = TprGeo<E>;

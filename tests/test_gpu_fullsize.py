@@ -100,6 +100,39 @@ def test_qwen3_full(env):
     assert (rg >= 1.0).all()
 
 
+def test_deepseek_full(env):
+    """The E = 64, k = 6 shape at full size (two 32-expert slices per tile in
+    the logits pass): sampled rows, one whole mask layer, invariants everywhere."""
+    torch, pipeline, gu = env
+    orc = oracle.get()
+    wl = gen.make_workload("c2")
+    b = wl.batch()
+    bd = pipeline.BatchDev.from_host(b)
+    logits = gu.device_logits(wl, b)
+    rs = pipeline.RoutingStats.for_workload(wl, max_T=b.T, max_nblk=b.nblk, max_R=b.R)
+    rs.step(logits, bd)
+    torch.cuda.synchronize()
+    assert rs.status() == 0
+    del logits
+    topk = gu.host(rs.topk_for(b.T))
+    rng = np.random.RandomState(2)
+    layers = rng.randint(0, wl.L, size=4000)
+    toks = rng.randint(0, b.T, size=4000)
+    rows = gen.host_logit_rows(wl, b.tok_key, b.tok_dom, layers, toks)
+    assert np.array_equal(topk[layers, toks], orc.topk(rows, wl.k))
+    li = int(rng.randint(0, wl.m))
+    layer = int(wl.mask[li])
+    lrows = gen.host_logit_rows(wl, b.tok_key, b.tok_dom, np.full(b.T, layer, np.int32),
+                                np.arange(b.T))
+    tk_l = orc.topk(lrows, wl.k)
+    assert np.array_equal(topk[layer], tk_l)
+    bc = orc.block_counts(tk_l[None], wl.E, b.req_off, wl.B, np.array([0], np.int32))
+    assert np.array_equal(gu.host(rs.blk_cnt[:b.nblk, li]), bc[:, 0])
+    A = gu.host(rs.affinity)
+    assert np.array_equal(A[layer].astype(np.int64), orc.affinity(tk_l[None], wl.E)[0])
+    _check_affinity_props(A, gu.host(rs.W), wl.k, b.T)
+
+
 def test_online_stream_full(env):
     torch, pipeline, gu = env
     orc = oracle.get()
