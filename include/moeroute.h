@@ -363,6 +363,18 @@ MOER_API moer_status moer_idf_fit(const moer_dims* d, const int32_t* req_cnt, in
  * workspace passed to earlier calls. */
 MOER_API moer_status moer_ws_status(void* ws, moer_stream_t stream);
 
+/* Diagnostic of the bounded device waits (no passage of the pages: it checks
+ * the library's own failure reporting).  Launches one small kernel whose
+ * mbarrier wait can never complete; the wait gives up after limit_us
+ * microseconds, records MOER_ETIMEOUT in ws's status word (read it with
+ * moer_ws_status) and writes 1 to ws's 32-bit word 2 (0 had the wait passed).
+ * The kernel then ends normally; nothing faults.
+ * ws        device workspace of at least 256 bytes, 16-byte aligned.
+ * limit_us  1 .. 1,000,000.
+ * Returns MOER_EINVAL / MOER_ENOMEM / MOER_ERANGE for bad arguments (nothing
+ * launched), MOER_ECUDA if the launch fails, else MOER_OK. */
+MOER_API moer_status moer_wait_selftest(void* ws, size_t ws_bytes, uint32_t limit_us, moer_stream_t stream);
+
 /* Static description of a status code. */
 MOER_API const char* moer_status_str(moer_status s);
 

@@ -66,6 +66,7 @@ def _load():
         "moer_kmeans_workspace_bytes": ([i32, i32, i32], sz),
         "moer_kmeans_balanced": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_ws_status": ([vp, vp], ctypes.c_int),
+        "moer_wait_selftest": ([vp, sz, ctypes.c_uint32, vp], ctypes.c_int),
         "moer_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "moer_version": ([], ctypes.c_int32),
     }
@@ -83,7 +84,7 @@ EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_n
            "moer_replication_plan", "moer_kmeans_workspace_bytes", "moer_kmeans_balanced",
            "moer_mask_select_workspace_bytes", "moer_mask_select", "moer_spectral_workspace_bytes",
            "moer_spectral_groups",
-           "moer_ws_status",
+           "moer_ws_status", "moer_wait_selftest",
            "moer_status_str", "moer_version")
 
 
@@ -210,6 +211,12 @@ def moer_gate_topk(dims, hidden, T, H, w_gate, blk_tab, nblk, logits, topk, blk_
 def moer_ws_status(ws, stream=None) -> int:
     """Waits for the stream and returns (and clears) the workspace status code."""
     return int(LIB.moer_ws_status(_ptr(ws), _stream(stream)))
+
+
+def moer_wait_selftest(ws, ws_bytes, limit_us, stream=None) -> None:
+    """One kernel whose bounded wait cannot complete: it gives up after limit_us and
+    records MOER_ETIMEOUT in ws (read it with moer_ws_status)."""
+    _check("moer_wait_selftest", LIB.moer_wait_selftest(_ptr(ws), int(ws_bytes), int(limit_us), _stream(stream)))
 
 
 def moer_status_str(code: int) -> str:

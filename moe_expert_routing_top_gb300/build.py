@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoeroute.so")
 SOURCES = ["api.cu", "topk_signature.cu", "topk_signature_tpr.cu", "block_counts.cu", "stitch.cu",
            "affinity_load.cu", "route.cu", "noalloc.cu", "gate_topk.cu", "kmeans.cu",
-           "replicate.cu", "mask_select.cu", "spectral.cu"]
+           "replicate.cu", "mask_select.cu", "spectral.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", os.path.join(os.path.dirname(HERE), "include")]

@@ -21,6 +21,7 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
                           float* centroids, int32_t* assign, int32_t* info, double* objective, void* ws,
                           cudaStream_t st);
 size_t k1_scratch_bytes(const moer_dims* d, int64_t T);
+moer_status wait_selftest_launch(void* ws, uint32_t limit_us, cudaStream_t st);
 moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64_t T,
                                   const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
                                   uint8_t* blk_cnt, int32_t* affinity, void* ws, cudaStream_t st);
@@ -322,6 +323,13 @@ moer_status moer_kmeans_balanced(const float* sig, int32_t N, int32_t dim, int32
   if (ws_bytes < moer_kmeans_workspace_bytes(N, dim, D)) return MOER_ENOMEM;
   return moer::kmeans_launch(sig, N, dim, D, init_centroids, max_iter, centroids, assign, info, objective, ws,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+moer_status moer_wait_selftest(void* ws, size_t ws_bytes, uint32_t limit_us, moer_stream_t stream) {
+  if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
+  if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
+  if (limit_us < 1 || limit_us > 1000000) return MOER_ERANGE;
+  return moer::wait_selftest_launch(ws, limit_us, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moer_status moer_ws_status(void* ws, moer_stream_t stream) {

@@ -71,13 +71,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; returns false (and
-// records MOER_ETIMEOUT in *status) once WAIT_LIMIT_NS has passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// records MOER_ETIMEOUT in *status) once limit_ns has passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && (globaltimer_ns() - t0 > WAIT_LIMIT_NS || it >= WAIT_LIMIT_ITERS)) {
+    if ((it & 63u) == 63u && (globaltimer_ns() - t0 > limit_ns || it >= WAIT_LIMIT_ITERS)) {
       if (status) atomicOr(status, WS_BIT_ETIMEOUT);
       return false;
     }

@@ -157,3 +157,12 @@ def test_spectral_arguments(nat):
     assert _code(s, d, None, 8, 64, 64, 64, 64, 256, ws, 0) == 1     # no co-activation
     assert _code(s, d, 64, 8, 64, 64, BADPTR, 64, 256, ws, 0) == 1   # misaligned curve
     assert _code(s, d, 64, 8, 64, 64, 64, 64, 256, ws - 8, 0) == 5
+
+
+def test_wait_selftest_arguments(nat):
+    t = nat.LIB.moer_wait_selftest
+    assert t(None, 256, 1000, None) == 1
+    assert t(BADPTR, 256, 1000, None) == 1
+    assert t(64, 100, 1000, None) == 5
+    assert t(64, 256, 0, None) == 3
+    assert t(64, 256, 1000001, None) == 3
