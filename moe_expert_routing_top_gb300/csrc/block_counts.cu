@@ -6,7 +6,7 @@
 // each expert in their top-k.
 //
 // A segmented histogram over the block table: a persistent grid of warps walks
-// the KV blocks; per block the warp reads the block's top-k ids of up to eight
+// the KV blocks; per block the warp reads the block's top-k ids of up to sixteen
 // mask layers at once (contiguous uint8, len * k bytes per layer, as 4-byte
 // words when k is a multiple of 4), counts them into private shared-memory
 // rows of packed 8-bit counters (four
@@ -32,7 +32,7 @@ struct BcParams {
   int16_t layer_row[256];  // ids row-block of mask layer i
 };
 
-constexpr int BC_MC = 8;  // mask layers counted together (their loads in flight at once)
+constexpr int BC_MC = 16;  // mask layers counted together (their loads in flight at once)
 
 __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __grid_constant__ BcParams p) {
   extern __shared__ uint32_t bc_smem[];  // [BC_WARPS][BC_MC][E / 4]
