@@ -286,8 +286,11 @@ void orc_loads(const uint8_t* topk, int L, int64_t T, int k, int E,
       for (int j = 0; j < k; ++j)
         W[(size_t)l * (size_t)E + topk[((size_t)l * (size_t)T + (size_t)t) * (size_t)k + (size_t)j]] += 1;
   for (int l = 0; l < L; ++l) {
-    for (int e = 0; e < E; ++e)
-      Wg[(size_t)l * (size_t)G + group_of[(size_t)l * (size_t)E + (size_t)e]] += W[(size_t)l * (size_t)E + (size_t)e];
+    for (int e = 0; e < E; ++e) {
+      /* W_{l,g} sums the experts whose group is g; an id outside [0, G) names no group */
+      const int g = group_of[(size_t)l * (size_t)E + (size_t)e];
+      if (g >= 0 && g < G) Wg[(size_t)l * (size_t)G + (size_t)g] += W[(size_t)l * (size_t)E + (size_t)e];
+    }
     double sum = 0.0, mx = 0.0;
     for (int g = 0; g < G; ++g) {
       double w = (double)Wg[(size_t)l * (size_t)G + (size_t)g];
