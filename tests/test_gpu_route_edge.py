@@ -1,0 +1,94 @@
+"""moer_route on its degenerate settings against the oracle (O4-O6): tau = 0 (the nearest
+centroid), a band wider than every distance (join-the-shortest-queue over all decoders),
+one decoder, a request whose counts are all zero (signature 0, so every distance is the
+centroid's norm), equal loads (ties to the lowest index), and live routing where each
+choice raises its decoder's load.  Signatures and distances within the stated tolerance;
+choices identical except at the band edge (then any valid pick).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_routing_top_gb300 import _native as nat
+    return torch, nat
+
+
+def _inputs(seed, R, m, E, D):
+    rs = np.random.RandomState(seed)
+    cnt = rs.poisson(3.0, size=(R, m, E)).astype(np.int32)
+    cnt[0] = 0                                       # an empty request
+    cnt[1] = 0
+    cnt[1, :, 5] = 7                                 # a single expert per layer
+    idf = (1.0 + rs.random_sample((m, E))).astype(np.float32)
+    cen = rs.standard_normal((D, m * E)).astype(np.float32)
+    cen /= np.linalg.norm(cen, axis=1, keepdims=True).astype(np.float32)
+    cen *= np.float32(0.2)
+    return cnt, idf, cen
+
+
+def _run(env, cnt, idf, cen, tau, loads, live):
+    torch, nat = env
+    R, m, E = cnt.shape
+    D = cen.shape[0]
+    dims = nat.make_dims(E, 8, m, list(range(m)), 16)
+    dc = torch.from_numpy(cnt).cuda()
+    di = torch.from_numpy(idf).cuda()
+    dcen = torch.from_numpy(cen).cuda()
+    dl = torch.from_numpy(np.asarray(loads, dtype=np.int32)).cuda()
+    sig = torch.zeros((R, m * E), dtype=torch.float32, device="cuda")
+    dist = torch.zeros((R, D), dtype=torch.float32, device="cuda")
+    ch = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    wsb = nat.moer_workspace_bytes(dims, 0, 0, R, D)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    nat.moer_route(dims, dc, R, di, dcen, D, tau, dl, 1 if live else 0, sig, dist, ch, ws, wsb)
+    assert nat.moer_ws_status(ws) == 0
+    return sig.cpu().numpy(), dist.cpu().numpy(), ch.cpu().numpy(), dl.cpu().numpy()
+
+
+CASES = [  # (tau, D, live, equal loads)
+    (0.0, 8, False, False),
+    (1e6, 8, False, False),
+    (0.1, 1, False, False),
+    (0.1, 16, False, True),
+    (0.05, 16, True, True),
+    (1e6, 4, True, False),
+]
+
+
+@pytest.mark.parametrize("tau,D,live,equal", CASES)
+def test_route_degenerate_settings(env, tau, D, live, equal):
+    orc = oracle.get()
+    R, m, E = 200, 3, 64
+    cnt, idf, cen = _inputs(int(tau * 100) + D, R, m, E, D)
+    loads0 = np.zeros(D, np.int32) if equal else np.random.RandomState(D).randint(0, 64, size=D).astype(np.int32)
+    sig, dist, ch, loads = _run(env, cnt, idf, cen, tau, loads0, live)
+    osig, odist = orc.sig_dist(cnt, idf, cen)
+    gu.assert_close(sig, osig, "signature")
+    gu.assert_close(dist, odist, "distance")
+    assert (sig[0] == 0).all()                                   # empty request: zero signature
+    assert np.allclose(dist[0], np.linalg.norm(cen.astype(np.float64), axis=1), rtol=1e-5)
+    och, oloads = orc.route(odist, tau, loads0, live)
+    if live:
+        gu.check_live_route(ch, odist, tau, loads0, och)
+        assert loads.sum() == loads0.sum() + R                   # every request counted once
+        assert np.array_equal(np.bincount(ch, minlength=D) + loads0, loads)
+    else:
+        gu.check_static_route(ch, odist, tau, loads0, och)
+        assert np.array_equal(loads, loads0)                     # static: loads untouched
+    if D == 1:
+        assert (ch == 0).all()
+    if tau == 0.0 and not live:                                  # nearest centroid (off the band edge)
+        off = ~gu.band_edge_rows(odist, tau)
+        assert (ch[off] == odist.argmin(axis=1)[off]).all()
+    if tau >= 1e6 and not live:                                  # least loaded, lowest index on ties
+        assert (ch == int(np.lexsort((np.arange(D), loads0))[0])).all()
