@@ -167,6 +167,27 @@ class RoutingStats:
         self.affinity_load()
         self.route(bd.R, write_sig)
 
+    def capture_step(self, logits, bd: BatchDev, write_topk=True, write_sig=True):
+        """A CUDA graph of one ``step`` on these buffers and inputs (their device addresses
+        are baked in): ``replay()`` runs the whole step again with no per-call host work.
+
+        One eager step runs first, on the pipeline's stream, so that the library's one-time
+        set-up (kernel attributes, the tensor-map encoder) and any buffer growth happen
+        outside the capture; its counts accumulate like any step's.  The capture itself
+        runs on a side stream (the legacy default stream cannot be captured)."""
+        self.step(logits, bd, write_topk, write_sig)
+        torch.cuda.synchronize(self.affinity.device)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=self.affinity.device)
+        own = self.stream
+        self.stream = side
+        try:
+            with torch.cuda.graph(graph, stream=side):
+                self.step(logits, bd, write_topk, write_sig)
+        finally:
+            self.stream = own
+        return graph
+
     def status(self) -> int:
         return nat.moer_ws_status(self.ws, self.stream)
 
