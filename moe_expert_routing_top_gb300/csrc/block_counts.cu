@@ -258,16 +258,11 @@ moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t 
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
   const size_t smem = ((size_t)d->E * (d->E + 1) + d->E) * sizeof(int);
-  static bool configured = false;
-  if (!configured) {
-    const int most = (int)((128 * 129 + 128) * sizeof(int));
-    if (cudaFuncSetAttribute(affinity_ids_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(affinity_ids_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
-            cudaSuccess)
-      return MOER_ECUDA;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> set8{0}, set6{0};
+  const int most = (int)((128 * 129 + 128) * sizeof(int));
+  if (smem_optin(affinity_ids_kernel<8>, most, set8) != cudaSuccess ||
+      smem_optin(affinity_ids_kernel<6>, most, set6) != cudaSuccess)
+    return MOER_ECUDA;
   const int grid = (int)min64(nitems, (int64_t)sms * 2);
   if (d->k == 8)
     affinity_ids_kernel<8><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity);

@@ -466,13 +466,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 template <int K>
 cudaError_t gate_launch_k(const GateParams& p, int grid, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gate_topk_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)GK_SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> set{0};
+  const cudaError_t e = smem_optin(gate_topk_kernel<K>, (int)GK_SMEM, set);
+  if (e != cudaSuccess) return e;
   gate_topk_kernel<K><<<grid, GK_THREADS, GK_SMEM, st>>>(p);
   return cudaGetLastError();
 }

@@ -647,15 +647,10 @@ moer_status spectral_launch(const moer_dims* d, const int32_t* affinity, int32_t
   double* U = reinterpret_cast<double*>(w + o.U);
   double* deg = reinterpret_cast<double*>(w + o.deg);
   int32_t* groups = reinterpret_cast<int32_t*>(w + o.groups);
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(spec_embed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)spec_embed_smem(SP_MAXE, SP_MAXG)) != cudaSuccess ||
-        cudaFuncSetAttribute(spec_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)spec_group_smem(SP_MAXE, SP_MAXG)) != cudaSuccess)
-      return MOER_ECUDA;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> embed_set{0}, group_set{0};
+  if (smem_optin(spec_embed_kernel, (int)spec_embed_smem(SP_MAXE, SP_MAXG), embed_set) != cudaSuccess ||
+      smem_optin(spec_group_kernel, (int)spec_group_smem(SP_MAXE, SP_MAXG), group_set) != cudaSuccess)
+    return MOER_ECUDA;
   spec_embed_kernel<<<L, SP_EMBED_THREADS, spec_embed_smem(E, G), st>>>(affinity, E, G, U, deg);
   spec_group_kernel<<<dim3(SP_NGRID, L), SP_GROUP_THREADS, spec_group_smem(E, G), st>>>(
       affinity, E, G, U, deg, groups, u_curve, s_curve, reinterpret_cast<uint32_t*>(ws));

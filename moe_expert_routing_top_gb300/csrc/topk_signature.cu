@@ -270,13 +270,9 @@ __global__ void __launch_bounds__(K1Geo<EPL>::THREADS, 1) k1_kernel(const __grid
 template <int EPL>
 cudaError_t k1_launch(const K1Params& p, int grid, cudaStream_t st) {
   using G = K1Geo<EPL>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k1_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> set{0};
+  const cudaError_t e = smem_optin(k1_kernel<EPL>, (int)G::SMEM, set);
+  if (e != cudaSuccess) return e;
   k1_kernel<EPL><<<grid, G::THREADS, G::SMEM, st>>>(p);
   return cudaGetLastError();
 }

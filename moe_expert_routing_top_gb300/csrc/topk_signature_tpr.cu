@@ -497,13 +497,9 @@ __global__ void __launch_bounds__(TprGeo<E>::THREADS, 1) k1_tpr_kernel(const __g
 template <int E, int K>
 cudaError_t tpr_launch(const K1Params& p, int grid, cudaStream_t st) {
   using G = TprGeo<E>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k1_tpr_kernel<E, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)G::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> set{0};
+  const cudaError_t e = smem_optin(k1_tpr_kernel<E, K>, (int)G::SMEM, set);
+  if (e != cudaSuccess) return e;
   k1_tpr_kernel<E, K><<<grid, G::THREADS, G::SMEM, st>>>(p);
   return cudaGetLastError();
 }
