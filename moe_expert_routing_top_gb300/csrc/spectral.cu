@@ -319,16 +319,20 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
 
 size_t spec_embed_smem(int E, int G);
 
-// Size-bounded assignment by warp 0 (lanes 0..31): a = previous assignment or
-// greedy nearest-with-room at the first step, then negative cycles of the
-// residual graph on the G groups plus the slack node t = G are cancelled.
+// Size-bounded assignment by the whole CTA: a = previous assignment or greedy
+// nearest-with-room at the first step, then negative cycles of the residual
+// graph on the G groups plus the slack node t = G are cancelled.  The edge
+// minima (the cheapest member of u to move to v, ties to the lower point)
+// take all threads, a few per edge; warp 0 runs Bellman-Ford with a lane per
+// node and extracts a cycle; thread 0 moves its points.
 __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int* a, const int* prev, bool first,
                           double* W, int* widx, int* sz, int* s_pred, int* mv_pt, int* mv_to, int* nmv,
                           uint32_t* status) {
-  const int lane = threadIdx.x & 31;
+  __shared__ double sp_red[SP_GROUP_THREADS / 32];
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int n = G + 1, t = G, ld = G + 1;
   if (first) {
-    if (lane == 0) {
+    if (tid == 0) {
       for (int g = 0; g < G; ++g) sz[g] = 0;
       for (int e = 0; e < E; ++e) {
         int best = -1;
@@ -341,115 +345,132 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
       }
     }
   } else {
-    for (int e = lane; e < E; e += 32) a[e] = prev[e];
+    for (int e = tid; e < E; e += nt) a[e] = prev[e];
   }
   double mx = 0.0;
-  for (int q = lane; q < E * G; q += 32) mx = fmax(mx, fabs(cost[q]));
+  for (int q = tid; q < E * G; q += nt) mx = fmax(mx, fabs(cost[q]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(FULL, mx, o));
+  if (lane == 0) sp_red[warp] = mx;
+  __syncthreads();
+  mx = 0.0;
+  for (int w = 0; w < nt / 32; ++w) mx = fmax(mx, sp_red[w]);
   const double eps = 1e-12 * mx + 1e-300;
   const double big = 1.0 + 4.0 * (mx + 1.0) * E;  // any lower-bound repair beats any cost change
-  __syncwarp();
+  int tpe = 32;  // threads per edge: a power of two, so an edge's threads share a warp
+  while (tpe > 1 && tpe * G * G > nt) tpe >>= 1;
   const int max_pass = 16 * E + 1024;
   int done = 0;
   for (int pass = 0; pass < max_pass; ++pass) {
-    if (lane == 0) {
-      for (int g = 0; g < G; ++g) sz[g] = 0;
-      for (int e = 0; e < E; ++e) sz[a[e]] += 1;
-    }
-    __syncwarp();
-    for (int q = lane; q < G * G; q += 32) {  // edge u -> v: the cheapest member of u to move
+    for (int g = tid; g < G; g += nt) sz[g] = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += nt) atomicAdd(&sz[a[e]], 1);
+    for (int q0 = 0; q0 < G * G; q0 += nt / tpe) {  // edge u -> v: the cheapest member of u to move
+      const int q = q0 + tid / tpe, sub = tid % tpe;
       const int u = q / G, v = q - u * G;
       double best = INFINITY;
       int bp = INT_MAX;
-      if (u != v)
-        for (int p = 0; p < E; ++p) {
+      if (q < G * G && u != v)
+        for (int p = sub; p < E; p += tpe) {
           if (a[p] != u) continue;
           const double val = cost[p * G + v] - cost[p * G + u];
-          if (val < best) {
+          if (val < best || (val == best && p < bp)) {
             best = val;
             bp = p;
           }
         }
-      W[u * ld + v] = best;
-      widx[q] = bp;
-    }
-    for (int u = lane; u < G; u += 32) {
-      W[t * ld + u] = sz[u] > lo ? 0.0 : INFINITY;                        // u may shrink
-      W[u * ld + t] = sz[u] < lo ? -big : (sz[u] < hi ? 0.0 : INFINITY);  // u may (must) grow
-    }
-    if (lane == 0) W[t * ld + t] = INFINITY;
-    __syncwarp();
-    double dist = 0.0;
-    int pred = -1;
-    for (int round = 0; round < 2 * (n + 1); ++round) {
-      double best = dist;
-      int from = pred;
-      for (int u = 0; u < n; ++u) {
-        const double du = __shfl_sync(FULL, dist, u);
-        if (lane < n && u != lane) {
-          const double w = W[u * ld + lane];
-          if (w < INFINITY && du + w < best) {
-            best = du + w;
-            from = u;
-          }
+      for (int o = tpe >> 1; o > 0; o >>= 1) {
+        const double ob = __shfl_xor_sync(FULL, best, o);
+        const int op = __shfl_xor_sync(FULL, bp, o);
+        if (ob < best || (ob == best && op < bp)) {
+          best = ob;
+          bp = op;
         }
       }
-      const bool changed = best < dist;
-      dist = best;
-      pred = from;
-      if (!__any_sync(FULL, changed)) break;
+      if (q < G * G && sub == 0) {
+        W[u * ld + v] = best;
+        widx[q] = bp;
+      }
     }
-    if (lane < n) s_pred[lane] = pred;
-    __syncwarp();
-    int x = lane;
-    bool alive = lane < n;
-    for (int st = 0; st < n && alive; ++st) {
-      const int nx = s_pred[x];
-      if (nx < 0) alive = false;
-      else x = nx;
-    }
-    const unsigned on = __ballot_sync(FULL, alive);
-    const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
-    if (lane == 0) {
-      *nmv = 0;
-      if (on) {
-        int y = start, k = 0, m = 0;
-        double w = 0.0;
-        bool ok = true;
-        do {
-          const int py = s_pred[y];
-          if (py < 0) {
-            ok = false;
-            break;
+    __syncthreads();
+    if (warp == 0) {
+      for (int u = lane; u < G; u += 32) {
+        W[t * ld + u] = sz[u] > lo ? 0.0 : INFINITY;                        // u may shrink
+        W[u * ld + t] = sz[u] < lo ? -big : (sz[u] < hi ? 0.0 : INFINITY);  // u may (must) grow
+      }
+      if (lane == 0) W[t * ld + t] = INFINITY;
+      __syncwarp();
+      double dist = 0.0;
+      int pred = -1;
+      for (int round = 0; round < 2 * (n + 1); ++round) {
+        double best = dist;
+        int from = pred;
+        for (int u = 0; u < n; ++u) {
+          const double du = __shfl_sync(FULL, dist, u);
+          if (lane < n && u != lane) {
+            const double w = W[u * ld + lane];
+            if (w < INFINITY && du + w < best) {
+              best = du + w;
+              from = u;
+            }
           }
-          w += W[py * ld + y];
-          if (py != t && y != t) {
-            if (widx[py * G + y] >= E) {
+        }
+        const bool changed = best < dist;
+        dist = best;
+        pred = from;
+        if (!__any_sync(FULL, changed)) break;
+      }
+      if (lane < n) s_pred[lane] = pred;
+      __syncwarp();
+      int x = lane;
+      bool alive = lane < n;
+      for (int st = 0; st < n && alive; ++st) {
+        const int nx = s_pred[x];
+        if (nx < 0) alive = false;
+        else x = nx;
+      }
+      const unsigned on = __ballot_sync(FULL, alive);
+      const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
+      if (lane == 0) {
+        *nmv = 0;
+        if (on) {
+          int y = start, k = 0, m = 0;
+          double w = 0.0;
+          bool ok = true;
+          do {
+            const int py = s_pred[y];
+            if (py < 0) {
               ok = false;
               break;
             }
-            mv_pt[m] = widx[py * G + y];
-            mv_to[m] = y;
-            ++m;
-          }
-          y = py;
-          ++k;
-        } while (y != start && k <= n);
-        if (ok && y == start && w < -eps) *nmv = m;
+            w += W[py * ld + y];
+            if (py != t && y != t) {
+              if (widx[py * G + y] >= E) {
+                ok = false;
+                break;
+              }
+              mv_pt[m] = widx[py * G + y];
+              mv_to[m] = y;
+              ++m;
+            }
+            y = py;
+            ++k;
+          } while (y != start && k <= n);
+          if (ok && y == start && w < -eps) *nmv = m;
+        }
       }
     }
-    __syncwarp();
+    __syncthreads();
     if (*nmv == 0) {
       done = 1;
       break;
     }
-    if (lane == 0)
+    if (tid == 0)
       for (int m = 0; m < *nmv; ++m) a[mv_pt[m]] = mv_to[m];
-    __syncwarp();
+    __syncthreads();
   }
-  if (lane == 0 && !done) atomicOr(status, WS_BIT_ETIMEOUT);
-  __syncwarp();
+  if (tid == 0 && !done) atomicOr(status, WS_BIT_ETIMEOUT);
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(SP_GROUP_THREADS, 1)
@@ -520,7 +541,7 @@ __global__ void __launch_bounds__(SP_GROUP_THREADS, 1)
       cost[q] = dd;
     }
     __syncthreads();
-    if (warp == 0) sp_assign(cost, E, G, lo, hi, a, prev, first, W, widx, sz, s_pred, mv_pt, mv_to, &s_nmv, status);
+    sp_assign(cost, E, G, lo, hi, a, prev, first, W, widx, sz, s_pred, mv_pt, mv_to, &s_nmv, status);
     __syncthreads();
     int changed = 0;
     if (!first)
