@@ -323,8 +323,10 @@ size_t spec_embed_smem(int E, int G);
 // nearest-with-room at the first step, then negative cycles of the residual
 // graph on the G groups plus the slack node t = G are cancelled.  The edge
 // minima (the cheapest member of u to move to v, ties to the lower point)
-// take all threads, a few per edge; warp 0 runs Bellman-Ford with a lane per
-// node and extracts a cycle; thread 0 moves its points.
+// take all threads, a few per edge.  Disjoint negative 2-cycles between
+// groups (swaps) go first, several per pass; when none is left, warp 0 runs
+// Bellman-Ford with a lane per node and extracts a longer cycle (through the
+// slack node when sizes must change).  Thread 0 moves the points.
 __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int* a, const int* prev, bool first,
                           double* W, int* widx, int* sz, int* s_pred, int* mv_pt, int* mv_to, int* nmv,
                           uint32_t* status) {
@@ -398,65 +400,83 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
         W[t * ld + u] = sz[u] > lo ? 0.0 : INFINITY;                        // u may shrink
         W[u * ld + t] = sz[u] < lo ? -big : (sz[u] < hi ? 0.0 : INFINITY);  // u may (must) grow
       }
-      if (lane == 0) W[t * ld + t] = INFINITY;
-      __syncwarp();
-      double dist = 0.0;
-      int pred = -1;
-      for (int round = 0; round < 2 * (n + 1); ++round) {
-        double best = dist;
-        int from = pred;
-        for (int u = 0; u < n; ++u) {
-          const double du = __shfl_sync(FULL, dist, u);
-          if (lane < n && u != lane) {
-            const double w = W[u * ld + lane];
-            if (w < INFINITY && du + w < best) {
-              best = du + w;
-              from = u;
+      if (lane == 0) {
+        W[t * ld + t] = INFINITY;
+        // disjoint negative 2-cycles between groups first, first fit in (u, v)
+        // order: each swaps two points and leaves the sizes as they are
+        unsigned used = 0u;
+        int m = 0;
+        for (int u = 0; u < G; ++u)
+          for (int v = u + 1; v < G; ++v) {
+            if (((used >> u) | (used >> v)) & 1u) continue;
+            if (W[u * ld + v] + W[v * ld + u] < -eps) {
+              used |= (1u << u) | (1u << v);
+              mv_pt[m] = widx[u * G + v], mv_to[m] = v, ++m;
+              mv_pt[m] = widx[v * G + u], mv_to[m] = u, ++m;
             }
           }
-        }
-        const bool changed = best < dist;
-        dist = best;
-        pred = from;
-        if (!__any_sync(FULL, changed)) break;
+        *nmv = m;
       }
-      if (lane < n) s_pred[lane] = pred;
       __syncwarp();
-      int x = lane;
-      bool alive = lane < n;
-      for (int st = 0; st < n && alive; ++st) {
-        const int nx = s_pred[x];
-        if (nx < 0) alive = false;
-        else x = nx;
-      }
-      const unsigned on = __ballot_sync(FULL, alive);
-      const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
-      if (lane == 0) {
-        *nmv = 0;
-        if (on) {
-          int y = start, k = 0, m = 0;
-          double w = 0.0;
-          bool ok = true;
-          do {
-            const int py = s_pred[y];
-            if (py < 0) {
-              ok = false;
-              break;
+      if (*nmv == 0) {
+        double dist = 0.0;
+        int pred = -1;
+        for (int round = 0; round < 2 * (n + 1); ++round) {
+          double best = dist;
+          int from = pred;
+          for (int u = 0; u < n; ++u) {
+            const double du = __shfl_sync(FULL, dist, u);
+            if (lane < n && u != lane) {
+              const double w = W[u * ld + lane];
+              if (w < INFINITY && du + w < best) {
+                best = du + w;
+                from = u;
+              }
             }
-            w += W[py * ld + y];
-            if (py != t && y != t) {
-              if (widx[py * G + y] >= E) {
+          }
+          const bool changed = best < dist;
+          dist = best;
+          pred = from;
+          if (!__any_sync(FULL, changed)) break;
+        }
+        if (lane < n) s_pred[lane] = pred;
+        __syncwarp();
+        int x = lane;
+        bool alive = lane < n;
+        for (int st = 0; st < n && alive; ++st) {
+          const int nx = s_pred[x];
+          if (nx < 0) alive = false;
+          else x = nx;
+        }
+        const unsigned on = __ballot_sync(FULL, alive);
+        const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
+        if (lane == 0) {
+          *nmv = 0;
+          if (on) {
+            int y = start, k = 0, m = 0;
+            double w = 0.0;
+            bool ok = true;
+            do {
+              const int py = s_pred[y];
+              if (py < 0) {
                 ok = false;
                 break;
               }
-              mv_pt[m] = widx[py * G + y];
-              mv_to[m] = y;
-              ++m;
-            }
-            y = py;
-            ++k;
-          } while (y != start && k <= n);
-          if (ok && y == start && w < -eps) *nmv = m;
+              w += W[py * ld + y];
+              if (py != t && y != t) {
+                if (widx[py * G + y] >= E) {
+                  ok = false;
+                  break;
+                }
+                mv_pt[m] = widx[py * G + y];
+                mv_to[m] = y;
+                ++m;
+              }
+              y = py;
+              ++k;
+            } while (y != start && k <= n);
+            if (ok && y == start && w < -eps) *nmv = m;
+          }
         }
       }
     }
