@@ -210,59 +210,85 @@ def oracle_gate_pass(orc, wl, x, w):
     orc.route(dist, wl.tau, wl.loads0, wl.live)
 
 
-def run_reference_gate(args, ws):
-    import oracle
+def _ref_worker(cfg, i, share, nrounds, barrier, results):
+    """One host core of the reference arm: its share of the sample (requests, or c5
+    tokens through the fp64 gate) is made first, untimed; then each round starts at the
+    common barrier and runs the oracle over the share once."""
     import gen
-    wl = gen.make_workload("c5")
+    import oracle
     orc = oracle.get()
-    ntok = args.ref_tokens
-    x = gen.host_hidden(wl.seed, 0, ntok, wl.hidden_dim)
-    w = gen.host_wgate(wl.seed, wl.L, wl.hidden_dim, wl.E, wl.wgate_scale)
-    for _ in range(args.warmup):
-        oracle_gate_pass(orc, wl, x, w)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_gate_pass(orc, wl, x, w)
-    dt = (time.perf_counter() - t0) / args.steps
-    v = wl.L * ntok / dt
-    sample = f"first {ntok} tokens of c5 as one request ({ntok} tokens x {wl.L} layers) per step"
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD["c5"], "sample": sample},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
+    wl = gen.make_workload(cfg)
+    if cfg == "c5":
+        x = gen.host_hidden(wl.seed, i * share, share, wl.hidden_dim)
+        w = gen.host_wgate(wl.seed, wl.L, wl.hidden_dim, wl.E, wl.wgate_scale)
+        units = share
+        run = lambda: oracle_gate_pass(orc, wl, x, w)  # noqa: E731
+    else:
+        b = wl.batch(i * share, (i + 1) * share)
+        logits = gen.host_logits(wl, b.tok_key, b.tok_dom)
+        units = b.T
+        run = lambda: oracle_pass(orc, wl, b, logits)  # noqa: E731
+    for _ in range(nrounds):
+        barrier.wait()
+        run()
+        results.put(units)
 
 
 def run_reference(args):
+    """The oracle, as it stands, on every host core: one spawned process per core, each with
+    its own share of a bounded sample (args.ref_requests requests of the config, or
+    args.ref_tokens c5 tokens through the fp64 gate); a step is one round of all shares,
+    timed from their common start to the last one's end."""
+    import multiprocessing as mp
     import oracle
     import gen
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    if args.config == "c5":
-        return run_reference_gate(args, ws)
-    wl = gen.make_workload(args.config)
-    orc = oracle.get()
-    b, logits = cpu_sample(wl, args.ref_requests)
-    units = wl.L * b.T
-    for _ in range(args.warmup):
-        oracle_pass(orc, wl, b, logits)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_pass(orc, wl, b, logits)
-    dt = (time.perf_counter() - t0) / args.steps
-    v = units / dt
-    sample = f"first {args.ref_requests} requests of {args.config} ({b.T} tokens x {wl.L} layers) per step"
+    oracle.get()  # built once here, so the workers only load it
+    cfg = args.config
+    wl = gen.make_workload(cfg)
+    try:
+        ncores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        ncores = os.cpu_count() or 1
+    share = args.ref_tokens if cfg == "c5" else args.ref_requests
+    limit = (int(np.sum(wl.prompt_len)) if cfg == "c5" else wl.R) // share  # shares the workload holds
+    ncores = max(1, min(ncores, limit))
+    nrounds = args.warmup + args.steps
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(ncores + 1)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_ref_worker, args=(cfg, i, share, nrounds, barrier, results))
+             for i in range(ncores)]
+    for pr in procs:
+        pr.start()
+    try:
+        total_t, total_units = 0.0, 0
+        for r in range(nrounds):
+            barrier.wait(timeout=600)
+            t0 = time.perf_counter()
+            units = sum(results.get(timeout=600) for _ in procs)
+            dt = time.perf_counter() - t0
+            if r >= args.warmup:
+                total_t += dt
+                total_units += units
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+    v = wl.L * total_units / total_t
+    per = total_units // max(args.steps, 1)
+    if cfg == "c5":
+        sample = (f"{share} c5 tokens per process through the fp64 gate on {ncores} host cores "
+                  f"({per} tokens x {wl.L} layers) per step")
+    else:
+        sample = (f"first {ncores * share} requests of {cfg}, {share} per process on {ncores} host "
+                  f"cores ({per} tokens x {wl.L} layers) per step")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD.get(args.config, args.config),
-                                            "sample": sample},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "data": "synthetic", "config": {"workload": WORKLOAD.get(cfg, cfg), "sample": sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": ncores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
