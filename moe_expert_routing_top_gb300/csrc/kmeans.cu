@@ -36,6 +36,7 @@ namespace moer {
 
 constexpr int KM_MAXD = 32;
 constexpr int KM_THREADS = 1024;
+constexpr int KM_SORT_MAX = 2048;  // points put in regret order for the first step's start
 
 struct KmState {
   int32_t steps;      // assignment steps done
@@ -112,6 +113,8 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   __shared__ int s_pred[KM_MAXD];
   __shared__ double red[KM_THREADS / 32];
   __shared__ int s_first;
+  __shared__ double s_key[KM_SORT_MAX];
+  __shared__ int s_ord[KM_SORT_MAX];
   if (state->converged) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -125,12 +128,59 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   __syncthreads();
   const bool first = s_first != 0;
 
-  // 1. a feasible start: the previous assignment, or greedy nearest-with-room
+  // 1. a feasible start: the previous assignment, or greedy nearest-with-room in
+  //    regret order (the points whose nearest centroid beats their second nearest
+  //    by most go first; index order when N > KM_SORT_MAX), which leaves fewer
+  //    cycles to cancel than index order
+  const bool sorted = first && N <= KM_SORT_MAX;
+  if (sorted) {
+    int P = 1;
+    while (P < N) P <<= 1;
+    for (int i = tid; i < P; i += KM_THREADS) {
+      double rk = -1.0;  // padding sorts last
+      if (i < N) {
+        double b1 = INFINITY, b2 = INFINITY;
+        for (int d = 0; d < D; ++d) {
+          const double c = cost[(size_t)i * D + d];
+          if (c < b1) {
+            b2 = b1;
+            b1 = c;
+          } else if (c < b2) {
+            b2 = c;
+          }
+        }
+        rk = D > 1 ? b2 - b1 : 0.0;
+      }
+      s_key[i] = rk;
+      s_ord[i] = i;
+    }
+    __syncthreads();
+    // bitonic sort: larger regret first, then lower index
+    for (int k = 2; k <= P; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < P; i += KM_THREADS) {
+          const int m = i ^ j;
+          if (m > i) {
+            const double ki = s_key[i], km = s_key[m];
+            const int oi = s_ord[i], om = s_ord[m];
+            const bool i_first = ki > km || (ki == km && oi < om);
+            if (((i & k) == 0) != i_first) {
+              s_key[i] = km;
+              s_key[m] = ki;
+              s_ord[i] = om;
+              s_ord[m] = oi;
+            }
+          }
+        }
+        __syncthreads();
+      }
+  }
   if (first) {
     if (tid == 0) {
       int cnt[KM_MAXD];
       for (int d = 0; d < D; ++d) cnt[d] = 0;
-      for (int i = 0; i < N; ++i) {
+      for (int r = 0; r < N; ++r) {
+        const int i = sorted ? s_ord[r] : r;
         int best = -1;
         double bc = 0.0;
         for (int d = 0; d < D; ++d) {
