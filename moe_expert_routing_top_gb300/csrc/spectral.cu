@@ -319,8 +319,8 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
 
 size_t spec_embed_smem(int E, int G);
 
-// Size-bounded assignment by the whole CTA: a = previous assignment or greedy
-// nearest-with-room at the first step, then negative cycles of the residual
+// Size-bounded assignment by the whole CTA: a = previous assignment or, at the
+// first step, greedy nearest-with-room in regret order, then negative cycles of the residual
 // graph on the G groups plus the slack node t = G are cancelled.  The edge
 // minima (the cheapest member of u to move to v, ties to the lower point)
 // take all threads, a few per edge.  Disjoint negative 2-cycles between
@@ -331,12 +331,56 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
                           double* W, int* widx, int* sz, int* s_pred, int* mv_pt, int* mv_to, int* nmv,
                           uint32_t* status) {
   __shared__ double sp_red[SP_GROUP_THREADS / 32];
+  __shared__ double s_key[SP_MAXE];
+  __shared__ int s_ord[SP_MAXE];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int n = G + 1, t = G, ld = G + 1;
   if (first) {
+    // greedy nearest-with-room in regret order: the experts whose nearest centroid
+    // beats their second nearest by most go first (larger regret, then lower id)
+    int P = 1;
+    while (P < E) P <<= 1;
+    for (int i = tid; i < P; i += nt) {
+      double rk = -1.0;  // padding sorts last
+      if (i < E) {
+        double b1 = INFINITY, b2 = INFINITY;
+        for (int g = 0; g < G; ++g) {
+          const double c = cost[i * G + g];
+          if (c < b1) {
+            b2 = b1;
+            b1 = c;
+          } else if (c < b2) {
+            b2 = c;
+          }
+        }
+        rk = b2 - b1;
+      }
+      s_key[i] = rk;
+      s_ord[i] = i;
+    }
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < P; i += nt) {
+          const int m = i ^ j;
+          if (m > i) {
+            const double ki = s_key[i], km = s_key[m];
+            const int oi = s_ord[i], om = s_ord[m];
+            const bool i_first = ki > km || (ki == km && oi < om);
+            if (((i & k) == 0) != i_first) {
+              s_key[i] = km;
+              s_key[m] = ki;
+              s_ord[i] = om;
+              s_ord[m] = oi;
+            }
+          }
+        }
+        __syncthreads();
+      }
     if (tid == 0) {
       for (int g = 0; g < G; ++g) sz[g] = 0;
-      for (int e = 0; e < E; ++e) {
+      for (int r = 0; r < E; ++r) {
+        const int e = s_ord[r];
         int best = -1;
         for (int g = 0; g < G; ++g) {
           if (sz[g] >= hi) continue;
