@@ -18,11 +18,13 @@
 //   * mask_stats_kernel: one CTA per (request, layer); the two halves' ids go
 //     into shared-memory histograms (at k = 8 one 8-byte load per token, four
 //     in flight per thread), then the three sums in fp64.
-//   * per greedy step, mask_eval_kernel (one CTA per candidate layer, threads
-//     over the requests: running sums of the chosen layers + the candidate's,
-//     fp64 cosines, a block reduction) and mask_pick_kernel (the argmax, then
-//     the chosen layer's sums added to every request's running sums).  The fp64
-//     square roots and divisions are spread over L SMs instead of one.
+//   * per greedy step, one mask_step_kernel: CTAs over (request slice,
+//     candidate layer) evaluate the candidates (fp64 cosines of the running
+//     sums plus the candidate's), and the last CTA to finish picks the layer
+//     and adds its sums to the running sums.  The fp64 square roots and
+//     divisions are spread over the SMs, and a step is one launch.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moer {
@@ -30,6 +32,7 @@ namespace moer {
 constexpr int MS_STATS_THREADS = 128;
 constexpr int MS_UNROLL = 4;  // token loads in flight per thread
 constexpr int MS_EVAL_THREADS = 256;
+constexpr int MS_MAX_SLICES = 16;  // request slices per candidate layer in one greedy step
 
 __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint8_t* __restrict__ topk, int64_t T,
                                                                       int k, int E, int L,
@@ -131,24 +134,31 @@ __device__ __forceinline__ double ms_cos(double s11, double s22, double s12) {
   return (s11 > 0.0 && s22 > 0.0) ? s12 / sqrt(s11 * s22) : 0.0;
 }
 
-// One greedy step, part 1: CTA l evaluates quality(M + {l}) for a layer l not
-// chosen yet -- the mean over requests of the cosine from the running sums of
-// the chosen layers plus layer l's sums.  run [R][3] is zeroed by the host.
-__global__ void __launch_bounds__(MS_EVAL_THREADS) mask_eval_kernel(const double* __restrict__ stats, int R,
-                                                                    const double* __restrict__ run,
-                                                                    const unsigned char* __restrict__ taken,
-                                                                    double* __restrict__ qual) {
+// One greedy step.  CTA (s, l) evaluates candidate layer l over its slice of
+// the requests: running sums of the chosen layers + the candidate's, fp64
+// cosines, a block reduction to one partial sum.  The CTA that finishes last
+// (a counter that every CTA bumps once, after publishing its partial: no CTA
+// waits for another) sums each layer's partials in slice order, takes the best
+// layer not chosen yet (ties: the lower layer; chosen layers read -inf),
+// records it, adds its sums to every request's running sums and resets the
+// counter for the next step.
+__global__ void __launch_bounds__(MS_EVAL_THREADS) mask_step_kernel(const double* __restrict__ stats, int R, int L,
+                                                                    double* run, unsigned char* taken,
+                                                                    double* part, unsigned int* counter, int step,
+                                                                    int32_t* __restrict__ mask_out,
+                                                                    double* __restrict__ quality_out) {
   __shared__ double red[MS_EVAL_THREADS / 32];
-  const int l = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (taken[l]) {  // never picked again
-    if (tid == 0) qual[l] = -INFINITY;
-    return;
-  }
+  __shared__ int s_last;
+  const int S = gridDim.x, s = blockIdx.x, l = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (R + S - 1) / S, r0 = s * per, r1 = min(R, r0 + per);
   double acc = 0.0;
-  for (int r = tid; r < R; r += MS_EVAL_THREADS) {
-    const double* s = stats + ((size_t)l * R + r) * 3;
-    const double* u = run + (size_t)r * 3;
-    acc += ms_cos(u[0] + s[0], u[1] + s[1], u[2] + s[2]);
+  if (!taken[l]) {
+    for (int r = r0 + tid; r < r1; r += MS_EVAL_THREADS) {
+      const double* sv = stats + ((size_t)l * R + r) * 3;
+      const double* u = run + (size_t)r * 3;
+      acc += ms_cos(u[0] + sv[0], u[1] + sv[1], u[2] + sv[2]);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
@@ -157,46 +167,61 @@ __global__ void __launch_bounds__(MS_EVAL_THREADS) mask_eval_kernel(const double
   if (tid == 0) {
     double sum = 0.0;
     for (int w = 0; w < MS_EVAL_THREADS / 32; ++w) sum += red[w];
-    qual[l] = sum / (double)R;
+    part[(size_t)l * S + s] = sum;
+    __threadfence();
+    s_last = atomicAdd(counter, 1u) == (unsigned)(S * L) - 1u;
   }
-}
-
-// Part 2: the best layer not chosen yet (ties: the lower layer; chosen layers
-// read -inf) joins the mask -- every CTA finds the same one from the read-only
-// qualities, CTA 0 records it -- and its sums join every request's running sums.
-__global__ void __launch_bounds__(MS_EVAL_THREADS) mask_pick_kernel(const double* __restrict__ stats, int R, int L,
-                                                                    double* __restrict__ run,
-                                                                    unsigned char* __restrict__ taken,
-                                                                    const double* __restrict__ qual, int step,
-                                                                    int32_t* __restrict__ mask_out,
-                                                                    double* __restrict__ quality_out) {
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Each thread takes layers tid, tid + blockDim, ...; then an argmax over the
+  // threads' (quality, layer) pairs, ties to the lower layer.
+  __shared__ double s_q[MS_EVAL_THREADS / 32];
+  __shared__ int s_c[MS_EVAL_THREADS / 32];
   __shared__ int s_best;
-  if (threadIdx.x == 0) {
-    int best = 0;
-    for (int l = 1; l < L; ++l)
-      if (qual[l] > qual[best]) best = l;
-    s_best = best;
-    if (blockIdx.x == 0) {
-      taken[best] = 1;
-      mask_out[step] = best;
-      if (quality_out != nullptr) quality_out[step] = qual[best];
+  double bq = -INFINITY;
+  int bc = L;
+  for (int c = tid; c < L; c += MS_EVAL_THREADS) {
+    double q = -INFINITY;
+    if (!taken[c]) {
+      double sum = 0.0;
+      for (int j = 0; j < S; ++j) sum += __ldcg(part + (size_t)c * S + j);
+      q = sum / (double)R;
     }
+    if (bc == L || q > bq) bq = q, bc = c;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double oq = __shfl_xor_sync(FULL, bq, o);
+    const int oc = __shfl_xor_sync(FULL, bc, o);
+    if (oc < L && (bc == L || oq > bq || (oq == bq && oc < bc))) bq = oq, bc = oc;
+  }
+  if (lane == 0) s_q[warp] = bq, s_c[warp] = bc;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < MS_EVAL_THREADS / 32; ++w)
+      if (s_c[w] < L && (bc == L || s_q[w] > bq || (s_q[w] == bq && s_c[w] < bc))) bq = s_q[w], bc = s_c[w];
+    s_best = bc;
+    taken[bc] = 1;
+    mask_out[step] = bc;
+    if (quality_out != nullptr) quality_out[step] = bq;
+    *counter = 0u;
   }
   __syncthreads();
   const int best = s_best;
-  for (int r = blockIdx.x * MS_EVAL_THREADS + threadIdx.x; r < R; r += gridDim.x * MS_EVAL_THREADS) {
-    const double* s = stats + ((size_t)best * R + r) * 3;
+  for (int r = tid; r < R; r += MS_EVAL_THREADS) {
+    const double* sv = stats + ((size_t)best * R + r) * 3;
     double* u = run + (size_t)r * 3;
-    u[0] += s[0];
-    u[1] += s[1];
-    u[2] += s[2];
+    u[0] += sv[0];
+    u[1] += sv[1];
+    u[2] += sv[2];
   }
 }
 
 size_t mask_select_workspace_bytes(int32_t L, int32_t R) {
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
   return WS_HEADER + r256((size_t)R * L * 3 * sizeof(double)) + r256((size_t)R * 3 * sizeof(double)) +
-         r256((size_t)L * sizeof(double)) + r256((size_t)L);
+         r256((size_t)L * MS_MAX_SLICES * sizeof(double)) + r256((size_t)L) + 256;
 }
 
 moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off, int32_t R,
@@ -206,18 +231,21 @@ moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t 
   char* w = static_cast<char*>(ws);
   double* stats = reinterpret_cast<double*>(w + WS_HEADER);
   double* run = reinterpret_cast<double*>(w + WS_HEADER + r256((size_t)R * d->L * 3 * sizeof(double)));
-  double* qual = reinterpret_cast<double*>(reinterpret_cast<char*>(run) + r256((size_t)R * 3 * sizeof(double)));
-  unsigned char* taken = reinterpret_cast<unsigned char*>(qual) + r256((size_t)d->L * sizeof(double));
+  double* part = reinterpret_cast<double*>(reinterpret_cast<char*>(run) + r256((size_t)R * 3 * sizeof(double)));
+  unsigned char* taken = reinterpret_cast<unsigned char*>(part) + r256((size_t)d->L * MS_MAX_SLICES * sizeof(double));
+  unsigned int* counter = reinterpret_cast<unsigned int*>(taken + r256((size_t)d->L));
   if (cudaMemsetAsync(run, 0, (size_t)R * 3 * sizeof(double), st) != cudaSuccess) return MOER_ECUDA;
-  if (cudaMemsetAsync(taken, 0, (size_t)d->L, st) != cudaSuccess) return MOER_ECUDA;
+  if (cudaMemsetAsync(taken, 0, r256((size_t)d->L) + sizeof(unsigned int), st) != cudaSuccess) return MOER_ECUDA;
   mask_stats_kernel<<<dim3((unsigned)R, (unsigned)d->L), MS_STATS_THREADS, 0, st>>>(
       topk, T, d->k, d->E, d->L, req_off, idf, stats, reinterpret_cast<uint32_t*>(ws));
-  const unsigned pick_grid = (unsigned)min64(((int64_t)R + MS_EVAL_THREADS - 1) / MS_EVAL_THREADS, 64);
-  for (int step = 0; step < m; ++step) {
-    mask_eval_kernel<<<d->L, MS_EVAL_THREADS, 0, st>>>(stats, R, run, taken, qual);
-    mask_pick_kernel<<<pick_grid, MS_EVAL_THREADS, 0, st>>>(stats, R, d->L, run, taken, qual, step, mask_out,
-                                                            quality_out);
-  }
+  // Request slices per layer: about two CTAs per SM in all, at least one
+  // request per thread.
+  const int64_t want = std::max<int64_t>(1, 2 * (int64_t)device_sm_count() / d->L);
+  const unsigned S = (unsigned)std::min<int64_t>(
+      std::min<int64_t>(((int64_t)R + MS_EVAL_THREADS - 1) / MS_EVAL_THREADS, want), MS_MAX_SLICES);
+  for (int step = 0; step < m; ++step)
+    mask_step_kernel<<<dim3(std::max(1u, S), (unsigned)d->L), MS_EVAL_THREADS, 0, st>>>(
+        stats, R, d->L, run, taken, part, counter, step, mask_out, quality_out);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
