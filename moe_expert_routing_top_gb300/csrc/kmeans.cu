@@ -21,11 +21,14 @@
 //     A cycle moves one point out of and one into every cluster on it, so the
 //     sizes stay put; with no negative cycle left the assignment is optimal
 //     (min-cost flow optimality).  Edge minima are scans of per-cluster member
-//     lists (a few threads per edge, shuffle-reduced).  Each pass first applies
+//     lists (a few threads per edge, shuffle-reduced); the costs, assignment
+//     and member lists are staged in shared memory when they fit.  Each pass first applies
 //     every disjoint negative 2-cycle (pairwise swap) it finds; only when none
 //     is left does one warp run Bellman-Ford over the D <= 32 nodes and cancel
 //     a longer cycle read off the predecessor graph.
-//   * Means: one thread per (centroid, coordinate), points in index order.
+//   * Means: one thread per (centroid, coordinate), points in index order,
+//     read from per-cluster member lists that the assignment step leaves in
+//     index order.
 //   * Every kernel of a step returns at once after convergence, so the host
 //     launches max_iter steps without reading anything back.
 #include <climits>
@@ -46,7 +49,7 @@ struct KmState {
 };
 
 struct KmLayout {
-  size_t state, cost, cent, prev, mem, pos, total;
+  size_t state, cost, cent, prev, mem, pos, dkey, total;
 };
 
 static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
@@ -58,7 +61,8 @@ static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
   l.prev = l.cent + r256((size_t)D * dim * sizeof(double));
   l.mem = l.prev + r256((size_t)N * sizeof(int32_t));
   l.pos = l.mem + r256((size_t)N * sizeof(int32_t));
-  l.total = l.pos + r256((size_t)N * sizeof(int32_t));
+  l.dkey = l.pos + r256((size_t)N * sizeof(int32_t));
+  l.total = l.dkey + r256((size_t)N * (D + 1) * sizeof(unsigned long long));
   return l;
 }
 
@@ -70,53 +74,114 @@ __global__ void km_init_kernel(const float* __restrict__ init, double* __restric
 }
 
 // cost[i][d] = ||s_i - c_d||^2 in fp64; block i, warp w takes centroids w, w + 8, ...
+// The signature row is widened to fp64 once per block, a chunk at a time, into
+// shared memory (each lane still sums its elements j = lane, lane + 32, ... in
+// order, then the warp reduces).
+constexpr int KM_COST_CHUNK = 2048;
 __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ sig, int32_t dim, int32_t D,
                                                       const double* __restrict__ cent, double* __restrict__ cost,
                                                       const KmState* state, int force) {
+  __shared__ double s64[KM_COST_CHUNK];
   if (!force && state->converged) return;
   const int i = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* s = sig + (size_t)i * dim;
-  for (int d = warp; d < D; d += 8) {
-    const double* c = cent + (size_t)d * dim;
-    double acc = 0.0;
-    for (int j = lane; j < dim; j += 32) {
-      const double t = (double)s[j] - c[j];
-      acc = fma(t, t, acc);
-    }
+  double acc[KM_MAXD / 8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL, acc, o);
-    if (lane == 0) cost[(size_t)i * D + d] = acc;
+  for (int q = 0; q < KM_MAXD / 8; ++q) acc[q] = 0.0;
+  for (int j0 = 0; j0 < dim; j0 += KM_COST_CHUNK) {
+    const int n = min(KM_COST_CHUNK, dim - j0);
+    for (int j = threadIdx.x; j < n; j += 256) s64[j] = (double)s[j0 + j];
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < KM_MAXD / 8; ++q) {
+      const int d = warp + 8 * q;
+      if (d < D) {
+        const double* c = cent + (size_t)d * dim + j0;
+        double t_acc = acc[q];
+        for (int j = lane; j < n; j += 32) {
+          const double t = s64[j] - c[j];
+          t_acc = fma(t, t, t_acc);
+        }
+        acc[q] = t_acc;
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int q = 0; q < KM_MAXD / 8; ++q) {
+    const int d = warp + 8 * q;
+    if (d < D) {
+      double t_acc = acc[q];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t_acc += __shfl_xor_sync(FULL, t_acc, o);
+      if (lane == 0) cost[(size_t)i * D + d] = t_acc;
+    }
   }
 }
 
-// Lexicographic (value, point) minimum, for edge minima that do not depend on
-// the order in which the points are visited.
-__device__ __forceinline__ void vmin(double& v, int& p, double v2, int p2) {
-  if (v2 < v || (v2 == v && p2 < p)) {
-    v = v2;
-    p = p2;
-  }
+// Order-preserving 64-bit key of a double that is not NaN: unsigned order of
+// the keys is the numeric order of the values (-0.0 sorts just below +0.0;
+// neither the costs, sums of squares, nor their differences produce -0.0).
+// GB300 issues fp64 compares at a small fraction of the integer rate, so the
+// scans and reductions below compare keys.
+__device__ __forceinline__ unsigned long long okey(double x) {
+  const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  return (b >> 63) ? ~b : b | 0x8000000000000000ull;
+}
+__device__ __forceinline__ double okey_value(unsigned long long k) {
+  return __longlong_as_double((long long)((k >> 63) ? k & 0x7FFFFFFFFFFFFFFFull : ~k));
+}
+
+// Warp-wide lexicographic minimum of (key, idx) over the lanes; every lane
+// gets the result.  Keys compare as two 32-bit halves with redux.sync.
+__device__ __forceinline__ void warp_min_key(unsigned long long& key, int& idx) {
+  const unsigned hi = (unsigned)(key >> 32), lo = (unsigned)key;
+  const unsigned mhi = __reduce_min_sync(FULL, hi);
+  const unsigned mlo = __reduce_min_sync(FULL, hi == mhi ? lo : 0xFFFFFFFFu);
+  const bool at = hi == mhi && lo == mlo;
+  idx = (int)__reduce_min_sync(FULL, at ? (unsigned)idx : 0xFFFFFFFFu);
+  key = ((unsigned long long)mhi << 32) | mlo;
 }
 
 // One balanced assignment step (single CTA).  `a` holds the result; `prev` the
 // previous step's assignment; `mem` / `pos` the per-cluster member lists
-// (cluster u's members at mem[off_u .. off_u + cap_u), pos[p] = p's slot).
+// (cluster u's members at mem[off_u .. off_u + cap_u), pos[p] = p's slot);
+// `dkey` row p holds okey(cost[p][v] - cost[p][a(p)]) for every v (stride
+// D + 1), the gain of moving p, rewritten only for the points that move.  With
+// `staged`, the assignment, member lists and keys live in shared memory
+// instead (the global arrays then only receive the result).
 __global__ void __launch_bounds__(KM_THREADS, 1)
     km_assign_kernel(const double* __restrict__ cost, int32_t N, int32_t D, int32_t* __restrict__ a,
                      int32_t* __restrict__ prev, int32_t* __restrict__ mem, int32_t* __restrict__ pos,
-                     KmState* state, int32_t max_pass, uint32_t* status) {
+                     unsigned long long* __restrict__ dkey, KmState* state, int32_t max_pass, int32_t staged,
+                     uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char km_dyn[];
   __shared__ double wval[KM_MAXD * KM_MAXD];
   __shared__ int widx[KM_MAXD * KM_MAXD];
   __shared__ int off[KM_MAXD + 1], fill[KM_MAXD];
   __shared__ int mv_pt[KM_MAXD], mv_from[KM_MAXD], mv_to[KM_MAXD], freed[KM_MAXD];
   __shared__ int nmv;
   __shared__ int s_pred[KM_MAXD];
-  __shared__ double red[KM_THREADS / 32];
+  __shared__ double bf_dist[2][KM_MAXD];
+  __shared__ unsigned negmask[KM_MAXD];
+  __shared__ unsigned long long red[KM_THREADS / 32];
+  __shared__ int wcnt[KM_MAXD][KM_THREADS / 32];
   __shared__ int s_first;
-  __shared__ double s_key[KM_SORT_MAX];
+  __shared__ unsigned long long s_key[KM_SORT_MAX];
   __shared__ int s_ord[KM_SORT_MAX];
   if (state->converged) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int DS = D + 1;  // key row stride: consecutive rows start in different banks
+  int32_t* as = a;
+  int32_t* mm = mem;
+  int32_t* ps = pos;
+  unsigned long long* dk = dkey;
+  if (staged) {
+    dk = reinterpret_cast<unsigned long long*>(km_dyn);
+    as = reinterpret_cast<int32_t*>(dk + (size_t)N * DS);
+    mm = as + N;
+    ps = as + 2 * (size_t)N;
+  }
   if (tid == 0) {
     s_first = (state->steps == 0);
     off[0] = 0;
@@ -137,11 +202,11 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
     int P = 1;
     while (P < N) P <<= 1;
     for (int i = tid; i < P; i += KM_THREADS) {
-      double rk = -1.0;  // padding sorts last
+      unsigned long long rk = 0ull;  // padding sorts last
       if (i < N) {
-        double b1 = INFINITY, b2 = INFINITY;
+        unsigned long long b1 = ~0ull, b2 = ~0ull;
         for (int d = 0; d < D; ++d) {
-          const double c = cost[(size_t)i * D + d];
+          const unsigned long long c = okey(cost[(size_t)i * D + d]);
           if (c < b1) {
             b2 = b1;
             b1 = c;
@@ -149,7 +214,7 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
             b2 = c;
           }
         }
-        rk = D > 1 ? b2 - b1 : 0.0;
+        rk = okey(D > 1 ? okey_value(b2) - okey_value(b1) : 0.0);
       }
       s_key[i] = rk;
       s_ord[i] = i;
@@ -161,7 +226,7 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
         for (int i = tid; i < P; i += KM_THREADS) {
           const int m = i ^ j;
           if (m > i) {
-            const double ki = s_key[i], km = s_key[m];
+            const unsigned long long ki = s_key[i], km = s_key[m];
             const int oi = s_ord[i], om = s_ord[m];
             const bool i_first = ki > km || (ki == km && oi < om);
             if (((i & k) == 0) != i_first) {
@@ -176,51 +241,63 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
       }
   }
   if (first) {
-    if (tid == 0) {
-      int cnt[KM_MAXD];
-      for (int d = 0; d < D; ++d) cnt[d] = 0;
+    if (warp == 0) {
+      // greedy nearest-with-room, one point at a time; lane d owns cluster d's
+      // fill, and a warp minimum over the lanes with room (ties: lower d) picks
+      const int capd = lane < D ? off[lane + 1] - off[lane] : 0;
+      int cnt = 0;
+      int i = sorted ? s_ord[0] : 0;
+      double c = lane < D ? cost[(size_t)i * D + lane] : 0.0;
       for (int r = 0; r < N; ++r) {
-        const int i = sorted ? s_ord[r] : r;
-        int best = -1;
-        double bc = 0.0;
-        for (int d = 0; d < D; ++d) {
-          if (cnt[d] >= off[d + 1] - off[d]) continue;
-          const double c = cost[(size_t)i * D + d];
-          if (best < 0 || c < bc) {
-            best = d;
-            bc = c;
-          }
-        }
-        a[i] = best;
-        cnt[best] += 1;
+        const int inext = r + 1 < N ? (sorted ? s_ord[r + 1] : r + 1) : i;
+        const double cnext = lane < D ? cost[(size_t)inext * D + lane] : 0.0;  // next row in flight
+        unsigned long long key = lane < D && cnt < capd ? okey(c) : ~0ull;
+        int d = lane;
+        warp_min_key(key, d);
+        if (lane == d) ++cnt;
+        if (lane == 0) as[i] = d;
+        i = inext;
+        c = cnext;
       }
     }
   } else {
-    for (int i = tid; i < N; i += KM_THREADS) a[i] = prev[i];
+    for (int i = tid; i < N; i += KM_THREADS) as[i] = prev[i];
   }
   __syncthreads();
   // member lists (slot order within a cluster does not matter)
   for (int i = tid; i < N; i += KM_THREADS) {
-    const int u = a[i];
+    const int u = as[i];
     const int slot = off[u] + atomicAdd(&fill[u], 1);
-    mem[slot] = i;
-    pos[i] = slot;
+    mm[slot] = i;
+    ps[i] = slot;
   }
-  // 2. tolerance: a move must gain more than 1e-12 of the largest cost
-  double mx = 0.0;
-  for (int64_t q = tid; q < (int64_t)N * D; q += KM_THREADS) mx = fmax(mx, fabs(cost[q]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(FULL, mx, o));
+  // gain keys of every point, and the largest |cost| (bit patterns of
+  // non-negative doubles order as integers)
+  unsigned long long mx = 0ull;
+  for (int64_t q = tid; q < (int64_t)N * D; q += KM_THREADS) {
+    const int p = (int)(q / D), v = (int)(q - (int64_t)p * D);
+    const double c = cost[q];
+    dk[(size_t)p * DS + v] = okey(c - cost[(size_t)p * D + as[p]]);
+    const unsigned long long ab = (unsigned long long)__double_as_longlong(c) & 0x7FFFFFFFFFFFFFFFull;
+    mx = ab > mx ? ab : mx;
+  }
+  {
+    unsigned long long cm = ~mx;  // the maximum is the complement of the complements' minimum
+    int unused = 0;
+    warp_min_key(cm, unused);
+    mx = ~cm;
+  }
   if (lane == 0) red[warp] = mx;
   __syncthreads();
   if (warp == 0) {
-    mx = lane < KM_THREADS / 32 ? red[lane] : 0.0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(FULL, mx, o));
-    if (lane == 0) red[0] = mx;
+    unsigned long long cm = lane < KM_THREADS / 32 ? ~red[lane] : ~0ull;
+    int unused = 0;
+    warp_min_key(cm, unused);
+    if (lane == 0) red[0] = ~cm;
   }
   __syncthreads();
-  const double eps = 1e-12 * red[0] + 1e-300;
+  // 2. tolerance: a move must gain more than 1e-12 of the largest cost
+  const double eps = 1e-12 * __longlong_as_double((long long)red[0]) + 1e-300;
 
   // threads per edge (a power of two <= 32, so an edge's threads share a warp)
   const int npairs = D * D;
@@ -228,103 +305,132 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   while (tpp > 1 && tpp * npairs > KM_THREADS) tpp >>= 1;
 
   // 3. improve until no negative cycle is left
-  int done = 0;
+  int done = 0, ncancel = 0;
   for (int pass = 0; pass < max_pass; ++pass) {
     // edge minima: W[u][v] = min over members p of u of cost[p][v] - cost[p][u]
+    // (ties: the lower point)
     {
       const int q = tid / tpp, sub = tid % tpp;
       const int u = q / D, v = q - (q / D) * D;
-      double best = INFINITY;
+      unsigned long long best = ~0ull;
       int bp = INT_MAX;
       if (q < npairs && u != v) {
         for (int k = off[u] + sub; k < off[u + 1]; k += tpp) {
-          const int p = mem[k];
-          vmin(best, bp, cost[(size_t)p * D + v] - cost[(size_t)p * D + u], p);
+          const int p = mm[k];
+          const unsigned long long kk = dk[(size_t)p * DS + v];
+          if (kk < best || (kk == best && p < bp)) {
+            best = kk;
+            bp = p;
+          }
         }
       }
       for (int o = tpp >> 1; o > 0; o >>= 1) {
-        const double ob = __shfl_xor_sync(FULL, best, o);
+        const unsigned long long ob = __shfl_xor_sync(FULL, best, o);
         const int op = __shfl_xor_sync(FULL, bp, o);
-        vmin(best, bp, ob, op);
+        if (ob < best || (ob == best && op < bp)) {
+          best = ob;
+          bp = op;
+        }
       }
       if (q < npairs && sub == 0) {
-        wval[q] = best;
+        wval[q] = bp == INT_MAX ? INFINITY : okey_value(best);
         widx[q] = bp;
       }
+      if (tid < D) negmask[tid] = 0u;
     }
     __syncthreads();
-    // disjoint pairwise swaps first (negative 2-cycles), first fit in (u, v) order
+    // disjoint pairwise swaps first (negative 2-cycles), first fit in (u, v)
+    // order: the negative pairs of each row u are marked (bit v, v > u), then
+    // one thread takes, for u ascending, the lowest v that is still free
+    if (tid < npairs) {
+      const int u = tid / D, v = tid - (tid / D) * D;
+      if (v > u && wval[u * D + v] + wval[v * D + u] < -eps) atomicOr(&negmask[u], 1u << v);
+    }
+    __syncthreads();
     if (tid == 0) {
       unsigned used = 0u;
       int n = 0;
-      for (int u = 0; u < D; ++u)
-        for (int v = u + 1; v < D; ++v) {
-          if ((used >> u) & 1u || (used >> v) & 1u) continue;
-          if (wval[u * D + v] + wval[v * D + u] < -eps) {
-            used |= (1u << u) | (1u << v);
-            mv_pt[n] = widx[u * D + v], mv_from[n] = u, mv_to[n] = v, ++n;
-            mv_pt[n] = widx[v * D + u], mv_from[n] = v, mv_to[n] = u, ++n;
-          }
-        }
+      for (int u = 0; u < D; ++u) {
+        if ((used >> u) & 1u) continue;
+        const unsigned m = negmask[u] & ~used;
+        if (m == 0u) continue;
+        const int v = __ffs(m) - 1;
+        used |= (1u << u) | (1u << v);
+        mv_pt[n] = widx[u * D + v], mv_from[n] = u, mv_to[n] = v, ++n;
+        mv_pt[n] = widx[v * D + u], mv_from[n] = v, mv_to[n] = u, ++n;
+      }
       nmv = n;
+      if (n == 0) {
+        for (int x = 0; x < D; ++x) {
+          bf_dist[0][x] = 0.0;
+          s_pred[x] = -1;
+        }
+      }
     }
     __syncthreads();
-    if (nmv == 0 && warp == 0) {
+    if (nmv == 0) {
       // no swap left: Bellman-Ford from a virtual source (0-weight edges to
-      // every node) for a longer negative cycle; lane v owns node v, rounds
-      // are synchronous (old distances through shuffles all lanes execute)
-      double dist = 0.0;
-      int pred = -1;
+      // every node) for a longer negative cycle.  Synchronous rounds; warp v
+      // relaxes node v, lane u offering dist[u] + W[u][v]; a node takes the
+      // smallest offer (ties: the lower u) only if it beats its distance.
+      int cur = 0;
       for (int round = 0; round < 2 * (D + 1); ++round) {
-        double best = dist;
-        int from = pred;
-        for (int u = 0; u < D; ++u) {
-          const double du = __shfl_sync(FULL, dist, u);
-          if (lane < D && u != lane) {
-            const double cand = du + wval[u * D + lane];
-            if (cand < best) {
-              best = cand;
-              from = u;
+        int changed = 0;
+        if (warp < D) {
+          const int v = warp;
+          unsigned long long key = ~0ull;
+          int from = lane;
+          if (lane < D && lane != v) key = okey(bf_dist[cur][lane] + wval[lane * D + v]);
+          warp_min_key(key, from);
+          if (lane == 0) {
+            const double dv = bf_dist[cur][v];
+            if (key < okey(dv)) {
+              bf_dist[cur ^ 1][v] = okey_value(key);
+              s_pred[v] = from;
+              changed = 1;
+            } else {
+              bf_dist[cur ^ 1][v] = dv;
             }
           }
         }
-        const bool changed = best < dist;
-        dist = best;
-        pred = from;
-        if (!__any_sync(FULL, changed)) break;
-      }
-      if (lane < D) s_pred[lane] = pred;
-      __syncwarp();
-      // A cycle of the predecessor graph has negative weight.  A walk of D
-      // steps along predecessors that never reaches the source ends on one.
-      int x = lane;
-      bool alive = lane < D;
-      for (int st = 0; st < D && alive; ++st) {
-        const int nx = s_pred[x];
-        if (nx < 0) alive = false;
-        else x = nx;
-      }
-      const unsigned on = __ballot_sync(FULL, alive);
-      const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
-      if (lane == 0 && on) {
-        // walk the cycle backwards (edges pred[y] -> y)
-        int y = start, n = 0;
-        double w = 0.0;
-        bool ok = true;
-        do {
-          const int py = s_pred[y];
-          if (py < 0 || widx[py * D + y] >= N) {  // cannot happen on a cycle; checked anyway
-            ok = false;
-            break;
+        cur ^= 1;
+        changed = __syncthreads_or(changed);
+        if (warp == 0) {
+          // A cycle of the predecessor graph has negative weight (its sum is
+          // checked anyway): stop at the first round that closes one.  A walk
+          // of D steps along predecessors that never reaches the source ends
+          // on a cycle.
+          int x = lane;
+          bool alive = lane < D;
+          for (int st = 0; st < D && alive; ++st) {
+            const int nx = s_pred[x];
+            if (nx < 0) alive = false;
+            else x = nx;
           }
-          mv_pt[n] = widx[py * D + y], mv_from[n] = py, mv_to[n] = y, ++n;
-          w += wval[py * D + y];
-          y = py;
-        } while (y != start && n < D);
-        nmv = (ok && y == start && w < -eps) ? n : 0;
+          const unsigned on = __ballot_sync(FULL, alive);
+          const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
+          if (lane == 0 && on) {
+            // walk the cycle backwards (edges pred[y] -> y)
+            int y = start, n = 0;
+            double w = 0.0;
+            bool ok = true;
+            do {
+              const int py = s_pred[y];
+              if (py < 0 || widx[py * D + y] >= N) {  // cannot happen on a cycle; checked anyway
+                ok = false;
+                break;
+              }
+              mv_pt[n] = widx[py * D + y], mv_from[n] = py, mv_to[n] = y, ++n;
+              w += wval[py * D + y];
+              y = py;
+            } while (y != start && n < D);
+            nmv = (ok && y == start && w < -eps) ? n : 0;
+          }
+        }
+        __syncthreads();
+        if (nmv != 0 || !changed) break;
       }
     }
-    __syncthreads();
     if (nmv == 0) {
       done = 1;
       break;
@@ -333,24 +439,61 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
       // every cluster on the moves loses one point and gains one: the incoming
       // point takes the outgoing point's slot (points are distinct: each move
       // leaves a different cluster)
-      for (int m = 0; m < nmv; ++m) freed[mv_from[m]] = pos[mv_pt[m]];
+      for (int m = 0; m < nmv; ++m) freed[mv_from[m]] = ps[mv_pt[m]];
       for (int m = 0; m < nmv; ++m) {
         const int pt = mv_pt[m], slot = freed[mv_to[m]];
-        a[pt] = mv_to[m];
-        mem[slot] = pt;
-        pos[pt] = slot;
+        as[pt] = mv_to[m];
+        mm[slot] = pt;
+        ps[pt] = slot;
       }
-      state->cancelled += 1;
+      ++ncancel;
+    }
+    __syncthreads();
+    // the moved points' gain keys, against their new clusters
+    for (int t = tid; t < nmv * D; t += KM_THREADS) {
+      const int p = mv_pt[t / D], v = t - (t / D) * D;
+      dk[(size_t)p * DS + v] = okey(cost[(size_t)p * D + v] - cost[(size_t)p * D + as[p]]);
     }
     __syncthreads();
   }
   // 4. convergence and bookkeeping
   int changed = 0;
   if (!first)
-    for (int i = tid; i < N; i += KM_THREADS) changed |= (a[i] != prev[i]);
+    for (int i = tid; i < N; i += KM_THREADS) changed |= (as[i] != prev[i]);
   changed = __syncthreads_or(changed);
-  for (int i = tid; i < N; i += KM_THREADS) prev[i] = a[i];
+  // 5. each cluster's members in index order, for the means: mem[off_u + r]
+  //    is the r-th lowest point of cluster u (a stable counting sort: warp
+  //    ballots per cluster, then a scan over the warps)
+  if (tid < D) fill[tid] = 0;
+  for (int base = 0; base < N; base += KM_THREADS) {
+    const int i = base + tid;
+    const int ai = i < N ? as[i] : -1;
+    int rank = 0;
+    for (int d = 0; d < D; ++d) {
+      const unsigned b = __ballot_sync(FULL, ai == d);
+      if (lane == 0) wcnt[d][warp] = __popc(b);
+      if (ai == d) rank = __popc(b & ((1u << lane) - 1u));
+    }
+    __syncthreads();
+    if (tid < D) {
+      int run = fill[tid];
+      for (int w = 0; w < KM_THREADS / 32; ++w) {
+        const int c = wcnt[tid][w];
+        wcnt[tid][w] = run;
+        run += c;
+      }
+      fill[tid] = run;
+    }
+    __syncthreads();
+    if (ai >= 0) mem[off[ai] + wcnt[ai][warp] + rank] = i;
+    __syncthreads();
+  }
+  for (int i = tid; i < N; i += KM_THREADS) {
+    prev[i] = as[i];
+    if (staged) a[i] = as[i];
+  }
   if (tid == 0) {
+    state->cancelled += ncancel;
     if (!first && !changed) state->converged = 1;
     if (!done) {
       state->capped = 1;
@@ -360,21 +503,30 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   }
 }
 
-// cent[d][j] = mean of sig[p][j] over the points p of cluster d.
+// cent[d][j] = mean of sig[p][j] over the points p of cluster d, summed in
+// index order: `ord` holds each cluster's members in index order at the
+// cluster's offset (written by the assignment step), eight loads in flight.
 __global__ void __launch_bounds__(256) km_update_kernel(const float* __restrict__ sig, int32_t N, int32_t dim,
-                                                        int32_t D, const int32_t* __restrict__ a,
+                                                        int32_t D, const int32_t* __restrict__ ord,
                                                         double* __restrict__ cent, const KmState* state) {
   if (state->converged) return;
   const int d = blockIdx.y;
   const int j = blockIdx.x * 256 + threadIdx.x;
+  if (j >= dim) return;
+  const int base = N / D, rem = N % D;
+  const int o = d * base + min(d, rem), n = base + (d < rem ? 1 : 0);
+  const int32_t* m = ord + o;
   double sum = 0.0;
-  int n = 0;
-  for (int p = 0; p < N; ++p) {
-    if (a[p] != d) continue;  // uniform across the block
-    if (j < dim) sum += (double)sig[(size_t)p * dim + j];
-    ++n;
+  int k = 0;
+  for (; k + 8 <= n; k += 8) {
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = sig[(size_t)m[k + q] * dim + j];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sum += (double)v[q];
   }
-  if (j < dim && n > 0) cent[(size_t)d * dim + j] = sum / n;
+  for (; k < n; ++k) sum += (double)sig[(size_t)m[k] * dim + j];
+  if (n > 0) cent[(size_t)d * dim + j] = sum / n;
 }
 
 __global__ void __launch_bounds__(KM_THREADS) km_finalize_kernel(const double* __restrict__ cost,
@@ -420,16 +572,28 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
   int32_t* prev = reinterpret_cast<int32_t*>(w + l.prev);
   int32_t* mem = reinterpret_cast<int32_t*>(w + l.mem);
   int32_t* pos = reinterpret_cast<int32_t*>(w + l.pos);
+  unsigned long long* dkey = reinterpret_cast<unsigned long long*>(w + l.dkey);
   uint32_t* status = reinterpret_cast<uint32_t*>(w);
   if (cudaMemsetAsync(state, 0, sizeof(KmState), st) != cudaSuccess) return MOER_ECUDA;
   const int64_t nc = (int64_t)D * dim;
   km_init_kernel<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(init, cent, nc);
   const int32_t max_cancel = 16 * N + 1024;
   const dim3 ug((unsigned)((dim + 255) / 256), (unsigned)D);
+  // shared-memory staging of the assignment step when it fits beside the
+  // kernel's static arrays (1,000 points x 16 clusters: 148 KB)
+  static std::atomic<unsigned long long> assign_set{0};
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, km_assign_kernel) != cudaSuccess) return MOER_ECUDA;
+  const int64_t dyn_max = 232448 - (int64_t)fa.sharedSizeBytes;
+  const int64_t dyn = (int64_t)N * (D + 1) * (int64_t)sizeof(unsigned long long) +
+                      3 * (int64_t)N * (int64_t)sizeof(int32_t);
+  const bool staged = dyn <= dyn_max;
+  if (staged && smem_optin(km_assign_kernel, (int)dyn_max, assign_set) != cudaSuccess) return MOER_ECUDA;
   for (int it = 0; it < max_iter; ++it) {
     km_cost_kernel<<<(unsigned)N, 256, 0, st>>>(sig, dim, D, cent, cost, state, 0);
-    km_assign_kernel<<<1, KM_THREADS, 0, st>>>(cost, N, D, assign, prev, mem, pos, state, max_cancel, status);
-    km_update_kernel<<<ug, 256, 0, st>>>(sig, N, dim, D, assign, cent, state);
+    km_assign_kernel<<<1, KM_THREADS, staged ? (size_t)dyn : 0, st>>>(cost, N, D, assign, prev, mem, pos, dkey,
+                                                                       state, max_cancel, staged ? 1 : 0, status);
+    km_update_kernel<<<ug, 256, 0, st>>>(sig, N, dim, D, mem, cent, state);
   }
   km_cost_kernel<<<(unsigned)N, 256, 0, st>>>(sig, dim, D, cent, cost, state, 1);
   km_finalize_kernel<<<1, KM_THREADS, 0, st>>>(cost, cent, assign, N, dim, D, centroids, info, objective, state);
