@@ -32,16 +32,18 @@
 //     not an option either: the co-activation spectra of real layers are
 //     nearly degenerate just below the leading eigenvalues, where it needs
 //     10^4 - 10^5 steps.
-//   * spec_group_kernel, one CTA per (grid point, layer): the size-bounded
-//     assignment is a transportation problem with lower and upper bounds; one
-//     warp keeps a feasible assignment and cancels negative cycles of the
-//     residual graph collapsed onto the G groups plus one slack node t (t -> u
-//     when u may shrink, u -> t when u may grow, a large negative u -> t while u
-//     is below its lower bound), Bellman-Ford with a lane per node.
+//   * spec_group_kernel, one CTA per (grid point, layer), four per SM: the
+//     size-bounded assignment is a transportation problem with lower and upper
+//     bounds; the CTA keeps a feasible assignment and cancels negative cycles of
+//     the residual graph collapsed onto the G groups plus one slack node t
+//     (t -> u when u may shrink, u -> t when u may grow, a large negative u -> t
+//     while u is below its lower bound).  Scans and minima compare integer keys
+//     of the fp64 gains; Bellman-Ford relaxes the nodes a warp each.
 //   * spec_knee_kernel, one warp per layer: the knee and the chosen groups.
 #include <climits>
 
 #include "common.cuh"
+#include "keys.cuh"
 
 namespace moer {
 
@@ -321,31 +323,36 @@ size_t spec_embed_smem(int E, int G);
 
 // Size-bounded assignment by the whole CTA: a = previous assignment or, at the
 // first step, greedy nearest-with-room in regret order, then negative cycles of the residual
-// graph on the G groups plus the slack node t = G are cancelled.  The edge
-// minima (the cheapest member of u to move to v, ties to the lower point)
-// take all threads, a few per edge.  Disjoint negative 2-cycles between
-// groups (swaps) go first, several per pass; when none is left, warp 0 runs
-// Bellman-Ford with a lane per node and extracts a longer cycle (through the
+// graph on the G groups plus the slack node t = G are cancelled.  Each expert
+// keeps a row of its gains cost[p][v] - cost[p][a(p)] as order-preserving
+// integer keys (rewritten only for the experts that move), so the edge minima
+// (the cheapest member of u to move to v, ties to the lower point), taken by
+// all threads a few per edge, compare integers.  Disjoint negative 2-cycles
+// between groups (swaps) go first, several per pass; when none is left,
+// Bellman-Ford runs with a warp per node in synchronous rounds and stops at the
+// first round whose predecessor graph closes a negative cycle (through the
 // slack node when sizes must change).  Thread 0 moves the points.
 __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int* a, const int* prev, bool first,
                           double* W, int* widx, int* sz, int* s_pred, int* mv_pt, int* mv_to, int* nmv,
-                          uint32_t* status) {
-  __shared__ double sp_red[SP_GROUP_THREADS / 32];
-  __shared__ double s_key[SP_MAXE];
+                          unsigned long long* dk, uint32_t* status) {
+  __shared__ unsigned long long sp_red[SP_GROUP_THREADS / 32];
+  __shared__ unsigned long long s_key[SP_MAXE];
   __shared__ int s_ord[SP_MAXE];
+  __shared__ double bf_dist[2][32];
+  __shared__ unsigned negmask[32];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  const int n = G + 1, t = G, ld = G + 1;
+  const int n = G + 1, t = G, ld = G + 1, DS = G + 1;
   if (first) {
     // greedy nearest-with-room in regret order: the experts whose nearest centroid
     // beats their second nearest by most go first (larger regret, then lower id)
     int P = 1;
     while (P < E) P <<= 1;
     for (int i = tid; i < P; i += nt) {
-      double rk = -1.0;  // padding sorts last
+      unsigned long long rk = 0ull;  // padding sorts last
       if (i < E) {
-        double b1 = INFINITY, b2 = INFINITY;
+        unsigned long long b1 = ~0ull, b2 = ~0ull;
         for (int g = 0; g < G; ++g) {
-          const double c = cost[i * G + g];
+          const unsigned long long c = okey(cost[i * G + g]);
           if (c < b1) {
             b2 = b1;
             b1 = c;
@@ -353,7 +360,7 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
             b2 = c;
           }
         }
-        rk = b2 - b1;
+        rk = okey(okey_value(b2) - okey_value(b1));
       }
       s_key[i] = rk;
       s_ord[i] = i;
@@ -364,7 +371,7 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
         for (int i = tid; i < P; i += nt) {
           const int m = i ^ j;
           if (m > i) {
-            const double ki = s_key[i], km = s_key[m];
+            const unsigned long long ki = s_key[i], km = s_key[m];
             const int oi = s_ord[i], om = s_ord[m];
             const bool i_first = ki > km || (ki == km && oi < om);
             if (((i & k) == 0) != i_first) {
@@ -377,56 +384,73 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
         }
         __syncthreads();
       }
-    if (tid == 0) {
-      for (int g = 0; g < G; ++g) sz[g] = 0;
+    if (warp == 0) {
+      // lane g owns group g's size; a keyed warp minimum over the lanes with
+      // room picks the nearest (ties: the lower group)
+      int cnt = 0;
       for (int r = 0; r < E; ++r) {
         const int e = s_ord[r];
-        int best = -1;
-        for (int g = 0; g < G; ++g) {
-          if (sz[g] >= hi) continue;
-          if (best < 0 || cost[e * G + g] < cost[e * G + best]) best = g;
-        }
-        a[e] = best;
-        sz[best] += 1;
+        unsigned long long key = lane < G && cnt < hi ? okey(cost[e * G + lane]) : ~0ull;
+        int g = lane;
+        warp_min_key(key, g);
+        if (lane == g) ++cnt;
+        if (lane == 0) a[e] = g;
       }
     }
   } else {
     for (int e = tid; e < E; e += nt) a[e] = prev[e];
   }
-  double mx = 0.0;
-  for (int q = tid; q < E * G; q += nt) mx = fmax(mx, fabs(cost[q]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(FULL, mx, o));
+  __syncthreads();
+  // gain keys of every expert, and the largest |cost| (bit patterns of
+  // non-negative doubles order as integers)
+  unsigned long long mx = 0ull;
+  for (int q = tid; q < E * G; q += nt) {
+    const int p = q / G, v = q - p * G;
+    const double c = cost[q];
+    dk[p * DS + v] = okey(c - cost[p * G + a[p]]);
+    const unsigned long long ab = (unsigned long long)__double_as_longlong(c) & 0x7FFFFFFFFFFFFFFFull;
+    mx = ab > mx ? ab : mx;
+  }
+  {
+    unsigned long long cm = ~mx;  // the maximum is the complement of the complements' minimum
+    int unused = 0;
+    warp_min_key(cm, unused);
+    mx = ~cm;
+  }
   if (lane == 0) sp_red[warp] = mx;
   __syncthreads();
-  mx = 0.0;
-  for (int w = 0; w < nt / 32; ++w) mx = fmax(mx, sp_red[w]);
-  const double eps = 1e-12 * mx + 1e-300;
-  const double big = 1.0 + 4.0 * (mx + 1.0) * E;  // any lower-bound repair beats any cost change
+  mx = 0ull;
+  for (int w = 0; w < nt / 32; ++w) mx = sp_red[w] > mx ? sp_red[w] : mx;
+  const double mxd = __longlong_as_double((long long)mx);
+  const double eps = 1e-12 * mxd + 1e-300;
+  const double big = 1.0 + 4.0 * (mxd + 1.0) * E;  // any lower-bound repair beats any cost change
   int tpe = 32;  // threads per edge: a power of two, so an edge's threads share a warp
   while (tpe > 1 && tpe * G * G > nt) tpe >>= 1;
   const int max_pass = 16 * E + 1024;
   int done = 0;
   for (int pass = 0; pass < max_pass; ++pass) {
-    for (int g = tid; g < G; g += nt) sz[g] = 0;
+    for (int g = tid; g < G; g += nt) {
+      sz[g] = 0;
+      negmask[g] = 0u;
+    }
     __syncthreads();
     for (int e = tid; e < E; e += nt) atomicAdd(&sz[a[e]], 1);
     for (int q0 = 0; q0 < G * G; q0 += nt / tpe) {  // edge u -> v: the cheapest member of u to move
       const int q = q0 + tid / tpe, sub = tid % tpe;
       const int u = q / G, v = q - u * G;
-      double best = INFINITY;
+      unsigned long long best = ~0ull;
       int bp = INT_MAX;
       if (q < G * G && u != v)
         for (int p = sub; p < E; p += tpe) {
           if (a[p] != u) continue;
-          const double val = cost[p * G + v] - cost[p * G + u];
-          if (val < best || (val == best && p < bp)) {
-            best = val;
+          const unsigned long long kk = dk[p * DS + v];
+          if (kk < best || (kk == best && p < bp)) {
+            best = kk;
             bp = p;
           }
         }
       for (int o = tpe >> 1; o > 0; o >>= 1) {
-        const double ob = __shfl_xor_sync(FULL, best, o);
+        const unsigned long long ob = __shfl_xor_sync(FULL, best, o);
         const int op = __shfl_xor_sync(FULL, bp, o);
         if (ob < best || (ob == best && op < bp)) {
           best = ob;
@@ -434,69 +458,85 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
         }
       }
       if (q < G * G && sub == 0) {
-        W[u * ld + v] = best;
+        W[u * ld + v] = bp == INT_MAX ? INFINITY : okey_value(best);
         widx[q] = bp;
       }
     }
     __syncthreads();
-    if (warp == 0) {
-      for (int u = lane; u < G; u += 32) {
-        W[t * ld + u] = sz[u] > lo ? 0.0 : INFINITY;                        // u may shrink
-        W[u * ld + t] = sz[u] < lo ? -big : (sz[u] < hi ? 0.0 : INFINITY);  // u may (must) grow
+    for (int u = tid; u < G; u += nt) {
+      W[t * ld + u] = sz[u] > lo ? 0.0 : INFINITY;                        // u may shrink
+      W[u * ld + t] = sz[u] < lo ? -big : (sz[u] < hi ? 0.0 : INFINITY);  // u may (must) grow
+    }
+    if (tid == 0) W[t * ld + t] = INFINITY;
+    // disjoint negative 2-cycles between groups first, first fit in (u, v)
+    // order: each swaps two points and leaves the sizes as they are; the
+    // negative pairs of each row u are marked (bit v, v > u), then one thread
+    // takes, for u ascending, the lowest v that is still free
+    for (int q = tid; q < G * G; q += nt) {
+      const int u = q / G, v = q - u * G;
+      if (v > u && W[u * ld + v] + W[v * ld + u] < -eps) atomicOr(&negmask[u], 1u << v);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned used = 0u;
+      int m = 0;
+      for (int u = 0; u < G; ++u) {
+        if ((used >> u) & 1u) continue;
+        const unsigned msk = negmask[u] & ~used;
+        if (msk == 0u) continue;
+        const int v = __ffs(msk) - 1;
+        used |= (1u << u) | (1u << v);
+        mv_pt[m] = widx[u * G + v], mv_to[m] = v, ++m;
+        mv_pt[m] = widx[v * G + u], mv_to[m] = u, ++m;
       }
-      if (lane == 0) {
-        W[t * ld + t] = INFINITY;
-        // disjoint negative 2-cycles between groups first, first fit in (u, v)
-        // order: each swaps two points and leaves the sizes as they are
-        unsigned used = 0u;
-        int m = 0;
-        for (int u = 0; u < G; ++u)
-          for (int v = u + 1; v < G; ++v) {
-            if (((used >> u) | (used >> v)) & 1u) continue;
-            if (W[u * ld + v] + W[v * ld + u] < -eps) {
-              used |= (1u << u) | (1u << v);
-              mv_pt[m] = widx[u * G + v], mv_to[m] = v, ++m;
-              mv_pt[m] = widx[v * G + u], mv_to[m] = u, ++m;
+      *nmv = m;
+      if (m == 0)
+        for (int x = 0; x < n; ++x) {
+          bf_dist[0][x] = 0.0;
+          s_pred[x] = -1;
+        }
+    }
+    __syncthreads();
+    if (*nmv == 0) {
+      // Bellman-Ford from a virtual source (0-weight edges to every node):
+      // warp w relaxes nodes w, w + 8, ..., lane u offering dist[u] + W[u][v];
+      // a node takes the smallest offer (ties: the lower u) only if it beats
+      // its distance.  After each round warp 0 walks the predecessor graph: a
+      // cycle there has negative weight (its sum is checked anyway).
+      int cur = 0;
+      for (int round = 0; round < 2 * (n + 1); ++round) {
+        int changed = 0;
+        for (int v = warp; v < n; v += nt / 32) {
+          unsigned long long key = ~0ull;
+          int from = lane;
+          if (lane < n && lane != v) key = okey(bf_dist[cur][lane] + W[lane * ld + v]);
+          warp_min_key(key, from);
+          if (lane == 0) {
+            const double dv = bf_dist[cur][v];
+            if (key < okey(dv)) {
+              bf_dist[cur ^ 1][v] = okey_value(key);
+              s_pred[v] = from;
+              changed = 1;
+            } else {
+              bf_dist[cur ^ 1][v] = dv;
             }
           }
-        *nmv = m;
-      }
-      __syncwarp();
-      if (*nmv == 0) {
-        double dist = 0.0;
-        int pred = -1;
-        for (int round = 0; round < 2 * (n + 1); ++round) {
-          double best = dist;
-          int from = pred;
-          for (int u = 0; u < n; ++u) {
-            const double du = __shfl_sync(FULL, dist, u);
-            if (lane < n && u != lane) {
-              const double w = W[u * ld + lane];
-              if (w < INFINITY && du + w < best) {
-                best = du + w;
-                from = u;
-              }
-            }
+        }
+        cur ^= 1;
+        changed = __syncthreads_or(changed);
+        if (warp == 0) {
+          // a walk of n steps along predecessors that never reaches the source
+          // ends on a cycle
+          int x = lane;
+          bool alive = lane < n;
+          for (int st = 0; st < n && alive; ++st) {
+            const int nx = s_pred[x];
+            if (nx < 0) alive = false;
+            else x = nx;
           }
-          const bool changed = best < dist;
-          dist = best;
-          pred = from;
-          if (!__any_sync(FULL, changed)) break;
-        }
-        if (lane < n) s_pred[lane] = pred;
-        __syncwarp();
-        int x = lane;
-        bool alive = lane < n;
-        for (int st = 0; st < n && alive; ++st) {
-          const int nx = s_pred[x];
-          if (nx < 0) alive = false;
-          else x = nx;
-        }
-        const unsigned on = __ballot_sync(FULL, alive);
-        const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
-        if (lane == 0) {
-          *nmv = 0;
-          if (on) {
+          const unsigned on = __ballot_sync(FULL, alive);
+          const int start = __shfl_sync(FULL, x, on ? (__ffs(on) - 1) : 0);
+          if (lane == 0 && on) {
             int y = start, k = 0, m = 0;
             double w = 0.0;
             bool ok = true;
@@ -522,9 +562,10 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
             if (ok && y == start && w < -eps) *nmv = m;
           }
         }
+        __syncthreads();
+        if (*nmv != 0 || !changed) break;
       }
     }
-    __syncthreads();
     if (*nmv == 0) {
       done = 1;
       break;
@@ -532,12 +573,17 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
     if (tid == 0)
       for (int m = 0; m < *nmv; ++m) a[mv_pt[m]] = mv_to[m];
     __syncthreads();
+    // the moved experts' gain keys, against their new groups
+    for (int q = tid; q < *nmv * G; q += nt) {
+      const int p = mv_pt[q / G], v = q - (q / G) * G;
+      dk[p * DS + v] = okey(cost[p * G + v] - cost[p * G + a[p]]);
+    }
   }
   if (tid == 0 && !done) atomicOr(status, WS_BIT_ETIMEOUT);
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(SP_GROUP_THREADS, 1)
+__global__ void __launch_bounds__(SP_GROUP_THREADS, 4)
     spec_group_kernel(const int32_t* __restrict__ affinity, int E, int G, const double* __restrict__ Uo,
                       const double* __restrict__ deg, int32_t* __restrict__ groups, double* __restrict__ ucurve,
                       double* __restrict__ scurve, uint32_t* status) {
@@ -547,7 +593,8 @@ __global__ void __launch_bounds__(SP_GROUP_THREADS, 1)
   double* cost = C + G * G;                  // [E][G]
   double* mind = cost + E * G;               // [E]
   double* W = mind + E;                      // [G+1][G+1]
-  int* a = reinterpret_cast<int*>(W + (G + 1) * (G + 1));  // [E]
+  unsigned long long* dk = reinterpret_cast<unsigned long long*>(W + (G + 1) * (G + 1));  // [E][G+1]
+  int* a = reinterpret_cast<int*>(dk + E * (G + 1));  // [E]
   int* prev = a + E;                         // [E]
   int* widx = prev + E;                      // [G][G]
   int* sz = widx + G * G;                    // [G]
@@ -605,7 +652,7 @@ __global__ void __launch_bounds__(SP_GROUP_THREADS, 1)
       cost[q] = dd;
     }
     __syncthreads();
-    sp_assign(cost, E, G, lo, hi, a, prev, first, W, widx, sz, s_pred, mv_pt, mv_to, &s_nmv, status);
+    sp_assign(cost, E, G, lo, hi, a, prev, first, W, widx, sz, s_pred, mv_pt, mv_to, &s_nmv, dk, status);
     __syncthreads();
     int changed = 0;
     if (!first)
@@ -704,7 +751,8 @@ __global__ void __launch_bounds__(32) spec_knee_kernel(const int32_t* __restrict
 }
 
 size_t spec_group_smem(int E, int G) {
-  return ((size_t)E * G * 2 + (size_t)G * G + E + (size_t)(G + 1) * (G + 1)) * sizeof(double) +
+  return ((size_t)E * G * 2 + (size_t)G * G + E + (size_t)(G + 1) * (G + 1) + (size_t)E * (G + 1)) *
+             sizeof(double) +
          ((size_t)E * 2 + (size_t)G * G + G + 96) * sizeof(int);
 }
 
