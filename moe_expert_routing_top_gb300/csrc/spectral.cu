@@ -17,7 +17,8 @@
 //     expert from the seeds so far; each step assigns at the least total
 //     squared distance under the bounds and moves the centroids to the means;
 //   * U(r) = affinity inside groups / all affinity off the diagonal; S(r) =
-//     std of the group sizes / (E/G); the knee of U over r (scaled to [0, 1],
+//     std of the group sizes / (E/G), evaluated as sqrt(G sum size^2 - E^2) / E
+//     from an exact integer; the knee of U over r (scaled to [0, 1],
 //     the point farthest above the chord from r = 0 to r = 1) picks the groups.
 //
 // Design (GB300):
@@ -705,13 +706,12 @@ __global__ void __launch_bounds__(SP_GROUP_THREADS, 4)
     ucurve[(size_t)l * SP_NGRID + j] = T_ > 0 ? (double)S_ / (double)T_ : 0.0;
     for (int g = 0; g < G; ++g) sz[g] = 0;
     for (int e = 0; e < E; ++e) sz[a[e]] += 1;
-    const double mean = (double)E / (double)G;
-    double acc = 0.0;
-    for (int g = 0; g < G; ++g) {
-      const double dlt = (double)sz[g] - mean;
-      acc = __dadd_rn(acc, __dmul_rn(dlt, dlt));
-    }
-    scurve[(size_t)l * SP_NGRID + j] = sqrt(acc / (double)G) / mean;
+    // S = sqrt(mean_g (size_g - E/G)^2) / (E/G) = sqrt(G sum_g size_g^2 - E^2) / E
+    // (the sizes sum to E): an exact integer under the root
+    long long s2 = 0;
+    for (int g = 0; g < G; ++g) s2 += (long long)sz[g] * sz[g];
+    const long long num = (long long)G * s2 - (long long)E * E;
+    scurve[(size_t)l * SP_NGRID + j] = __dsqrt_rn((double)num) / (double)E;
   }
 }
 

@@ -107,10 +107,14 @@ def utilisation(A, groups) -> float:
 
 
 def size_deviation(groups, G) -> float:
+    """S(r) = sqrt(mean_g (size_g - E/G)^2) / (E/G).  Since sum_g size_g = E, the mean of
+    the squared deviations is (G * sum_g size_g^2 - E^2) / G^2, so S = sqrt(G * sum_g
+    size_g^2 - E^2) / E: an exact integer under the root, rounded only by the root and the
+    division (a floating-point sum of the squared deviations would depend on its order)."""
     E = len(groups)
-    mean = E / G
-    sizes = np.bincount(groups, minlength=G).astype(np.float64)
-    return float(np.sqrt(((sizes - mean) ** 2).sum() / G) / mean)
+    sizes = np.bincount(groups, minlength=G).astype(np.int64)
+    num = int(G) * int((sizes * sizes).sum()) - E * E
+    return float(np.sqrt(float(num)) / float(E))
 
 
 def knee(Uc) -> int:

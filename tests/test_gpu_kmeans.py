@@ -5,7 +5,8 @@ balanced assignment, so the assignments and the number of steps must be identica
 fp32 centroids must equal the oracle's fp64 means to fp32 rounding, and the objective
 must agree to 1e-9 relative.  Cases: the pages' calibration scale (1,000 signatures of
 12 x 128 dims into 16 decoders, and 1,003 so the sizes differ by one), one cluster, one
-point per cluster, 32 clusters, and a first step that starts far from balance.
+point per cluster, 32 clusters, a first step that starts far from balance, and a problem
+too large for the assignment step's shared-memory staging.
 """
 import numpy as np
 import pytest
@@ -90,6 +91,16 @@ def test_far_from_balance_start(env):
     S = rs.standard_normal((300, 16)).astype(np.float32)
     C0 = (np.full((8, 16), 3.0) + 0.01 * rs.standard_normal((8, 16))).astype(np.float32)
     _check(env, S, C0, 60)
+
+
+def test_large_problem_in_global_memory(env):
+    # 2,100 points into 24 clusters: the assignment step's gain rows and member lists
+    # (445 KB) do not fit in shared memory and live in the workspace, and the first
+    # step's greedy start takes the points in index order (more than 2,048 points)
+    S, _ = gen.calib_signatures(2100, 32, ndom=30, seed=12)
+    C0 = S[gen.kmeans_seed_rows(2100, 24, seed=13)]
+    info = _check(env, S, C0, 8)
+    assert info[0] == 8
 
 
 def test_max_iter_stops_early(env):

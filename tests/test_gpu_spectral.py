@@ -66,8 +66,7 @@ def _check_properties(A, G, g, k, uc, sc):
         tot = Al.sum()
         same = Al[g[l][:, None] == g[l][None, :]].sum()
         assert uc[l, k[l]] == (float(same) / float(tot) if tot else 0.0)
-        mean = E / G
-        assert sc[l, k[l]] == np.sqrt(((sz - mean) ** 2).sum() / G) / mean
+        assert sc[l, k[l]] == gp.size_deviation(g[l], G)
         # the knee read off the returned curve
         y = uc[l] - uc[l].min()
         rng = uc[l].max() - uc[l].min()
@@ -78,13 +77,19 @@ def _check_properties(A, G, g, k, uc, sc):
         assert kk == k[l], l
 
 
-@pytest.mark.parametrize("E,G", [(128, 8), (64, 4)])
+@pytest.mark.parametrize("E,G", [(128, 8), (64, 4), (128, 16), (128, 31)])
 def test_planted_partitions(env, E, G):
+    # G = 16 and 31: Bellman-Ford over 17 and 32 nodes (several per warp), swap
+    # masks up to bit 30, and the largest shared-memory layout
     profiles = {8: [[24, 20, 16, 16, 16, 12, 12, 12], [16] * 8, [30, 18, 16, 14, 14, 12, 12, 12]],
-                4: [[24, 16, 12, 12], [16] * 4, [20, 16, 16, 12]]}[G]
+                4: [[24, 16, 12, 12], [16] * 4, [20, 16, 16, 12]],
+                16: [[10, 10, 9, 9, 8, 8, 8, 8, 8, 8, 7, 7, 7, 7, 7, 7], [8] * 16],
+                31: [[5] * 4 + [4] * 27, [4] * 30 + [8]]}[G]
+    assert all(sum(p) == E for p in profiles)
     layers, labs = [], []
     for i, sizes in enumerate(profiles):
-        A, lab = _planted(sizes, inside=30 + 10 * i, outside=1, noise=3, seed=10 * G + i)
+        A, lab = _planted(sizes, inside=30 + 10 * i, outside=1, noise=3,
+                          seed=(10 if G <= 8 else 100) * G + i)
         layers.append(A)
         labs.append(lab)
     A = np.stack(layers)

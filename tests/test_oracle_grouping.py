@@ -100,6 +100,26 @@ def test_utilisation_and_deviation_by_hand():
     assert gp.utilisation(np.zeros((3, 3)), np.array([0, 1, 2])) == 0.0
 
 
+def test_size_deviation_against_the_definition_in_high_precision():
+    # S = sqrt(mean_g (size_g - E/G)^2) / (E/G) evaluated with 50 significant digits
+    # from the sizes themselves (non-integer means included), against the oracle's
+    # double: within one unit in the last place
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    rs = np.random.RandomState(21)
+    for E, G in [(128, 31), (128, 8), (100, 7), (64, 3), (128, 2)]:
+        for _ in range(20):
+            g = rs.randint(0, G, size=E)
+            sizes = np.bincount(g, minlength=G)
+            mean = Decimal(E) / Decimal(G)
+            var = sum((Decimal(int(x)) - mean) ** 2 for x in sizes) / Decimal(G)
+            exact = var.sqrt() / mean
+            got = gp.size_deviation(g, G)
+            assert abs(Decimal(got) - exact) <= Decimal(np.spacing(got)), (E, G, got, exact)
+    # balanced sizes give 0 exactly
+    assert gp.size_deviation(np.repeat(np.arange(8), 16), 8) == 0.0
+
+
 def test_knee_by_hand():
     r = np.linspace(0, 1, 17)
     Uc = 1 - (1 - r) ** 6                          # steep rise, then flat: knee early
