@@ -40,7 +40,6 @@ __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint
                                                                       const float* __restrict__ idf,
                                                                       double* __restrict__ stats, uint32_t* status) {
   __shared__ int c1[256], c2[256];
-  __shared__ double red[3][MS_STATS_THREADS / 32];
   const int r = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t0 = req_off[r], t1 = req_off[r + 1];
   const int R = gridDim.x;
@@ -100,33 +99,50 @@ __global__ void __launch_bounds__(MS_STATS_THREADS) mask_stats_kernel(const uint
   }
   if (bad_id) atomicOr(status, WS_BIT_EDATA);  // an id outside [0, E) is skipped and reported
   __syncthreads();
-  double a = 0.0, b = 0.0, c = 0.0;
-  for (int e = tid; e < E; e += MS_STATS_THREADS) {
-    const double w = idf != nullptr ? (double)idf[(size_t)l * E + e] : 1.0;
-    const double w1 = c1[e] * w, w2 = c2[e] * w;
-    a = fma(w1, w1, a);
-    b = fma(w2, w2, b);
-    c = fma(w1, w2, c);
-  }
+  // the three sums, by warp 0 alone: GB300 issues fp64 at about 16 cycles per
+  // warp instruction per SM, and the grid has one CTA per (request, layer)
+  if (warp != 0) return;
+  if (idf == nullptr) {
+    // unit weights: sums of integer products, exact in int64 (and in the
+    // double they are converted to, being far below 2^53)
+    long long a = 0, b = 0, c = 0;
+    for (int e = lane; e < E; e += 32) {
+      const long long x = c1[e], y = c2[e];
+      a += x * x;
+      b += y * y;
+      c += x * y;
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a += __shfl_xor_sync(FULL, a, o);
-    b += __shfl_xor_sync(FULL, b, o);
-    c += __shfl_xor_sync(FULL, c, o);
-  }
-  if (lane == 0) {
-    red[0][warp] = a;
-    red[1][warp] = b;
-    red[2][warp] = c;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    double s[3] = {0.0, 0.0, 0.0};
-    for (int w = 0; w < MS_STATS_THREADS / 32; ++w)
-      for (int j = 0; j < 3; ++j) s[j] += red[j][w];
-    out[0] = s[0];
-    out[1] = s[1];
-    out[2] = s[2];
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(FULL, a, o);
+      b += __shfl_xor_sync(FULL, b, o);
+      c += __shfl_xor_sync(FULL, c, o);
+    }
+    if (lane == 0) {
+      out[0] = (double)a;
+      out[1] = (double)b;
+      out[2] = (double)c;
+    }
+  } else {
+    double a = 0.0, b = 0.0, c = 0.0;
+    for (int e = lane; e < E; e += 32) {
+      const double w = (double)idf[(size_t)l * E + e];
+      const double w1 = c1[e] * w, w2 = c2[e] * w;
+      a = fma(w1, w1, a);
+      b = fma(w2, w2, b);
+      c = fma(w1, w2, c);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(FULL, a, o);
+      b += __shfl_xor_sync(FULL, b, o);
+      c += __shfl_xor_sync(FULL, c, o);
+    }
+    if (lane == 0) {
+      out[0] = a;
+      out[1] = b;
+      out[2] = c;
+    }
   }
 }
 
