@@ -54,6 +54,7 @@ constexpr int SP_NGRID = 17;
 constexpr int SP_EMBED_THREADS = 1024;
 constexpr int SP_GROUP_THREADS = 256;
 constexpr int SP_MAX_STEPS = 100;
+constexpr int SP_LU_SLOTS = 8;  // eigenvectors whose inverse iterations run at once (a warp each)
 
 
 __device__ __forceinline__ double sp_warp_sum(double v) {
@@ -62,16 +63,35 @@ __device__ __forceinline__ double sp_warp_sum(double v) {
   return v;
 }
 
-__device__ __forceinline__ int sp_sturm(const double* dg, const double* e2, int n, double x, double pivmin) {
-  // number of eigenvalues of the tridiagonal form below x (signs of the pivots
-  // of T - x I = L D L^T)
-  double q = dg[0] - x;
-  if (fabs(q) < pivmin) q = -pivmin;
-  int c = q < 0.0 ? 1 : 0;
+// Number of eigenvalues of the tridiagonal form below x: the sign changes in
+// the leading principal minors of T - x I (p_0 = 1, p_1 = d_0 - x,
+// p_{i+1} = (d_i - x) p_i - e_i^2 p_{i-1}, e_i^2 = e2[i]).  This is the ratio
+// form's count (pivot q_i = p_{i+1} / p_i < 0) without its division: fp64
+// divisions are a long instruction sequence on this part, and a Sturm count
+// is the multisection's whole cost.  A minor below 2^-52 of the one before it
+// is replaced by -2^-52 times that one (the ratio form's pivot floored to a
+// tiny negative), and both carried minors are rescaled by an exact power of
+// two when the newer leaves [2^-256, 2^256]; both tests read the exponent
+// field.
+__device__ __forceinline__ int sp_sturm(const double* dg, const double* e2, int n, double x) {
+  auto expo = [](double v) { return (int)(((unsigned long long)__double_as_longlong(v) >> 52) & 0x7FF); };
+  auto sgn = [](double v) { return (unsigned)((unsigned long long)__double_as_longlong(v) >> 63); };
+  double pm = 1.0, p = dg[0] - x;
+  if (expo(p) + 52 < 1023) p = -0x1p-52;
+  int c = (int)sgn(p);
   for (int i = 1; i < n; ++i) {
-    q = (dg[i] - x) - e2[i] / q;
-    if (fabs(q) < pivmin) q = -pivmin;
-    c += q < 0.0 ? 1 : 0;
+    const double pn = fma(dg[i] - x, p, -(e2[i] * pm));
+    pm = p;
+    p = pn;
+    const int ep = expo(p);
+    if (ep + 52 < expo(pm)) {
+      p = -0x1p-52 * pm;
+    } else if (ep > 1023 + 256 || ep < 1023 - 256) {
+      const double sc = __longlong_as_double((long long)(2046 - ep) << 52);  // 2^(1023 - ep)
+      p *= sc;
+      pm *= sc;
+    }
+    c += (int)(sgn(p) ^ sgn(pm));
   }
   return c;
 }
@@ -87,9 +107,10 @@ __device__ __forceinline__ int sp_sturm(const double* dg, const double* e2, int 
 //     (j+1)-th largest between Gershgorin bounds and narrows the bracket 33-fold
 //     per step with a Sturm count at 32 points (one per lane).
 //   * Their eigenvectors by inverse iteration on T (LU with partial pivoting,
-//     three solves from a fixed start vector, each re-orthogonalised against
-//     the vectors found before it whose eigenvalues lie within 1e-3 |T|),
-//     then taken back through the reflections: x = H_0 ... H_{E-3} y.
+//     three solves from a fixed start vector; after each solve, in eigenvalue
+//     order, re-orthogonalised against the earlier vectors whose eigenvalues
+//     lie within 1e-3 |T|), eight vectors at once, a warp each; then taken
+//     back through the reflections: x = H_0 ... H_{E-3} y.
 //   Rows of the embedding are the G eigenvectors' components, scaled to unit
 //   length.  Only the G vectors are formed: fp64 divisions and square roots
 //   are slow on this part, and a full QL solve spent ~37 M clock cycles per
@@ -106,14 +127,17 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
   double* dg = pw + E;       // [E] diagonal of T
   double* sd = dg + E;       // [E] subdiagonal: sd[i] couples i and i + 1
   double* bet = sd + E;      // [E] beta of reflection k (0: none needed)
-  double* lu0 = bet + E;     // [E] LU of T - lambda I: reciprocal pivots,
-  double* lu1 = lu0 + E;     // [E]   first and
-  double* lu2 = lu1 + E;     // [E]   second superdiagonal,
-  double* lmul = lu2 + E;    // [E]   multipliers
-  double* lam = lmul + E;    // [32] eigenvalues, largest first
+  double* lam = bet + E;     // [32] eigenvalues, largest first
   double* red = lam + 32;    // [32]
   double* Y = red + 32;      // [G][E] eigenvectors
-  int* lsw = reinterpret_cast<int*>(Y + (size_t)G * E);  // [E] row swaps of the LU
+  // LU of T - lambda I for up to SP_LU_SLOTS eigenvectors at once, slot s at
+  // s * E: reciprocal pivots, first and second superdiagonal, multipliers,
+  // row swaps
+  double* lu0 = Y + (size_t)G * E;
+  double* lu1 = lu0 + SP_LU_SLOTS * E;
+  double* lu2 = lu1 + SP_LU_SLOTS * E;
+  double* lmul = lu2 + SP_LU_SLOTS * E;
+  int* lsw = reinterpret_cast<int*>(lmul + SP_LU_SLOTS * E);
   const int l = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int32_t* A = affinity + (size_t)l * E * E;
@@ -213,7 +237,7 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     double lo = -tn - pivmin, hi = tn + pivmin;
     for (int it = 0; it < 64; ++it) {
       const double x = lo + (hi - lo) * ((double)(lane + 1) / 33.0);
-      const int cnt = sp_sturm(dg, pw, n, x, pivmin);
+      const int cnt = sp_sturm(dg, pw, n, x);
       const unsigned above = __ballot_sync(FULL, cnt > j);
       if (above == 0u) {
         lo = __shfl_sync(FULL, x, 31);
@@ -228,74 +252,89 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     if (lane == 0) lam[warp] = 0.5 * (lo + hi);
   }
   __syncthreads();
-  // ---- inverse iteration, one eigenvector after another (warp 0)
-  if (warp == 0) {
-    for (int w = 0; w < G; ++w) {
-      const double lambda = lam[w];
+  // ---- inverse iteration, up to SP_LU_SLOTS eigenvectors at once: warp w
+  //      factors and solves for vector w0 + w (lane 0 runs the recurrences);
+  //      between iterations warp 0 re-orthogonalises the batch in order against
+  //      the earlier vectors with eigenvalues within 1e-3 |T| and normalises
+  for (int w0 = 0; w0 < G; w0 += SP_LU_SLOTS) {
+    const int nb = min(SP_LU_SLOTS, G - w0);
+    const int w = warp;
+    double* y = Y + (size_t)(w0 + w) * n;
+    double* f0 = lu0 + (size_t)w * n;
+    double* f1 = lu1 + (size_t)w * n;
+    double* f2 = lu2 + (size_t)w * n;
+    double* fm = lmul + (size_t)w * n;
+    int* fs = lsw + (size_t)w * n;
+    if (w < nb) {
+      const double lambda = lam[w0 + w];
       if (lane == 0) {
         double ca = dg[0] - lambda, cb = sd[0];
         for (int i = 0; i + 1 < n; ++i) {
-          const double nc = sd[i], na = dg[i + 1] - lambda, nb = i + 2 < n ? sd[i + 1] : 0.0;
+          const double nc = sd[i], na = dg[i + 1] - lambda, nb2 = i + 2 < n ? sd[i + 1] : 0.0;
           if (fabs(ca) >= fabs(nc) || fabs(nc) <= pivmin) {  // no swap; a pivot below pivmin is floored
             const double piv = fabs(ca) > pivmin ? ca : (ca >= 0.0 ? pivmin : -pivmin);
             const double r = 1.0 / piv;
-            lu0[i] = r;
-            lu1[i] = cb;
-            lu2[i] = 0.0;
-            lmul[i] = nc * r;
-            lsw[i] = 0;
-            ca = na - lmul[i] * cb;
-            cb = nb;
+            f0[i] = r;
+            f1[i] = cb;
+            f2[i] = 0.0;
+            fm[i] = nc * r;
+            fs[i] = 0;
+            ca = na - fm[i] * cb;
+            cb = nb2;
           } else {
             const double r = 1.0 / nc;
-            lu0[i] = r;
-            lu1[i] = na;
-            lu2[i] = nb;
-            lmul[i] = ca * r;
-            lsw[i] = 1;
-            ca = cb - lmul[i] * na;
-            cb = -lmul[i] * nb;
+            f0[i] = r;
+            f1[i] = na;
+            f2[i] = nb2;
+            fm[i] = ca * r;
+            fs[i] = 1;
+            ca = cb - fm[i] * na;
+            cb = -fm[i] * nb2;
           }
         }
-        lu0[n - 1] = 1.0 / (fabs(ca) > pivmin ? ca : (ca >= 0.0 ? pivmin : -pivmin));
+        f0[n - 1] = 1.0 / (fabs(ca) > pivmin ? ca : (ca >= 0.0 ? pivmin : -pivmin));
       }
-      double* y = Y + (size_t)w * n;
       for (int i = lane; i < n; i += 32) y[i] = (double)(((unsigned)i * 2654435761u) % 1000u) / 1000.0 - 0.499;
       __syncwarp();
-      for (int it = 0; it < 3; ++it) {
-        if (lane == 0) {  // solve (T - lambda I) y' = y
-          for (int i = 0; i + 1 < n; ++i) {
-            if (lsw[i]) {
-              const double t = y[i];
-              y[i] = y[i + 1];
-              y[i + 1] = t;
-            }
-            y[i + 1] -= lmul[i] * y[i];
+    }
+    for (int it = 0; it < 3; ++it) {
+      if (w < nb && lane == 0) {  // solve (T - lambda I) y' = y
+        for (int i = 0; i + 1 < n; ++i) {
+          if (fs[i]) {
+            const double t = y[i];
+            y[i] = y[i + 1];
+            y[i + 1] = t;
           }
-          y[n - 1] *= lu0[n - 1];
-          y[n - 2] = (y[n - 2] - lu1[n - 2] * y[n - 1]) * lu0[n - 2];
-          for (int i = n - 3; i >= 0; --i) y[i] = (y[i] - lu1[i] * y[i + 1] - lu2[i] * y[i + 2]) * lu0[i];
+          y[i + 1] -= fm[i] * y[i];
         }
-        __syncwarp();
-        for (int u = 0; u < w; ++u) {
-          if (fabs(lam[u] - lambda) > 1e-3 * tn) continue;
-          const double* z = Y + (size_t)u * n;
-          double t = 0.0;
-          for (int i = lane; i < n; i += 32) t = fma(z[i], y[i], t);
-          t = sp_warp_sum(t);
-          for (int i = lane; i < n; i += 32) y[i] = fma(-t, z[i], y[i]);
+        y[n - 1] *= f0[n - 1];
+        y[n - 2] = (y[n - 2] - f1[n - 2] * y[n - 1]) * f0[n - 2];
+        for (int i = n - 3; i >= 0; --i) y[i] = (y[i] - f1[i] * y[i + 1] - f2[i] * y[i + 2]) * f0[i];
+      }
+      __syncthreads();
+      if (warp == 0) {
+        for (int v = w0; v < w0 + nb; ++v) {
+          double* yv = Y + (size_t)v * n;
+          for (int u = 0; u < v; ++u) {
+            if (fabs(lam[u] - lam[v]) > 1e-3 * tn) continue;
+            const double* z = Y + (size_t)u * n;
+            double t = 0.0;
+            for (int i = lane; i < n; i += 32) t = fma(z[i], yv[i], t);
+            t = sp_warp_sum(t);
+            for (int i = lane; i < n; i += 32) yv[i] = fma(-t, z[i], yv[i]);
+            __syncwarp();
+          }
+          double s2 = 0.0;
+          for (int i = lane; i < n; i += 32) s2 = fma(yv[i], yv[i], s2);
+          s2 = sp_warp_sum(s2);
+          const double sc = s2 > 0.0 ? 1.0 / sqrt(s2) : 0.0;
+          for (int i = lane; i < n; i += 32) yv[i] *= sc;
           __syncwarp();
         }
-        double s2 = 0.0;
-        for (int i = lane; i < n; i += 32) s2 = fma(y[i], y[i], s2);
-        s2 = sp_warp_sum(s2);
-        const double sc = s2 > 0.0 ? 1.0 / sqrt(s2) : 0.0;
-        for (int i = lane; i < n; i += 32) y[i] *= sc;
-        __syncwarp();
       }
+      __syncthreads();
     }
   }
-  __syncthreads();
   // ---- back through the reflections: y <- H_k y for k = E-3 .. 0, warp j for vector j
   if (warp < G) {
     double* y = Y + (size_t)warp * n;
@@ -792,7 +831,8 @@ moer_status spectral_launch(const moer_dims* d, const int32_t* affinity, int32_t
 }
 
 size_t spec_embed_smem(int E, int G) {
-  return ((size_t)E * E + 10 * (size_t)E + 64 + (size_t)G * E) * sizeof(double) + (size_t)E * sizeof(int);
+  return ((size_t)E * E + 6 * (size_t)E + 64 + (size_t)G * E + 4 * (size_t)SP_LU_SLOTS * E) * sizeof(double) +
+         (size_t)SP_LU_SLOTS * E * sizeof(int);
 }
 
 }  // namespace moer
