@@ -253,8 +253,8 @@ MOER_API moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, 
  * Limits: E <= 128, 2 <= G <= 31, G <= E.
  * ws       at least moer_spectral_workspace_bytes(d, G) bytes, 256-byte aligned
  *          (status word, eigenvectors, embedding, degrees, groups per grid
- *          point).  A Jacobi sweep or an assignment that hits its bound
- *          records MOER_ETIMEOUT.
+ *          point).  A bounded assignment that hits its pass bound records
+ *          MOER_ETIMEOUT.
  */
 MOER_API size_t moer_spectral_workspace_bytes(const moer_dims* d, int32_t G);
 MOER_API moer_status moer_spectral_groups(const moer_dims* d, const int32_t* affinity, int32_t G,
