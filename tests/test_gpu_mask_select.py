@@ -2,7 +2,9 @@
 (oracle/mask_select.py): the layers in the order chosen must be identical, except where
 two candidates' qualities agree to 1e-12 (then either is a correct greedy step), and the
 qualities must agree to 1e-12 relative.  Inputs: synthetic ids with informative, partly
-informative and noise layers; and the path's own top-k over a calibration-shaped batch.
+informative and noise layers; 700 requests (several request slices per layer in a greedy
+step); requests of 0 and 1 tokens, a single request, and every layer chosen; and the path's
+own top-k over a calibration-shaped batch.
 """
 import numpy as np
 import pytest
@@ -68,6 +70,41 @@ def _compare(topk, off, E, m, idf, got_mask, got_q):
             assert abs(qa - qb) <= 1e-12 * max(1.0, abs(qb)), (step, got_mask, om)
             return
         assert abs(got_q[step] - oq[step]) <= 1e-12 * max(1.0, abs(oq[step])), step
+
+
+def _with_lengths(seed, L, E, k, lens):
+    rs = np.random.RandomState(seed)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = max(int(off[-1]), 1)
+    topk = np.stack([np.stack([rs.choice(E, size=k, replace=False) for _ in range(T)]) for _ in range(L)])
+    return topk.astype(np.uint8), off
+
+
+def test_several_request_slices_per_layer(env):
+    # 700 requests over 8 layers: each greedy step splits every layer's requests over
+    # three CTAs, and the last CTA to finish combines their partial sums
+    topk, off = _synthetic(4, 8, 32, 4, 700)
+    got_m, got_q = _run(env, topk, off, 32, 6)
+    _compare(topk, off, 32, 6, None, got_m, got_q)
+
+
+@pytest.mark.parametrize("case", ["empty_and_one_token", "one_request", "all_layers"])
+def test_degenerate_requests_and_masks(env, case):
+    # requests of 0 and 1 tokens (both halves, or the first, empty: cosine 0), one
+    # request, and m = L (every layer chosen, the last with the only quality left)
+    L, E, k = 6, 32, 4
+    if case == "empty_and_one_token":
+        lens, m = [0, 1, 5, 0, 1, 2, 9, 0], 4
+    elif case == "one_request":
+        lens, m = [37], 3
+    else:
+        lens, m = [3, 8, 1, 12, 6], L
+    topk, off = _with_lengths(len(case), L, E, k, lens)
+    got_m, got_q = _run(env, topk, off, E, m)
+    assert sorted(got_m.tolist()) == sorted(set(got_m.tolist())) and (got_m >= 0).all() and (got_m < L).all()
+    _compare(topk, off, E, m, None, got_m, got_q)
+    if case == "all_layers":
+        assert sorted(got_m.tolist()) == list(range(L))
 
 
 @pytest.mark.parametrize("seed,L,E,k,R,m", [(1, 8, 32, 4, 50, 8), (2, 24, 64, 6, 120, 10), (3, 48, 128, 8, 60, 12)])
