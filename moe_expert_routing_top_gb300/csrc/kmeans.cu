@@ -69,6 +69,17 @@ static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
 
 __device__ __forceinline__ int km_cap(int d, int N, int D) { return N / D + (d < N % D ? 1 : 0); }
 
+// The kernels of a fit are chained by programmatic dependent launch: each
+// waits for the grid before it in the stream (whose writes are then visible),
+// then lets the next grid start launching, so that a launch's latency overlaps
+// the work before it (after convergence the steps return at once, and their
+// launches are the fit's cost).  A dependent grid is scheduled only after every
+// CTA of the grid it waits for has started.
+__device__ __forceinline__ void km_chain() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __global__ void km_init_kernel(const float* __restrict__ init, double* __restrict__ cent, int64_t n) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) cent[i] = (double)init[i];
@@ -83,6 +94,7 @@ __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ 
                                                       const double* __restrict__ cent, double* __restrict__ cost,
                                                       const KmState* state, int force) {
   __shared__ double s64[KM_COST_CHUNK];
+  km_chain();
   if (!force && state->converged) return;
   const int i = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* s = sig + (size_t)i * dim;
@@ -146,6 +158,7 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
   __shared__ int s_first;
   __shared__ unsigned long long s_key[KM_SORT_MAX];
   __shared__ int s_ord[KM_SORT_MAX];
+  km_chain();
   if (state->converged) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int DS = D + 1;  // key row stride: consecutive rows start in different banks
@@ -486,6 +499,7 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
 __global__ void __launch_bounds__(256) km_update_kernel(const float* __restrict__ sig, int32_t N, int32_t dim,
                                                         int32_t D, const int32_t* __restrict__ ord,
                                                         double* __restrict__ cent, const KmState* state) {
+  km_chain();
   if (state->converged) return;
   const int d = blockIdx.y;
   const int j = blockIdx.x * 256 + threadIdx.x;
@@ -512,6 +526,7 @@ __global__ void __launch_bounds__(KM_THREADS) km_finalize_kernel(const double* _
                                                                   int32_t dim, int32_t D, float* __restrict__ out,
                                                                   int32_t* info, double* objective,
                                                                   const KmState* state) {
+  km_chain();
   __shared__ double red[KM_THREADS / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int64_t q = tid; q < (int64_t)D * dim; q += KM_THREADS) out[q] = (float)cent[q];
@@ -566,14 +581,39 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
                       3 * (int64_t)N * (int64_t)sizeof(int32_t);
   const bool staged = dyn <= dyn_max;
   if (staged && smem_optin(km_assign_kernel, (int)dyn_max, assign_set) != cudaSuccess) return MOER_ECUDA;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  auto cfg = [&](dim3 g, dim3 b, size_t smem) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = g;
+    c.blockDim = b;
+    c.dynamicSmemBytes = smem;
+    c.stream = st;
+    c.attrs = pdl;
+    c.numAttrs = 1;
+    return c;
+  };
+  const cudaLaunchConfig_t c_cost = cfg(dim3((unsigned)N), dim3(256), 0);
+  const cudaLaunchConfig_t c_assign = cfg(dim3(1), dim3(KM_THREADS), staged ? (size_t)dyn : 0);
+  const cudaLaunchConfig_t c_update = cfg(ug, dim3(256), 0);
+  const cudaLaunchConfig_t c_final = cfg(dim3(1), dim3(KM_THREADS), 0);
+  const int32_t stg = staged ? 1 : 0;
   for (int it = 0; it < max_iter; ++it) {
-    km_cost_kernel<<<(unsigned)N, 256, 0, st>>>(sig, dim, D, cent, cost, state, 0);
-    km_assign_kernel<<<1, KM_THREADS, staged ? (size_t)dyn : 0, st>>>(cost, N, D, assign, prev, mem, pos, dkey,
-                                                                       state, max_cancel, staged ? 1 : 0, status);
-    km_update_kernel<<<ug, 256, 0, st>>>(sig, N, dim, D, mem, cent, state);
+    if (cudaLaunchKernelEx(&c_cost, km_cost_kernel, sig, dim, D, (const double*)cent, cost, (const KmState*)state,
+                           0) != cudaSuccess ||
+        cudaLaunchKernelEx(&c_assign, km_assign_kernel, (const double*)cost, N, D, assign, prev, mem, pos, dkey,
+                           state, max_cancel, stg, status) != cudaSuccess ||
+        cudaLaunchKernelEx(&c_update, km_update_kernel, sig, N, dim, D, (const int32_t*)mem, cent,
+                           (const KmState*)state) != cudaSuccess)
+      return MOER_ECUDA;
   }
-  km_cost_kernel<<<(unsigned)N, 256, 0, st>>>(sig, dim, D, cent, cost, state, 1);
-  km_finalize_kernel<<<1, KM_THREADS, 0, st>>>(cost, cent, assign, N, dim, D, centroids, info, objective, state);
+  if (cudaLaunchKernelEx(&c_cost, km_cost_kernel, sig, dim, D, (const double*)cent, cost, (const KmState*)state,
+                         1) != cudaSuccess ||
+      cudaLaunchKernelEx(&c_final, km_finalize_kernel, (const double*)cost, (const double*)cent,
+                         (const int32_t*)assign, N, dim, D, centroids, info, objective,
+                         (const KmState*)state) != cudaSuccess)
+    return MOER_ECUDA;
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
