@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
                       double* __restrict__ deg_out) {
   extern __shared__ double sp_sm[];
   const int n = E;
-  double* M = sp_sm;         // [E][E]
-  double* inv = M + E * E;   // [E] D^-1/2
+  double* M = sp_sm;         // [E][E + 1] (padded rows)
+  double* inv = M + E * (E + 1);  // [E] D^-1/2
   double* vv = inv + E;      // [E] Householder vector
   double* pw = vv + E;       // [E] p, then w; later e2[i] = sd[i-1]^2
   double* dg = pw + E;       // [E] diagonal of T
@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
   int* lsw = reinterpret_cast<int*>(lmul + SP_LU_SLOTS * E);
   const int l = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const int S = E + 1;  // row stride of M: consecutive rows start two banks apart
   const int32_t* A = affinity + (size_t)l * E * E;
   for (int a = tid; a < E; a += nt) {
     long long d = 0;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
   for (int q = tid; q < E * E; q += nt) {
     const int a = q / E, b = q - a * E;
     const int32_t x = A[q] > 0 ? A[q] : 0;
-    M[q] = (a == b) ? 0.0 : inv[a] * (double)x * inv[b];
+    M[a * S + b] = (a == b) ? 0.0 : inv[a] * (double)x * inv[b];
   }
   __syncthreads();
   // ---- Householder reduction to tridiagonal form
@@ -161,12 +162,12 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     if (warp == 0) {
       double s2 = 0.0;
       for (int j = 1 + lane; j < m; j += 32) {
-        const double x = M[(k + 1 + j) * n + k];
+        const double x = M[(k + 1 + j) * S + k];
         s2 = fma(x, x, s2);
       }
       s2 = sp_warp_sum(s2);
       if (lane == 0) {
-        const double x0 = M[(k + 1) * n + k];
+        const double x0 = M[(k + 1) * S + k];
         if (s2 == 0.0) {  // already reduced
           sd[k] = x0;
           bet[k] = 0.0;
@@ -177,20 +178,21 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
           bet[k] = 1.0 / (sig - alpha * x0);
           red[0] = x0 - alpha;
         }
-        dg[k] = M[k * n + k];
+        dg[k] = M[k * S + k];
       }
     }
     __syncthreads();
     const double beta = bet[k];
     if (beta == 0.0) continue;
-    for (int j = tid; j < m; j += nt) vv[j] = j == 0 ? red[0] : M[(k + 1 + j) * n + k];
+    for (int j = tid; j < m; j += nt) vv[j] = j == 0 ? red[0] : M[(k + 1 + j) * S + k];
     __syncthreads();
-    {  // p = beta A22 v, eight threads per row (nt / 8 >= m rows)
+    {  // p = beta A22 v, eight threads per row (nt / 8 >= m rows); only the
+       // lower triangle of A22 is kept, so A22[i][j] for j > i is read as A22[j][i]
       const int i = tid >> 3;
       double acc = 0.0;
       if (i < m) {
-        const double* row = M + (k + 1 + i) * n + (k + 1);
-        for (int j = tid & 7; j < m; j += 8) acc = fma(row[j], vv[j], acc);
+        const double* a22 = M + (k + 1) * S + (k + 1);
+        for (int j = tid & 7; j < m; j += 8) acc = fma(j <= i ? a22[i * S + j] : a22[j * S + i], vv[j], acc);
       }
       acc += __shfl_xor_sync(FULL, acc, 1);
       acc += __shfl_xor_sync(FULL, acc, 2);
@@ -208,18 +210,27 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     const double kc = red[1];
     for (int j = tid; j < m; j += nt) pw[j] = fma(-kc, vv[j], pw[j]);
     __syncthreads();
-    for (int q = tid; q < m * m; q += nt) {  // A22 -= v w^T + w v^T
-      const int i = q / m, j = q - i * m;
-      double* e = M + (k + 1 + i) * n + (k + 1 + j);
-      *e = *e - vv[i] * pw[j] - pw[i] * vv[j];
+    {  // A22 -= v w^T + w v^T on the lower triangle: warp u takes rows u and
+       // m-1-u (together m+1 elements), then u + 32 and m-1-(u+32), ...
+      double* a22 = M + (k + 1) * S + (k + 1);
+      const int nw = nt >> 5;
+      for (int pr = warp; pr < (m + 1) / 2; pr += nw) {
+        const int ra = pr, rb = m - 1 - pr;
+        const int len = (ra + 1) + (rb != ra ? rb + 1 : 0);
+        for (int t = lane; t < len; t += 32) {
+          const int i = t <= ra ? ra : rb, j = t <= ra ? t : t - (ra + 1);
+          double* e = a22 + i * S + j;
+          *e = *e - vv[i] * pw[j] - pw[i] * vv[j];
+        }
+      }
     }
-    for (int j = tid; j < m; j += nt) M[k * n + (k + 1 + j)] = vv[j];  // v, for the eigenvectors
+    for (int j = tid; j < m; j += nt) M[k * S + (k + 1 + j)] = vv[j];  // v, for the eigenvectors
     __syncthreads();
   }
   if (tid == 0) {
-    dg[n - 2] = M[(n - 2) * n + (n - 2)];
-    sd[n - 2] = M[(n - 1) * n + (n - 2)];
-    dg[n - 1] = M[(n - 1) * n + (n - 1)];
+    dg[n - 2] = M[(n - 2) * S + (n - 2)];
+    sd[n - 2] = M[(n - 1) * S + (n - 2)];
+    dg[n - 1] = M[(n - 1) * S + (n - 1)];
     sd[n - 1] = 0.0;
     double tn = 0.0;  // Gershgorin bound of T
     for (int i = 0; i < n; ++i) tn = fmax(tn, fabs(dg[i]) + fabs(sd[i]) + (i > 0 ? fabs(sd[i - 1]) : 0.0));
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
     for (int k = n - 3; k >= 0; --k) {
       if (bet[k] == 0.0) continue;
       const int m = n - k - 1;
-      const double* v = M + k * n + (k + 1);
+      const double* v = M + k * S + (k + 1);
       double t = 0.0;
       for (int j = lane; j < m; j += 32) t = fma(v[j], y[k + 1 + j], t);
       const double f = bet[k] * sp_warp_sum(t);
@@ -831,7 +842,7 @@ moer_status spectral_launch(const moer_dims* d, const int32_t* affinity, int32_t
 }
 
 size_t spec_embed_smem(int E, int G) {
-  return ((size_t)E * E + 6 * (size_t)E + 64 + (size_t)G * E + 4 * (size_t)SP_LU_SLOTS * E) * sizeof(double) +
+  return ((size_t)E * (E + 1) + 6 * (size_t)E + 64 + (size_t)G * E + 4 * (size_t)SP_LU_SLOTS * E) * sizeof(double) +
          (size_t)SP_LU_SLOTS * E * sizeof(int);
 }
 
