@@ -11,8 +11,9 @@
 // after max_iter steps.
 //
 // Design (GB300):
-//   * Squared distances in fp64 (one CTA per point, one warp per centroid:
-//     the assignment decisions are taken in double precision).
+//   * Squared distances in fp64 as ||s||^2 + ||c||^2 - 2 s.c (one CTA per
+//     point, one warp per centroid: the assignment decisions are taken in
+//     double precision).
 //   * The balanced assignment is a transportation problem with N unit sources
 //     and D sinks.  One CTA keeps a feasible assignment (the previous step's,
 //     or a greedy one at the first step) and cancels negative cycles of the
@@ -50,7 +51,7 @@ struct KmState {
 };
 
 struct KmLayout {
-  size_t state, cost, cent, prev, mem, pos, dkey, total;
+  size_t state, cost, cent, cpart, prev, mem, pos, dkey, total;
 };
 
 static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
@@ -59,7 +60,8 @@ static KmLayout km_layout(int32_t N, int32_t dim, int32_t D) {
   l.state = WS_HEADER;
   l.cost = l.state + 256;
   l.cent = l.cost + r256((size_t)N * D * sizeof(double));
-  l.prev = l.cent + r256((size_t)D * dim * sizeof(double));
+  l.cpart = l.cent + r256((size_t)D * dim * sizeof(double));
+  l.prev = l.cpart + r256((size_t)D * ((dim + 255) / 256) * sizeof(double));
   l.mem = l.prev + r256((size_t)N * sizeof(int32_t));
   l.pos = l.mem + r256((size_t)N * sizeof(int32_t));
   l.dkey = l.pos + r256((size_t)N * sizeof(int32_t));
@@ -80,20 +82,49 @@ __device__ __forceinline__ void km_chain() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__global__ void km_init_kernel(const float* __restrict__ init, double* __restrict__ cent, int64_t n) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) cent[i] = (double)init[i];
+// Sum of v over a block of 256 threads, in a fixed order; thread 0 gets it.
+__device__ __forceinline__ double km_block_sum256(double v, double* red8) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  if (lane == 0) red8[warp] = v;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < 8; ++w) t += red8[w];
+  return t;
 }
 
-// cost[i][d] = ||s_i - c_d||^2 in fp64; block i, warp w takes centroids w, w + 8, ...
-// The signature row is widened to fp64 once per block, a chunk at a time, into
-// shared memory (each lane still sums its elements j = lane, lane + 32, ... in
-// order, then the warp reduces).
+// cent = init widened to fp64; block (bx, d) also leaves the sum of squares of
+// its 256 coordinates of centroid d in cpart[d][bx] (see km_cost_kernel).
+__global__ void __launch_bounds__(256) km_init_kernel(const float* __restrict__ init, int32_t dim,
+                                                      double* __restrict__ cent, double* __restrict__ cpart) {
+  __shared__ double red8[8];
+  const int d = blockIdx.y, j = blockIdx.x * 256 + threadIdx.x;
+  double c = 0.0;
+  if (j < dim) {
+    c = (double)init[(size_t)d * dim + j];
+    cent[(size_t)d * dim + j] = c;
+  }
+  const double t = km_block_sum256(c * c, red8);
+  if (threadIdx.x == 0) cpart[(size_t)d * gridDim.x + blockIdx.x] = t;
+}
+
+// cost[i][d] = ||s_i - c_d||^2 in fp64, as ||s_i||^2 + ||c_d||^2 - 2 s_i.c_d:
+// one fused multiply-add per element instead of a subtraction and one (fp64
+// runs at about 16 cycles per warp instruction per SM on this part).  Block i,
+// warp w takes centroids w, w + 8, ...; the signature row is widened to fp64
+// once per block, a chunk at a time, into shared memory, and its squares are
+// summed on the way.  ||c_d||^2 is the sum, in block order, of the partials
+// cpart[d][0 .. nbk) left by the kernel that wrote the centroids.
 constexpr int KM_COST_CHUNK = 2048;
 __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ sig, int32_t dim, int32_t D,
-                                                      const double* __restrict__ cent, double* __restrict__ cost,
-                                                      const KmState* state, int force) {
+                                                      const double* __restrict__ cent,
+                                                      const double* __restrict__ cpart, int32_t nbk,
+                                                      double* __restrict__ cost, const KmState* state, int force) {
   __shared__ double s64[KM_COST_CHUNK];
+  __shared__ double red8[8];
+  __shared__ double s_ss;
   km_chain();
   if (!force && state->converged) return;
   const int i = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -101,9 +132,14 @@ __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ 
   double acc[KM_MAXD / 8];
 #pragma unroll
   for (int q = 0; q < KM_MAXD / 8; ++q) acc[q] = 0.0;
+  double ssp = 0.0;
   for (int j0 = 0; j0 < dim; j0 += KM_COST_CHUNK) {
     const int n = min(KM_COST_CHUNK, dim - j0);
-    for (int j = threadIdx.x; j < n; j += 256) s64[j] = (double)s[j0 + j];
+    for (int j = threadIdx.x; j < n; j += 256) {
+      const double v = (double)s[j0 + j];
+      s64[j] = v;
+      ssp = fma(v, v, ssp);
+    }
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < KM_MAXD / 8; ++q) {
@@ -111,15 +147,16 @@ __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ 
       if (d < D) {
         const double* c = cent + (size_t)d * dim + j0;
         double t_acc = acc[q];
-        for (int j = lane; j < n; j += 32) {
-          const double t = s64[j] - c[j];
-          t_acc = fma(t, t, t_acc);
-        }
+        for (int j = lane; j < n; j += 32) t_acc = fma(s64[j], c[j], t_acc);
         acc[q] = t_acc;
       }
     }
     __syncthreads();
   }
+  const double sst = km_block_sum256(ssp, red8);
+  if (threadIdx.x == 0) s_ss = sst;
+  __syncthreads();
+  const double ss = s_ss;
 #pragma unroll
   for (int q = 0; q < KM_MAXD / 8; ++q) {
     const int d = warp + 8 * q;
@@ -127,7 +164,11 @@ __global__ void __launch_bounds__(256) km_cost_kernel(const float* __restrict__ 
       double t_acc = acc[q];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) t_acc += __shfl_xor_sync(FULL, t_acc, o);
-      if (lane == 0) cost[(size_t)i * D + d] = t_acc;
+      if (lane == 0) {
+        double cc = 0.0;
+        for (int b = 0; b < nbk; ++b) cc += cpart[(size_t)d * nbk + b];
+        cost[(size_t)i * D + d] = fma(-2.0, t_acc, ss + cc);
+      }
     }
   }
 }
@@ -498,12 +539,14 @@ __global__ void __launch_bounds__(KM_THREADS, 1)
 // cluster's offset (written by the assignment step), eight loads in flight.
 __global__ void __launch_bounds__(256) km_update_kernel(const float* __restrict__ sig, int32_t N, int32_t dim,
                                                         int32_t D, const int32_t* __restrict__ ord,
-                                                        double* __restrict__ cent, const KmState* state) {
+                                                        double* __restrict__ cent, double* __restrict__ cpart,
+                                                        const KmState* state) {
+  __shared__ double red8[8];
   km_chain();
   if (state->converged) return;
   const int d = blockIdx.y;
   const int j = blockIdx.x * 256 + threadIdx.x;
-  if (j >= dim) return;
+  const int jj = j < dim ? j : dim - 1;  // threads past the end read a valid column, store nothing
   const int base = N / D, rem = N % D;
   const int o = d * base + min(d, rem), n = base + (d < rem ? 1 : 0);
   const int32_t* m = ord + o;
@@ -512,12 +555,18 @@ __global__ void __launch_bounds__(256) km_update_kernel(const float* __restrict_
   for (; k + 8 <= n; k += 8) {
     float v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = sig[(size_t)m[k + q] * dim + j];
+    for (int q = 0; q < 8; ++q) v[q] = sig[(size_t)m[k + q] * dim + jj];
 #pragma unroll
     for (int q = 0; q < 8; ++q) sum += (double)v[q];
   }
-  for (; k < n; ++k) sum += (double)sig[(size_t)m[k] * dim + j];
-  if (n > 0) cent[(size_t)d * dim + j] = sum / n;
+  for (; k < n; ++k) sum += (double)sig[(size_t)m[k] * dim + jj];
+  double c = 0.0;
+  if (j < dim && n > 0) {
+    c = sum / n;
+    cent[(size_t)d * dim + j] = c;
+  }
+  const double t = km_block_sum256(c * c, red8);
+  if (threadIdx.x == 0) cpart[(size_t)d * gridDim.x + blockIdx.x] = t;
 }
 
 __global__ void __launch_bounds__(KM_THREADS) km_finalize_kernel(const double* __restrict__ cost,
@@ -561,14 +610,15 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
   KmState* state = reinterpret_cast<KmState*>(w + l.state);
   double* cost = reinterpret_cast<double*>(w + l.cost);
   double* cent = reinterpret_cast<double*>(w + l.cent);
+  double* cpart = reinterpret_cast<double*>(w + l.cpart);
   int32_t* prev = reinterpret_cast<int32_t*>(w + l.prev);
   int32_t* mem = reinterpret_cast<int32_t*>(w + l.mem);
   int32_t* pos = reinterpret_cast<int32_t*>(w + l.pos);
   unsigned long long* dkey = reinterpret_cast<unsigned long long*>(w + l.dkey);
   uint32_t* status = reinterpret_cast<uint32_t*>(w);
   if (cudaMemsetAsync(state, 0, sizeof(KmState), st) != cudaSuccess) return MOER_ECUDA;
-  const int64_t nc = (int64_t)D * dim;
-  km_init_kernel<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(init, cent, nc);
+  const int32_t nbk = (dim + 255) / 256;
+  km_init_kernel<<<dim3((unsigned)nbk, (unsigned)D), 256, 0, st>>>(init, dim, cent, cpart);
   const int32_t max_cancel = 16 * N + 1024;
   const dim3 ug((unsigned)((dim + 255) / 256), (unsigned)D);
   // shared-memory staging of the assignment step when it fits beside the
@@ -600,16 +650,16 @@ moer_status kmeans_launch(const float* sig, int32_t N, int32_t dim, int32_t D, c
   const cudaLaunchConfig_t c_final = cfg(dim3(1), dim3(KM_THREADS), 0);
   const int32_t stg = staged ? 1 : 0;
   for (int it = 0; it < max_iter; ++it) {
-    if (cudaLaunchKernelEx(&c_cost, km_cost_kernel, sig, dim, D, (const double*)cent, cost, (const KmState*)state,
-                           0) != cudaSuccess ||
+    if (cudaLaunchKernelEx(&c_cost, km_cost_kernel, sig, dim, D, (const double*)cent, (const double*)cpart, nbk,
+                           cost, (const KmState*)state, 0) != cudaSuccess ||
         cudaLaunchKernelEx(&c_assign, km_assign_kernel, (const double*)cost, N, D, assign, prev, mem, pos, dkey,
                            state, max_cancel, stg, status) != cudaSuccess ||
-        cudaLaunchKernelEx(&c_update, km_update_kernel, sig, N, dim, D, (const int32_t*)mem, cent,
+        cudaLaunchKernelEx(&c_update, km_update_kernel, sig, N, dim, D, (const int32_t*)mem, cent, cpart,
                            (const KmState*)state) != cudaSuccess)
       return MOER_ECUDA;
   }
-  if (cudaLaunchKernelEx(&c_cost, km_cost_kernel, sig, dim, D, (const double*)cent, cost, (const KmState*)state,
-                         1) != cudaSuccess ||
+  if (cudaLaunchKernelEx(&c_cost, km_cost_kernel, sig, dim, D, (const double*)cent, (const double*)cpart, nbk,
+                         cost, (const KmState*)state, 1) != cudaSuccess ||
       cudaLaunchKernelEx(&c_final, km_finalize_kernel, (const double*)cost, (const double*)cent,
                          (const int32_t*)assign, N, dim, D, centroids, info, objective,
                          (const KmState*)state) != cudaSuccess)
