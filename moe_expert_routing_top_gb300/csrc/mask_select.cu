@@ -22,7 +22,8 @@
 //     candidate layer) evaluate the candidates (fp64 cosines of the running
 //     sums plus the candidate's), and the last CTA to finish picks the layer
 //     and adds its sums to the running sums.  The fp64 square roots and
-//     divisions are spread over the SMs, and a step is one launch.
+//     divisions are spread over the SMs, a step is one launch, and the steps
+//     are chained by programmatic dependent launch.
 #include <algorithm>
 
 #include "common.cuh"
@@ -165,6 +166,11 @@ __global__ void __launch_bounds__(MS_EVAL_THREADS) mask_step_kernel(const double
                                                                     double* __restrict__ quality_out) {
   __shared__ double red[MS_EVAL_THREADS / 32];
   __shared__ int s_last;
+  // the greedy steps are chained by programmatic dependent launch: wait for
+  // the grid before this one (its pick and running sums are then visible),
+  // then let the next step start launching
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int S = gridDim.x, s = blockIdx.x, l = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (R + S - 1) / S, r0 = s * per, r1 = min(R, r0 + per);
@@ -259,9 +265,20 @@ moer_status mask_select_launch(const moer_dims* d, const uint8_t* topk, int64_t 
   const int64_t want = std::max<int64_t>(1, 2 * (int64_t)device_sm_count() / d->L);
   const unsigned S = (unsigned)std::min<int64_t>(
       std::min<int64_t>(((int64_t)R + MS_EVAL_THREADS - 1) / MS_EVAL_THREADS, want), MS_MAX_SLICES);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c_step = {};
+  c_step.gridDim = dim3(std::max(1u, S), (unsigned)d->L);
+  c_step.blockDim = dim3(MS_EVAL_THREADS);
+  c_step.dynamicSmemBytes = 0;
+  c_step.stream = st;
+  c_step.attrs = pdl;
+  c_step.numAttrs = 1;
   for (int step = 0; step < m; ++step)
-    mask_step_kernel<<<dim3(std::max(1u, S), (unsigned)d->L), MS_EVAL_THREADS, 0, st>>>(
-        stats, R, d->L, run, taken, part, counter, step, mask_out, quality_out);
+    if (cudaLaunchKernelEx(&c_step, mask_step_kernel, (const double*)stats, R, d->L, run, taken, part, counter, step,
+                           mask_out, quality_out) != cudaSuccess)
+      return MOER_ECUDA;
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
