@@ -55,6 +55,7 @@ constexpr int SP_EMBED_THREADS = 1024;
 constexpr int SP_GROUP_THREADS = 256;
 constexpr int SP_MAX_STEPS = 100;
 constexpr int SP_LU_SLOTS = 8;  // eigenvectors whose inverse iterations run at once (a warp each)
+constexpr int SP_MS_POINTS = 16;  // multisection trial points per eigenvalue (a lane each)
 
 
 __device__ __forceinline__ double sp_warp_sum(double v) {
@@ -103,9 +104,10 @@ __device__ __forceinline__ int sp_sturm(const double* dg, const double* e2, int 
 //     v = x - alpha e_1 with alpha = -sign(x_0) |x|, beta = 2 / v.v; the
 //     trailing block becomes A - v w^T - w v^T with p = beta A v,
 //     w = p - (beta v.p / 2) v).  v is kept in row k right of the diagonal.
-//   * The G largest eigenvalues of T by multisection: warp j brackets the
-//     (j+1)-th largest between Gershgorin bounds and narrows the bracket 33-fold
-//     per step with a Sturm count at 32 points (one per lane).
+//   * The G largest eigenvalues of T by multisection: a group of sixteen lanes
+//     brackets the (j+1)-th largest between Gershgorin bounds and narrows the
+//     bracket 17-fold per step with Sturm counts at sixteen points (one per
+//     lane), two eigenvalues per warp.
 //   * Their eigenvectors by inverse iteration on T (LU with partial pivoting,
 //     three solves from a fixed start vector; after each solve, in eigenvalue
 //     order, re-orthogonalised against the earlier vectors whose eigenvalues
@@ -242,25 +244,40 @@ __global__ void __launch_bounds__(SP_EMBED_THREADS, 1)
   const double eps = 2.220446049250313e-16;
   const double tn = red[2];
   const double pivmin = eps * tn + 1e-300;
-  // ---- the G largest eigenvalues by multisection, warp j for the (j+1)-th
-  if (warp < G) {
-    const int j = n - 1 - warp;  // eigenvalues below it: j
-    double lo = -tn - pivmin, hi = tn + pivmin;
-    for (int it = 0; it < 64; ++it) {
-      const double x = lo + (hi - lo) * ((double)(lane + 1) / 33.0);
-      const int cnt = sp_sturm(dg, pw, n, x);
-      const unsigned above = __ballot_sync(FULL, cnt > j);
-      if (above == 0u) {
-        lo = __shfl_sync(FULL, x, 31);
-      } else {
-        const int f = __ffs(above) - 1;
-        const double xf = __shfl_sync(FULL, x, f), xp = __shfl_sync(FULL, x, f > 0 ? f - 1 : 0);
-        hi = xf;
-        if (f > 0) lo = xp;
+  // ---- the G largest eigenvalues by multisection: lanes in groups of
+  //      SP_MS_POINTS, group e (warp e / groups-per-warp) for the (e+1)-th
+  //      largest, a trial point per lane.  Two eigenvalues share a warp: half
+  //      the warps of one per warp (32 points), for 4.1 rather than 5 bits a
+  //      step; the counts of fewer warps contend less for the fp64 pipe.
+  {
+    constexpr int P = SP_MS_POINTS, GPW = 32 / SP_MS_POINTS;
+    const int ev = warp * GPW + lane / P, sub = lane % P, base = lane - sub;
+    if (warp * GPW < G) {
+      const bool act = ev < G;
+      const int j = n - 1 - ev;  // eigenvalues below the (ev+1)-th largest
+      double lo = -tn - pivmin, hi = tn + pivmin;
+      bool done = !act;
+      for (int it = 0; it < 256; ++it) {
+        const double x = lo + (hi - lo) * ((double)(sub + 1) / (double)(P + 1));
+        const int cnt = act ? sp_sturm(dg, pw, n, x) : 0;
+        const unsigned gb = (__ballot_sync(FULL, act && cnt > j) >> base) & ((1u << P) - 1u);
+        const int f = gb ? __ffs(gb) - 1 : 0;
+        const double xl = __shfl_sync(FULL, x, base + P - 1);
+        const double xf = __shfl_sync(FULL, x, base + f);
+        const double xp = __shfl_sync(FULL, x, base + (f > 0 ? f - 1 : 0));
+        if (!done) {
+          if (gb == 0u) {
+            lo = xl;
+          } else {
+            hi = xf;
+            if (f > 0) lo = xp;
+          }
+          done = hi - lo <= 2.0 * eps * fmax(fabs(lo), fabs(hi)) + pivmin;
+        }
+        if (__all_sync(FULL, done)) break;
       }
-      if (hi - lo <= 2.0 * eps * fmax(fabs(lo), fabs(hi)) + pivmin) break;
+      if (act && sub == 0) lam[ev] = 0.5 * (lo + hi);
     }
-    if (lane == 0) lam[warp] = 0.5 * (lo + hi);
   }
   __syncthreads();
   // ---- inverse iteration, up to SP_LU_SLOTS eigenvectors at once: warp w
