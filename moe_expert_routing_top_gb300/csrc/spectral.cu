@@ -33,7 +33,7 @@
 //     not an option either: the co-activation spectra of real layers are
 //     nearly degenerate just below the leading eigenvalues, where it needs
 //     10^4 - 10^5 steps.
-//   * spec_group_kernel, one CTA per (grid point, layer), four per SM: the
+//   * spec_group_kernel, one CTA per (grid point, layer), six per SM: the
 //     size-bounded assignment is a transportation problem with lower and upper
 //     bounds; the CTA keeps a feasible assignment and cancels negative cycles of
 //     the residual graph collapsed onto the G groups plus one slack node t
@@ -651,7 +651,7 @@ __device__ void sp_assign(const double* cost, int E, int G, int lo, int hi, int*
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(SP_GROUP_THREADS, 4)
+__global__ void __launch_bounds__(SP_GROUP_THREADS, 6)
     spec_group_kernel(const int32_t* __restrict__ affinity, int E, int G, const double* __restrict__ Uo,
                       const double* __restrict__ deg, int32_t* __restrict__ groups, double* __restrict__ ucurve,
                       double* __restrict__ scurve, uint32_t* status) {
