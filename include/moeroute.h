@@ -308,7 +308,8 @@ MOER_API moer_status moer_replication_plan(const moer_dims* d, const int64_t* W,
  * quality_out [m] fp64 or NULL: quality after each addition.
  * Limits: 1 <= m <= L, R >= 1.
  * ws       at least moer_mask_select_workspace_bytes(d, R) bytes, 256-byte
- *          aligned (status word, per (request, layer) sums, running sums).
+ *          aligned (status word, per (request, layer) sums, running sums,
+ *          per-step partial sums and a step counter, zeroed by the call).
  */
 MOER_API size_t moer_mask_select_workspace_bytes(const moer_dims* d, int32_t R);
 MOER_API moer_status moer_mask_select(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* req_off,
@@ -339,8 +340,10 @@ MOER_API moer_status moer_mask_select(const moer_dims* d, const uint8_t* topk, i
  * objective  [1] fp64 out or NULL: sum of squared distances of the points to
  *            their returned centroids.
  * ws         at least moer_kmeans_workspace_bytes(N, dim, D) bytes, 256-byte
- *            aligned (status word, fp64 distances and centroids, previous
- *            assignment).  Launches 3 * max_iter + 3 kernels; steps after
+ *            aligned (status word, fp64 distances, centroids and their norm
+ *            partials, previous assignment, member lists, gain keys).
+ *            Launches 3 * max_iter + 3 kernels, chained by programmatic
+ *            dependent launch on the caller's stream; steps after
  *            convergence return at once.
  */
 MOER_API size_t moer_kmeans_workspace_bytes(int32_t N, int32_t dim, int32_t D);
