@@ -123,18 +123,24 @@ MOER_API moer_status moer_topk_signature(const moer_dims* d, const float* logits
  * Arguments and results are those of moer_topk_signature, without ws.
  * The caller still passes every input and output.
  *  - With topk == NULL and blk_cnt requested, m * T * k must not exceed
- *    32 MiB, else MOER_ENOMEM is returned and nothing is launched.  With a
- *    topk buffer the size limit does not apply.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current.  Make that first call
- *    before any stream capture.
+ *    MOER_NOALLOC_IDS_BYTES, else MOER_ENOMEM is returned and nothing is
+ *    launched.  With a topk buffer the size limit does not apply.
+ *  - The first call in a CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress) with that context current, and keeps it for that
+ *    context only; a context created later (after cudaDeviceReset, say)
+ *    gets its own look-up.  Make the first call in each context before any
+ *    stream capture.
  *  - Every call on a device shares the one array; each call clears the
  *    status part before use.  Calls whose kernels overlap on the GPU (for
  *    example on different streams without ordering) race on it.
- *  - Malformed block-table entries are skipped as in moer_topk_signature,
- *    but their MOER_EDATA status is not readable from the host; use
- *    moer_topk_signature with a workspace when that report is needed.
+ *  - The device-side statuses are not readable from the host: malformed
+ *    block-table entries are skipped as in moer_topk_signature (MOER_EDATA
+ *    there), and a bounded device wait that expires (MOER_ETIMEOUT there)
+ *    leaves that part of the top-k ids, block counts or co-activation
+ *    unwritten, both without a report.  Use moer_topk_signature with a
+ *    workspace when those reports are needed.
  */
+#define MOER_NOALLOC_IDS_BYTES (32u << 20)
 MOER_API moer_status moer_topk_signature_noalloc(const moer_dims* d, const float* logits, int64_t T,
                                                  const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
                                                  uint8_t* blk_cnt, int32_t* affinity,
@@ -157,29 +163,23 @@ MOER_API moer_status moer_topk_signature_noalloc(const moer_dims* d, const float
  * blk_cnt [nblk][m][E] uint8; blk_tab [nblk][2] (tok0, len) as above;
  * req_blk_off [R+1] int32; cache [nslots][m][E] uint8 (in/out) or NULL
  * together with cache_idx [ncached], req_cache_off [R+1] and
- * insert_slot [nblk] (all NULL when there is no cache);
- * req_cnt [R][m][E] int32 (overwritten).  Slot ids outside [0, nslots)
- * are skipped and recorded as MOER_EDATA in ws (ws may be NULL: then
- * they are skipped silently).
+ * insert_slot [nblk] (all NULL, and ncached 0, when there is no cache;
+ * cache_idx may be NULL when ncached is 0); req_cnt [R][m][E] int32
+ * (overwritten).  Device data is checked as it is read: a request whose
+ * block range is not within [0, nblk) or whose cached range
+ * [req_cache_off[r], req_cache_off[r+1]) is not within [0, ncached) has
+ * that part skipped, and a slot id outside [0, nslots) is skipped; each is
+ * recorded as MOER_EDATA in ws (ws may be NULL: then they are skipped
+ * silently).
  */
 MOER_API moer_status moer_block_stitch(const moer_dims* d, const uint8_t* blk_cnt,
                               const int32_t* blk_tab, int32_t nblk,
                               const int32_t* req_blk_off, int32_t R,
-                              const int32_t* cache_idx, const int32_t* req_cache_off,
+                              const int32_t* cache_idx, int32_t ncached, const int32_t* req_cache_off,
                               uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
                               int32_t* req_cnt, void* ws, size_t ws_bytes,
                               moer_stream_t stream);
 
-/* Expert and group loads and load skew from the affinity matrices.
- *   [GRACE] section 4 "Method" (load statistics from profiling), section 4.2
- *   "Expert replication" (rho = W_max / W_mean) and section 7 glossary.
- * affinity [L][E][E] int32; group_of [L][E] int32 in [0, G).
- * W_expert [L][E] int64 = affinity[l][e][e];
- * W_group  [L][G] int64 = sum of W_expert over the group's experts;
- * rho_group [L] fp64 = max_g W_group / (sum_g W_group / G), 0 if the sum is 0;
- * rho_expert [L] fp64 = the same over the E experts.  Any output may be NULL.
- * Group ids outside [0, G) are skipped.
- */
 MOER_API moer_status moer_affinity_load(const moer_dims* d, const int32_t* affinity,
                                const int32_t* group_of, int32_t G, int64_t* W_expert,
                                int64_t* W_group, double* rho_group, double* rho_expert,

@@ -50,7 +50,7 @@ def _load():
         "moer_workspace_bytes": ([dp, i64, i32, i32, i32], sz),
         "moer_topk_signature": ([dp, vp, i64, vp, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_topk_signature_noalloc": ([dp, vp, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
-        "moer_block_stitch": ([dp, vp, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp],
+        "moer_block_stitch": ([dp, vp, vp, i32, vp, i32, vp, i32, vp, vp, i32, vp, vp, vp, sz, vp],
                               ctypes.c_int),
         "moer_affinity_load": ([dp, vp, vp, i32, vp, vp, vp, vp, vp], ctypes.c_int),
         "moer_route": ([dp, vp, i32, vp, vp, i32, f32, vp, i32, vp, vp, vp, vp, sz, vp],
@@ -128,11 +128,11 @@ def moer_topk_signature_noalloc(dims, logits, T, blk_tab, nblk, topk, blk_cnt, a
         _ptr(blk_cnt), _ptr(affinity), _stream(stream)))
 
 
-def moer_block_stitch(dims, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, req_cache_off,
+def moer_block_stitch(dims, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, ncached, req_cache_off,
                       cache, nslots, insert_slot, req_cnt, ws, ws_bytes, stream=None) -> None:
     _check("moer_block_stitch", LIB.moer_block_stitch(
         ctypes.byref(dims), _ptr(blk_cnt), _ptr(blk_tab), int(nblk), _ptr(req_blk_off), int(R),
-        _ptr(cache_idx), _ptr(req_cache_off), _ptr(cache), int(nslots), _ptr(insert_slot),
+        _ptr(cache_idx), int(ncached), _ptr(req_cache_off), _ptr(cache), int(nslots), _ptr(insert_slot),
         _ptr(req_cnt), _ptr(ws), int(ws_bytes), _stream(stream)))
 
 

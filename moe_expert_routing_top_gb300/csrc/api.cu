@@ -27,7 +27,7 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
                                   uint8_t* blk_cnt, int32_t* affinity, void* ws, cudaStream_t st);
 moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, const int32_t* blk_tab,
                                 int32_t nblk, const int32_t* req_blk_off, int32_t R,
-                                const int32_t* cache_idx, const int32_t* req_cache_off,
+                                const int32_t* cache_idx, int32_t ncached, const int32_t* req_cache_off,
                                 uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
                                 int32_t* req_cnt, uint32_t* status, cudaStream_t st);
 moer_status affinity_load_launch(const moer_dims* d, const int32_t* affinity, const int32_t* group_of,
@@ -133,25 +133,26 @@ moer_status moer_topk_signature(const moer_dims* d, const float* logits, int64_t
 
 moer_status moer_block_stitch(const moer_dims* d, const uint8_t* blk_cnt, const int32_t* blk_tab,
                               int32_t nblk, const int32_t* req_blk_off, int32_t R,
-                              const int32_t* cache_idx, const int32_t* req_cache_off,
+                              const int32_t* cache_idx, int32_t ncached, const int32_t* req_cache_off,
                               uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
                               int32_t* req_cnt, void* ws, size_t ws_bytes, moer_stream_t stream) {
   moer_status s = check_dims(d, true);
   if (s != MOER_OK) return s;
   if (d->m < 1) return MOER_ERANGE;
-  if (R < 0 || nblk < 0 || nslots < 0) return MOER_ERANGE;
+  if (R < 0 || nblk < 0 || nslots < 0 || ncached < 0) return MOER_ERANGE;
   if (R == 0) return MOER_OK;
   if (req_blk_off == nullptr || req_cnt == nullptr) return MOER_EINVAL;
   if (nblk > 0 && (blk_cnt == nullptr || !aligned(blk_cnt, 4))) return MOER_EINVAL;
   const bool has_cache = cache != nullptr;
   if (has_cache) {
     if (!aligned(cache, 4) || req_cache_off == nullptr) return MOER_EINVAL;
+    if (ncached > 0 && cache_idx == nullptr) return MOER_EINVAL;
     if (insert_slot != nullptr && blk_tab == nullptr) return MOER_EINVAL;
-  } else if (cache_idx != nullptr || req_cache_off != nullptr || insert_slot != nullptr) {
+  } else if (cache_idx != nullptr || req_cache_off != nullptr || insert_slot != nullptr || ncached != 0) {
     return MOER_EINVAL;
   }
   if (ws != nullptr && (!aligned(ws, 16) || ws_bytes < WS_HEADER)) return MOER_ENOMEM;
-  return block_stitch_launch(d, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, req_cache_off,
+  return block_stitch_launch(d, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, ncached, req_cache_off,
                              cache, nslots, insert_slot, req_cnt,
                              ws ? reinterpret_cast<uint32_t*>(ws) : nullptr,
                              reinterpret_cast<cudaStream_t>(stream));

@@ -20,8 +20,6 @@ constexpr unsigned FULL = 0xffffffffu;
 // gate GEMM's tile counter (zeroed by each moer_gate_topk call).
 constexpr size_t WS_HEADER = 256;
 constexpr size_t WS_TILE_CTR = 128;
-// Capacity of moer_topk_signature_noalloc's fixed scratch for staged top-k ids.
-#define MOER_NOALLOC_IDS_BYTES (32u << 20)
 constexpr uint32_t WS_BIT_EDATA = 1u;
 constexpr uint32_t WS_BIT_ETIMEOUT = 2u;
 

@@ -8,9 +8,10 @@
 // them the scratch that moer_topk_signature takes as a caller workspace lives
 // here, in one fixed-size array in device memory that every GPU loading this
 // library holds until the process exits.
-#include <mutex>
+#include <cuda.h>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 
 namespace moer {
 
@@ -27,22 +28,56 @@ static __device__ __align__(256) uint8_t noalloc_scratch[WS_HEADER + MOER_NOALLO
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_ptr[kMaxDevices] = {nullptr};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the host-side symbol is not a device address).
-void* scratch_on_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ptr[dev] == nullptr) {
+// The driver's cuCtxGetCurrent and cuCtxGetId, resolved through the runtime
+// (the library does not link libcuda directly).
+struct CtxApi {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const CtxApi& ctx_api() {
+  static const CtxApi api = []() {
+    CtxApi a;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.get_id = reinterpret_cast<CtxGetIdFn>(f);
+    return a;
+  }();
+  return api;
+}
+
+// ID of the context current on this thread; false when there is none yet.
+bool current_context_id(unsigned long long* id) {
+  const CtxApi& a = ctx_api();
+  if (a.get_current == nullptr || a.get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (a.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return a.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+CtxAddressCache<64> g_scratch_addr;
+
+bool lookup_scratch(void** p) { return cudaGetSymbolAddress(p, noalloc_scratch) == cudaSuccess; }
+
+// Device address of the scratch array in the current context (the host-side
+// symbol is not a device address), looked up once per context.
+void* scratch_in_current_context() {
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) {
+    // No context is current on this thread yet: the runtime's look-up makes
+    // the current device's primary context current, then it has an ID.
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, noalloc_scratch) != cudaSuccess) return nullptr;
-    g_ptr[dev] = p;
+    if (!lookup_scratch(&p) || !current_context_id(&id)) return nullptr;
   }
-  return g_ptr[dev];
+  return g_scratch_addr.get(id, lookup_scratch);
 }
 
 }  // namespace
@@ -59,7 +94,7 @@ extern "C" MOER_API moer_status moer_topk_signature_noalloc(const moer_dims* d, 
   if (topk == nullptr && blk_cnt != nullptr && d->m > 0 &&
       (uint64_t)d->m * (uint64_t)T * (uint64_t)d->k > (uint64_t)MOER_NOALLOC_IDS_BYTES)
     return MOER_ENOMEM;
-  void* ws = scratch_on_current_device();
+  void* ws = scratch_in_current_context();
   if (ws == nullptr) return MOER_ECUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the status word must start at zero; earlier calls left their contents

@@ -57,14 +57,17 @@ __device__ __forceinline__ void accv(uint32_t (&a)[16], uint4 v) {
 // blocks, four block loads in flight at a time.
 template <typename V, int NB>
 __global__ void stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t* __restrict__ req_blk_off,
-                           const int32_t* __restrict__ cache_idx, const int32_t* __restrict__ req_cache_off,
-                           const V* __restrict__ cache_w, int nslots, int rec_v, int32_t* __restrict__ req_cnt,
-                           uint32_t* status) {
+                           const int32_t* __restrict__ cache_idx, int ncached,
+                           const int32_t* __restrict__ req_cache_off, const V* __restrict__ cache_w, int nslots,
+                           int rec_v, int32_t* __restrict__ req_cnt, uint32_t* status) {
   const int r = blockIdx.x;
   const int b0 = req_blk_off[r], b1 = req_blk_off[r + 1];
-  const int c0 = cache_w ? req_cache_off[r] : 0, c1 = cache_w ? req_cache_off[r + 1] : 0;
+  int c0 = cache_w ? req_cache_off[r] : 0, c1 = cache_w ? req_cache_off[r + 1] : 0;
   const bool bad_blocks = b0 < 0 || b1 < b0 || b1 > nblk;
-  if (bad_blocks && threadIdx.x == 0 && status != nullptr) atomicOr(status, WS_BIT_EDATA);
+  // a cached-prefix range outside [0, ncached) is skipped whole, like a bad block range
+  const bool bad_cache = c0 < 0 || c1 < c0 || c1 > ncached;
+  if ((bad_blocks || bad_cache) && threadIdx.x == 0 && status != nullptr) atomicOr(status, WS_BIT_EDATA);
+  if (bad_cache) c0 = c1 = 0;
   for (int w = threadIdx.x; w < rec_v; w += blockDim.x) {
     uint32_t a[NB];
 #pragma unroll
@@ -104,7 +107,7 @@ __global__ void stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t*
 
 moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, const int32_t* blk_tab,
                                 int32_t nblk, const int32_t* req_blk_off, int32_t R,
-                                const int32_t* cache_idx, const int32_t* req_cache_off,
+                                const int32_t* cache_idx, int32_t ncached, const int32_t* req_cache_off,
                                 uint8_t* cache, int32_t nslots, const int32_t* insert_slot,
                                 int32_t* req_cnt, uint32_t* status, cudaStream_t st) {
   const int rec_bytes = d->m * d->E;
@@ -129,13 +132,13 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
     const int rec_v = rec_bytes / 16;
     const int threads = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
     stitch_sum<uint4, 16><<<R, threads, 0, st>>>(reinterpret_cast<const uint4*>(blk_cnt), nblk, req_blk_off,
-                                                 cache_idx, req_cache_off, reinterpret_cast<const uint4*>(cache),
+                                                 cache_idx, ncached, req_cache_off, reinterpret_cast<const uint4*>(cache),
                                                  nslots, rec_v, req_cnt, status);
   } else {
     const int rec_v = rec_bytes / 4;
     const int threads = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
     stitch_sum<uint32_t, 4><<<R, threads, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), nblk, req_blk_off,
-                                                   cache_idx, req_cache_off,
+                                                   cache_idx, ncached, req_cache_off,
                                                    reinterpret_cast<const uint32_t*>(cache), nslots, rec_v,
                                                    req_cnt, status);
   }

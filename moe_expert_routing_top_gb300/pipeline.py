@@ -38,6 +38,7 @@ class BatchDev:
     cache_idx: Optional[torch.Tensor]
     req_cache_off: Optional[torch.Tensor]
     insert_slot: Optional[torch.Tensor]
+    ncached: int = 0
 
     @staticmethod
     def from_host(b, device="cuda", with_cache=True, pin=False) -> "BatchDev":
@@ -51,7 +52,8 @@ class BatchDev:
                         req_blk_off=t(b.req_blk_off),
                         cache_idx=ci if with_cache else None,
                         req_cache_off=t(b.req_cache_off) if with_cache else None,
-                        insert_slot=t(b.insert_slot) if with_cache else None)
+                        insert_slot=t(b.insert_slot) if with_cache else None,
+                        ncached=int(len(b.cache_idx)) if with_cache else 0)
 
 
 class RoutingStats:
@@ -131,6 +133,7 @@ class RoutingStats:
         use_cache = self.cache is not None and bd.req_cache_off is not None
         nat.moer_block_stitch(self.dims, self.blk_cnt, bd.blk_tab, bd.nblk, bd.req_blk_off, bd.R,
                               bd.cache_idx if use_cache else None,
+                              bd.ncached if use_cache else 0,
                               bd.req_cache_off if use_cache else None,
                               self.cache if use_cache else None, self.nslots,
                               bd.insert_slot if use_cache else None, self.req_cnt, self.ws,

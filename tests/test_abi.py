@@ -83,8 +83,11 @@ def test_bad_pointers_and_sizes(nat):
     assert _code(r, d, 64, 10, 64, 64, 16, 0.1, 64, 2, None, None, 64, None, 0, 0) == 1
     assert _code(r, d, 64, 10, 64, 64, 16, 0.1, 64, 1, None, None, 64, None, 0, 0) == 1  # live, no ws
     s = nat.moer_block_stitch
-    assert _code(s, d, 64, 64, 10, None, 5, None, None, None, 0, None, 64, None, 0, 0) == 1
-    assert _code(s, d, 64, 64, 10, 64, 5, 64, None, None, 0, None, 64, None, 0, 0) == 1  # idx w/o cache
+    assert _code(s, d, 64, 64, 10, None, 5, None, 0, None, None, 0, None, 64, None, 0, 0) == 1
+    assert _code(s, d, 64, 64, 10, 64, 5, 64, 1, None, None, 0, None, 64, None, 0, 0) == 1  # idx w/o cache
+    assert _code(s, d, 64, 64, 10, 64, 5, None, 3, 64, 64, 4, None, 64, None, 0, 0) == 1   # ncached, no idx
+    assert _code(s, d, 64, 64, 10, 64, 5, 64, -1, 64, 64, 4, None, 64, None, 0, 0) == 3    # ncached < 0
+    assert _code(s, d, 64, 64, 10, 64, 5, None, 2, None, None, 0, None, 64, None, 0, 0) == 1  # ncached w/o cache
     nat.moer_topk_signature(d, 64, 0, None, 0, None, None, None, 64, ws, 0)  # T = 0: no-op
 
 

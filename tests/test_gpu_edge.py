@@ -169,6 +169,32 @@ def test_stitch_bad_slot_is_reported(env):
     ins = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
     out = torch.empty((1, m, E), dtype=torch.int32, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    nat.moer_block_stitch(dims, blk, tab, 2, rbo, 1, cidx, rco, cache, 3, ins, out, ws, 256)
+    nat.moer_block_stitch(dims, blk, tab, 2, rbo, 1, cidx, 1, rco, cache, 3, ins, out, ws, 256)
     assert nat.moer_ws_status(ws) == 6
     assert (out == 2).all()
+
+
+@pytest.mark.parametrize("rco_vals", [[0, 5], [-1, 1], [1, 0]])
+def test_stitch_bad_cache_offsets_are_reported(env, rco_vals):
+    """A request whose cached-prefix range is not within [0, ncached) has its cached part
+    skipped (its computed blocks are still summed) and MOER_EDATA is recorded; no cache_idx
+    entry outside the buffer is read."""
+    torch, nat = env
+    E, m = 64, 1
+    dims = nat.make_dims(E, 8, 1, [0], 16)
+    blk = torch.ones((2, m, E), dtype=torch.uint8, device="cuda")
+    tab = torch.tensor([0, 16, 16, 16], dtype=torch.int32, device="cuda")
+    rbo = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
+    cache = torch.full((3, m, E), 9, dtype=torch.uint8, device="cuda")
+    cidx = torch.tensor([1], dtype=torch.int32, device="cuda")      # one cached block
+    rco = torch.tensor(rco_vals, dtype=torch.int32, device="cuda")
+    out = torch.empty((1, m, E), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    nat.moer_block_stitch(dims, blk, tab, 2, rbo, 1, cidx, 1, rco, cache, 3, None, out, ws, 256)
+    assert nat.moer_ws_status(ws) == 6
+    assert (out == 2).all()                                         # computed blocks only
+    # the well-formed range sums the cached block too, and reports nothing
+    rco = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    nat.moer_block_stitch(dims, blk, tab, 2, rbo, 1, cidx, 1, rco, cache, 3, None, out, ws, 256)
+    assert nat.moer_ws_status(ws) == 0
+    assert (out == 11).all()
