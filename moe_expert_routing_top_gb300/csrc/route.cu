@@ -46,8 +46,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // Decoder choice from D distances: d_min, band {q : d_q <= d_min + tau}, the
-// smallest load in the band, ties to the lowest index.  Sequential form used
-// by the static path (one thread).
+// smallest load in the band, ties to the lowest index.  NaN distances are
+// outside the band and take no part in d_min (fminf skips them); with no
+// finite distance the band is empty and the choice is -1.  Sequential form
+// used by the static path (one thread).
 __device__ __forceinline__ int band_pick(const float* dist, int D, float tau, const int32_t* loads) {
   float dmin = dist[0];
   for (int q = 1; q < D; ++q) dmin = fminf(dmin, dist[q]);
@@ -135,7 +137,13 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_live(const float* __restr
         const float d0 = lane < D ? b[i * D + lane] : FLT_MAX;
         const float d1 = lane + 32 < D ? b[i * D + lane + 32] : FLT_MAX;
         // distances are non-negative, so their bit patterns order as integers
-        const int dm = __reduce_min_sync(FULL, min(__float_as_int(d0), __float_as_int(d1)));
+        // (+inf included); a NaN distance and an absent decoder take no part
+        // in d_min (as fminf in band_pick)
+        const int k0 = (lane < D && !isnan(d0)) ? __float_as_int(d0) : INT_MAX;
+        const int k1 = (lane + 32 < D && !isnan(d1)) ? __float_as_int(d1) : INT_MAX;
+        const int dm = __reduce_min_sync(FULL, min(k0, k1));
+        // every distance NaN: dm stays INT_MAX, a NaN pattern, so thr is NaN
+        // and the band is empty
         const float thr = __fadd_rn(__int_as_float(dm), tau);
         const bool in0 = lane < D && d0 <= thr;
         const bool in1 = lane + 32 < D && d1 <= thr;
@@ -143,9 +151,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_live(const float* __restr
         const int lm = __reduce_min_sync(FULL, min(c0, c1));
         const unsigned b0 = __ballot_sync(FULL, in0 && ld0 == lm);
         const unsigned b1 = __ballot_sync(FULL, in1 && ld1 == lm);
-        const int q = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        // empty band (no finite distance): no decoder, loads unchanged
+        const int q = b0 ? __ffs(b0) - 1 : (b1 ? 32 + __ffs(b1) - 1 : -1);
         if (lane == 0) choice[r0 + i] = q;
-        if (lane == (q & 31)) {
+        if (q >= 0 && lane == (q & 31)) {
           if (q < 32)
             ld0 += 1;
           else

@@ -213,6 +213,9 @@ void orc_sig_dist(const int32_t* req_cnt, int R, const float* idf, int m, int E,
  * (additive band); choice = the band member with the smallest load, ties to
  * the lowest decoder index.  Live mode takes requests in arrival order and
  * adds one routed request to the chosen decoder's load after each decision.
+ * The pages do not consider undefined distances; reading: a NaN distance is
+ * outside the band and does not take part in d_min, and a request with no
+ * finite distance gets no decoder (-1) and changes no load.
  */
 void orc_route(const double* dist, int R, int D, double tau,
                const int32_t* loads_in, int live, int32_t* choice,
@@ -221,9 +224,10 @@ void orc_route(const double* dist, int R, int D, double tau,
   memcpy(load, loads_in, sizeof(int32_t) * (size_t)D);
   for (int r = 0; r < R; ++r) {
     const double* d = dist + (size_t)r * (size_t)D;
-    double dmin = d[0];
-    for (int q = 1; q < D; ++q)
-      if (d[q] < dmin) dmin = d[q];
+    /* NaN distances are outside the band and do not define d_min */
+    double dmin = NAN;
+    for (int q = 0; q < D; ++q)
+      if (!isnan(d[q]) && (isnan(dmin) || d[q] < dmin)) dmin = d[q];
     int best = -1;
     for (int q = 0; q < D; ++q) {
 #if ORACLE_MUTANT == 7 /* mutant: band test dropped (pure least-loaded) */
@@ -235,7 +239,8 @@ void orc_route(const double* dist, int R, int D, double tau,
       if (best < 0 || load[q] < load[best]) best = q;
     }
     choice[r] = best;
-    if (live) load[best] += 1;
+    /* no finite distance: the band is empty, no decoder is chosen */
+    if (live && best >= 0) load[best] += 1;
   }
   if (loads_out) memcpy(loads_out, load, sizeof(int32_t) * (size_t)D);
   free(load);

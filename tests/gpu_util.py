@@ -40,14 +40,18 @@ def assert_close(gpu, ref, what):
 
 
 def band_edge_rows(dist_ref, tau):
-    """Requests whose oracle distances put some decoder within BAND_EDGE of the band edge."""
-    dmin = dist_ref.min(axis=1, keepdims=True)
+    """Requests whose oracle distances put some decoder within BAND_EDGE of the band edge
+    (NaN distances are outside every band and do not define the minimum)."""
+    with np.errstate(invalid="ignore"):
+        dmin = np.fmin.reduce(dist_ref, axis=1, keepdims=True)
     return (np.abs(dist_ref - (dmin + tau)) <= BAND_EDGE).any(axis=1)
 
 
 def valid_choice(q, dist_row, tau, loads):
     """True if q is the tau-band least-loaded pick for some band between the edge tolerances."""
-    dmin = dist_row.min()
+    if q < 0:
+        return bool(np.isnan(dist_row).all())
+    dmin = np.fmin.reduce(dist_row)
     hi = dist_row <= dmin + tau + BAND_EDGE
     lo = dist_row <= dmin + tau - BAND_EDGE
     if not hi[q]:

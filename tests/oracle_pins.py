@@ -178,6 +178,27 @@ def pin_route(orc):
         assert ch[r] in band and cur[ch[r]] == cur[band].min()
         assert ch[r] == band[np.argmin(cur[band])]
         cur[ch[r]] += 1
+    # undefined distances: a NaN is outside the band and does not define d_min (numpy's
+    # nanmin); a request without any finite distance gets -1 and leaves every load alone
+    dn = dist[:6].copy()
+    dn[0, 0] = np.nan                      # NaN first: d_min from the other six
+    dn[1, 3] = np.nan
+    dn[2, :] = np.nan                      # no finite distance
+    dn[3, :] = np.inf                      # all infinite: every decoder is in the band
+    for live in (False, True):
+        ch, out = orc.route(dn, 0.1, loads, live=live)
+        cur = loads.copy()
+        for r in range(6):
+            if r == 2:
+                assert ch[r] == -1
+                continue
+            with np.errstate(invalid="ignore"):
+                band = np.flatnonzero(dn[r] <= np.nanmin(dn[r]) + 0.1)
+            assert ch[r] == band[np.argmin(cur[band])]
+            if live:
+                cur[ch[r]] += 1
+        assert np.array_equal(out, cur)
+    assert orc.route(dn[3:4], 0.1, loads, live=False)[0][0] == np.argmin(loads)
 
 
 def pin_affinity(orc):

@@ -92,3 +92,37 @@ def test_route_degenerate_settings(env, tau, D, live, equal):
         assert (ch[off] == odist.argmin(axis=1)[off]).all()
     if tau >= 1e6 and not live:                                  # least loaded, lowest index on ties
         assert (ch == int(np.lexsort((np.arange(D), loads0))[0])).all()
+
+
+@pytest.mark.parametrize("live", [False, True])
+def test_route_undefined_distances(env, live):
+    """Centroids with NaN entries give NaN distances to those decoders: they are outside the band
+    and take no part in d_min; with every centroid NaN no decoder is chosen (-1) and no load
+    changes.  Static and live mode agree with the oracle on both."""
+    orc = oracle.get()
+    R, m, E, D = 64, 2, 64, 8
+    cnt, idf, cen = _inputs(77, R, m, E, D)
+    loads0 = np.random.RandomState(5).randint(0, 8, size=D).astype(np.int32)
+    cen_nan = cen.copy()
+    cen_nan[0, 3] = np.nan                                       # decoder 0: NaN distance
+    cen_nan[5, :] = np.nan                                       # decoder 5: NaN distance
+    sig, dist, ch, loads = _run(env, cnt, idf, cen_nan, 0.1, loads0, live)
+    assert np.isnan(dist[:, 0]).all() and np.isnan(dist[:, 5]).all()
+    _, odist = orc.sig_dist(cnt, idf, cen_nan)
+    keep = [q for q in range(D) if q not in (0, 5)]
+    gu.assert_close(dist[:, keep], odist[:, keep], "distance")
+    och, oloads = orc.route(odist, 0.1, loads0, live)
+    assert not np.isin(ch, [0, 5]).any() and (ch >= 0).all()
+    if live:
+        gu.check_live_route(ch, odist, 0.1, loads0, och)
+        assert np.array_equal(np.bincount(ch, minlength=D) + loads0, loads)
+    else:
+        gu.check_static_route(ch, odist, 0.1, loads0, och)
+    # every centroid NaN: no decoder, loads unchanged
+    cen_all = np.full_like(cen, np.nan)
+    _, dist, ch, loads = _run(env, cnt, idf, cen_all, 0.1, loads0, live)
+    assert np.isnan(dist).all()
+    assert (ch == -1).all()
+    assert np.array_equal(loads, loads0)
+    och, oloads = orc.route(dist.astype(np.float64), 0.1, loads0, live)
+    assert (och == -1).all() and np.array_equal(oloads, loads0)
