@@ -1,0 +1,160 @@
+// rank.cuh -- the ranking of the top-k gate, in one place for every kernel
+// that selects experts (the warp-per-row and thread-per-row logits passes and
+// the gate GEMM's epilogue).
+//
+// The order is the standard top-k gate's (ELDR, section "What it tries to
+// solve": each token keeps the k experts with the largest router logits),
+// made total: larger logit first; equal logits, -0.0 == +0.0 included, rank
+// the lower expert id first; NaN ranks below every number, NaNs among
+// themselves by expert id.
+//
+// Two forms of the order live here:
+//   * exact keys: rank_key() maps a float to a 32-bit unsigned key whose
+//     integer order is the ranking by value (NaN -> 1, the lowest key a
+//     value can take; 0 is reserved for "taken"), and rank_key40() appends
+//     the inverted expert id so that equal values order by id;
+//   * truncated keys for the fast paths: the float's upper 24 bits with an
+//     8-bit inverted position below them, compared as signed ints, sorted
+//     by comparator networks.  These agree with the exact order only on
+//     positive finite values whose truncations differ, which
+//     trunc_top8_uncertain() checks; rows it rejects are redone exactly.
+#pragma once
+
+#include <climits>
+
+#include "common.cuh"
+
+namespace moer {
+
+// ------------------------------------------------------------ exact keys
+__device__ __forceinline__ uint32_t rank_key_bits(uint32_t b) {
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 1u;  // NaN: below every number
+  if (b == 0x80000000u) b = 0u;                      // -0.0 ranks as +0.0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t rank_key(float x) { return rank_key_bits(__float_as_uint(x)); }
+
+// 40-bit key: the value key above the inverted expert id (ties to the lower id).
+__device__ __forceinline__ uint64_t rank_key40(uint32_t bits, int e) {
+  return ((uint64_t)rank_key_bits(bits) << 8) | (uint64_t)(255 - e);
+}
+
+// ------------------------------------------------------- truncated keys
+// The float's upper 24 bits with `low` (an inverted position, < 256) below.
+// (The thread-per-row pass forms the same value with a multiply-high and a
+// multiply-add, to keep it off the integer ALU pipe.)
+__device__ __forceinline__ int trunc_key(uint32_t bits, int low) {
+  return (int)(bits & 0xFFFFFF00u) | low;
+}
+
+// ---------------------------------------------------- comparator networks
+__device__ __forceinline__ void cas(int& a, int& b) {  // a <- max, b <- min
+  const int hi = max(a, b), lo = min(a, b);
+  a = hi;
+  b = lo;
+}
+__device__ __forceinline__ void cas64(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Sorts 8 keys in descending order (19 comparators, depth 6).
+__device__ __forceinline__ void sort8_desc(int (&c)[8]) {
+  cas(c[0], c[2]); cas(c[1], c[3]); cas(c[4], c[6]); cas(c[5], c[7]);
+  cas(c[0], c[4]); cas(c[1], c[5]); cas(c[2], c[6]); cas(c[3], c[7]);
+  cas(c[0], c[1]); cas(c[2], c[3]); cas(c[4], c[5]); cas(c[6], c[7]);
+  cas(c[2], c[4]); cas(c[3], c[5]);
+  cas(c[1], c[4]); cas(c[3], c[6]);
+  cas(c[1], c[2]); cas(c[3], c[4]); cas(c[5], c[6]);
+}
+
+// Sorts a bitonic sequence of 8 keys in descending order (half-cleaners).
+__device__ __forceinline__ void clean8_desc(int (&m)[8]) {
+  cas(m[0], m[4]); cas(m[1], m[5]); cas(m[2], m[6]); cas(m[3], m[7]);
+  cas(m[0], m[2]); cas(m[1], m[3]); cas(m[4], m[6]); cas(m[5], m[7]);
+  cas(m[0], m[1]); cas(m[2], m[3]); cas(m[4], m[5]); cas(m[6], m[7]);
+}
+
+// Folds the losers of a half-cleaner step (mins of T[i] and U[7 - i]) into
+// the running 9th key with 3-input maxima (one ALU op each).
+__device__ __forceinline__ int fold_losers(int L9, const int (&lo)[8]) {
+  const int a = __vimax3_s32(lo[0], lo[1], lo[2]);
+  const int b = __vimax3_s32(lo[3], lo[4], lo[5]);
+  const int c = __vimax3_s32(lo[6], lo[7], L9);
+  return __vimax3_s32(a, b, c);
+}
+
+// T <- top-8 of T and U (both sorted descending), sorted descending; with
+// WANT9, L9 <- max(L9, 9th key of T and U).
+template <bool WANT9>
+__device__ __forceinline__ void merge8(int (&T)[8], const int (&U)[8], int& L9) {
+  int mrg[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mrg[i] = max(T[i], U[7 - i]);
+  if constexpr (WANT9) {
+    int lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo[i] = min(T[i], U[7 - i]);
+    L9 = fold_losers(L9, lo);
+  }
+  clean8_desc(mrg);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) T[i] = mrg[i];
+}
+
+// True when the truncated-key top-8 T (descending; L9 the best key outside
+// it, used when K == 8) may differ from the exact top-K: a leading key is not
+// a positive finite float (zero, negative, NaN and +-inf all land here), or
+// two of the K + 1 leading keys share their upper 24 bits.
+template <int K>
+__device__ __forceinline__ bool trunc_top8_uncertain(const int (&T)[8], int L9) {
+  static_assert(K >= 1 && K <= 8, "truncated keys serve k <= 8");
+  const int nxt = (K == 8) ? L9 : T[K < 8 ? K : 7];
+  bool bad = (T[K - 1] < 256) || (T[0] >= 0x7F800000);
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const int b = (i + 1 < K) ? T[i + 1] : nxt;
+    bad = bad || (b >= (T[i] & (int)0xFFFFFF00));
+  }
+  return bad;
+}
+
+// ------------------------------------------------------ exact warp path
+// Exact top-k of one row of E <= 32 * EPL logits, any k <= 32, by one warp:
+// lane l holds experts [l * EPL, l * EPL + EPL); k rounds of a warp maximum
+// over exact keys, the lowest lane (hence the lowest id) winning ties.
+// Returns, in lane r < k, the id ranked r-th; -1 in the other lanes.
+template <int EPL>
+__device__ int warp_topk_exact(const float* row, int E, int k, int lane) {
+  uint32_t key[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = lane * EPL + j;
+    key[j] = e < E ? rank_key(row[e]) : 0u;
+  }
+  int myidx = -1;
+  for (int r = 0; r < k; ++r) {
+    uint32_t best = 0u;
+    int bj = 0;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (key[j] > best) {
+        best = key[j];
+        bj = j;
+      }
+    const uint32_t M = __reduce_max_sync(FULL, best);
+    const unsigned bal = __ballot_sync(FULL, best == M);
+    const int w = __ffs(bal) - 1;
+    const int e = __shfl_sync(FULL, lane * EPL + bj, w);
+    if (lane == w) {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (j == bj) key[j] = 0u;
+    }
+    if (lane == r) myidx = e;
+  }
+  return myidx;
+}
+
+}  // namespace moer

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "k1_params.cuh"
+#include "rank.cuh"
 
 namespace moer {
 
@@ -76,50 +77,6 @@ size_t k1_scratch_bytes(const moer_dims* d, int64_t T) {
 }
 
 // ----------------------------------------------------------- row selection
-// Order-preserving 32-bit key of the ranking: NaN lowest (above only the
-// "removed" key 0), -0.0 equal to +0.0, otherwise by value.
-__device__ __forceinline__ uint32_t rank_key(float x) {
-  uint32_t b = __float_as_uint(x);
-  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 1u;
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Exact top-k of one row held in shared memory, any E <= 32*EPL, k <= 32.
-// Lane owns experts [lane*EPL, lane*EPL+EPL).  Returns, in lane r < k, the
-// id ranked r-th; -1 in other lanes.
-template <int EPL>
-__device__ int topk_exact(const float* row, int E, int k, int lane) {
-  uint32_t key[EPL];
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    const int e = lane * EPL + j;
-    key[j] = e < E ? rank_key(row[e]) : 0u;
-  }
-  int myidx = -1;
-  for (int r = 0; r < k; ++r) {
-    uint32_t best = 0u;
-    int bj = 0;
-#pragma unroll
-    for (int j = 0; j < EPL; ++j)
-      if (key[j] > best) {
-        best = key[j];
-        bj = j;
-      }
-    const uint32_t M = __reduce_max_sync(FULL, best);
-    const unsigned bal = __ballot_sync(FULL, best == M);
-    const int w = __ffs(bal) - 1;
-    const int e = __shfl_sync(FULL, lane * EPL + bj, w);
-    if (lane == w) {
-#pragma unroll
-      for (int j = 0; j < EPL; ++j)
-        if (j == bj) key[j] = 0u;
-    }
-    if (lane == r) myidx = e;
-  }
-  return myidx;
-}
-
 // Adds the k*k ordered pairs of one row (ids in lanes r < k) to a counter
 // matrix with row stride `stride`.
 __device__ __forceinline__ void aff_pairs_any(int* aff, int stride, int myidx, int k, int lane) {
@@ -221,7 +178,7 @@ __device__ void k1_consumer(const K1Params& p, char* smem, int64_t i0, int64_t i
     if (p.ids != nullptr && (!p.ids_mask_only || slot >= 0))
       out = p.ids + ((size_t)(p.ids_mask_only ? slot : l) * p.T + tok0) * k;
     for (int r = warp; r < ntok; r += G::CWARPS) {
-      const int myidx = topk_exact<EPL>(stage + (size_t)r * p.E, p.E, k, lane);
+      const int myidx = warp_topk_exact<EPL>(stage + (size_t)r * p.E, p.E, k, lane);
       if (out != nullptr && lane < k) out[(size_t)r * k + lane] = (uint8_t)myidx;
       if (aff_on) {
         if constexpr (G::SMEM_AFF)

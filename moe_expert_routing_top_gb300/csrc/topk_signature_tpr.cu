@@ -46,6 +46,7 @@
 
 #include "common.cuh"
 #include "k1_params.cuh"
+#include "rank.cuh"
 
 namespace moer {
 
@@ -94,66 +95,16 @@ struct TprGeo {
 };
 
 
-// ------------------------------------------------------ comparator networks
-__device__ __forceinline__ void cas(int& a, int& b) {  // a <- max, b <- min
-  const int hi = max(a, b), lo = min(a, b);
-  a = hi;
-  b = lo;
-}
-
-// Sorts 8 keys in descending order (19 comparators, depth 6).
-__device__ __forceinline__ void sort8_desc(int (&c)[8]) {
-  cas(c[0], c[2]); cas(c[1], c[3]); cas(c[4], c[6]); cas(c[5], c[7]);
-  cas(c[0], c[4]); cas(c[1], c[5]); cas(c[2], c[6]); cas(c[3], c[7]);
-  cas(c[0], c[1]); cas(c[2], c[3]); cas(c[4], c[5]); cas(c[6], c[7]);
-  cas(c[2], c[4]); cas(c[3], c[5]);
-  cas(c[1], c[4]); cas(c[3], c[6]);
-  cas(c[1], c[2]); cas(c[3], c[4]); cas(c[5], c[6]);
-}
-
-// Sorts a bitonic sequence of 8 keys in descending order (half-cleaners).
-__device__ __forceinline__ void clean8_desc(int (&m)[8]) {
-  cas(m[0], m[4]); cas(m[1], m[5]); cas(m[2], m[6]); cas(m[3], m[7]);
-  cas(m[0], m[2]); cas(m[1], m[3]); cas(m[4], m[6]); cas(m[5], m[7]);
-  cas(m[0], m[1]); cas(m[2], m[3]); cas(m[4], m[5]); cas(m[6], m[7]);
-}
-
-// Folds the losers of a half-cleaner step (mins of T[i] and U[7 - i]) into
-// the running 9th key with 3-input maxima (one ALU op each).
-__device__ __forceinline__ int fold_losers(int L9, const int (&lo)[8]) {
-  const int a = __vimax3_s32(lo[0], lo[1], lo[2]);
-  const int b = __vimax3_s32(lo[3], lo[4], lo[5]);
-  const int c = __vimax3_s32(lo[6], lo[7], L9);
-  return __vimax3_s32(a, b, c);
-}
-
-// T <- top-8 of T and U (both sorted descending), sorted descending; with
-// WANT9, L9 <- max(L9, 9th key of T and U).
-template <bool WANT9>
-__device__ __forceinline__ void merge8(int (&T)[8], const int (&U)[8], int& L9) {
-  int mrg[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) mrg[i] = max(T[i], U[7 - i]);
-  if constexpr (WANT9) {
-    int lo[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) lo[i] = min(T[i], U[7 - i]);
-    L9 = fold_losers(L9, lo);
-  }
-  clean8_desc(mrg);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) T[i] = mrg[i];
-}
-
 // Folds one slice of this lane's row (SW values, experts col0 .. col0 + SW - 1)
 // into the running top-8 keys T (descending) and, if WANT9, the 9th key L9.
 // The slice row is read in 16-byte units whose order is XOR-rotated by
 // rot = (lane & 7).  The value at read position p of the row gets the low key
 // byte 255 - p; its expert id is p ^ (4 rot) (the rotation permutes the units
 // of each 128-byte slice row, and col0 is a multiple of 32).  The key keeps
-// the float's upper 24 bits: (bits >> 8) * 256 + byte, computed as a
-// multiply-high and a multiply-add by the run-time constants hi_mul = 2^24
-// and lo_mul = 2^8.  FIRST starts a row: the first chunk becomes T.
+// the float's upper 24 bits: (bits >> 8) * 256 + byte, the value of
+// trunc_key(bits, byte), computed as a multiply-high and a multiply-add by
+// the run-time constants hi_mul = 2^24 and lo_mul = 2^8.  FIRST starts a
+// row: the first chunk becomes T.
 template <int SW, bool WANT9, bool FIRST>
 __device__ __forceinline__ void slice_top8(const float* srow, int rot, int col0, uint32_t hi_mul,
                                            uint32_t lo_mul, int (&T)[8], int& L9) {
@@ -177,45 +128,6 @@ __device__ __forceinline__ void slice_top8(const float* srow, int rot, int col0,
       merge8<WANT9>(T, c, L9);
     }
   }
-}
-
-// Exact warp-cooperative top-k of one row (ties to the lower expert id, NaN
-// lowest, -0.0 == +0.0); lane r < k receives the id ranked r-th.
-__device__ __forceinline__ uint32_t exact_key(float x) {
-  uint32_t b = __float_as_uint(x);
-  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 1u;
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-template <int E>
-__device__ int row_topk_exact(const float* row, int k, int lane) {
-  constexpr int EPL = E / 32;
-  uint32_t key[EPL];
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) key[j] = exact_key(row[lane * EPL + j]);
-  int myidx = -1;
-  for (int r = 0; r < k; ++r) {
-    uint32_t best = 0u;
-    int bj = 0;
-#pragma unroll
-    for (int j = 0; j < EPL; ++j)
-      if (key[j] > best) {
-        best = key[j];
-        bj = j;
-      }
-    const uint32_t M = __reduce_max_sync(FULL, best);
-    const unsigned bal = __ballot_sync(FULL, best == M);
-    const int w = __ffs(bal) - 1;
-    const int e = __shfl_sync(FULL, lane * EPL + bj, w);
-    if (lane == w) {
-#pragma unroll
-      for (int j = 0; j < EPL; ++j)
-        if (j == bj) key[j] = 0u;
-    }
-    if (lane == r) myidx = e;
-  }
-  return myidx;
 }
 
 // ------------------------------------------------------------- slice copy
@@ -382,14 +294,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     }
     if (dead) continue;
     // certification of the truncated-key result
-    const int nxt = (K == 8) ? L9 : Tk[K < 8 ? K : 7];
-    bool bad = (Tk[K - 1] < 256) || (Tk[0] >= 0x7F800000);
-#pragma unroll
-    for (int i = 0; i < K; ++i) {
-      const int a = Tk[i];
-      const int b = (i + 1 < K) ? Tk[i + 1] : nxt;
-      bad = bad || (b >= (a & (int)0xFFFFFF00));
-    }
+    const bool bad = trunc_top8_uncertain<K>(Tk, L9);
     const bool live = lane < ntok;
     const unsigned redo = __ballot_sync(FULL, bad && live);
     // expert ids: read position pos = 255 - low byte, id = pos ^ 4 (lane & 7)
@@ -444,7 +349,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     while (todo) {
       const int f = __ffs(todo) - 1;
       todo &= todo - 1;
-      const int e = row_topk_exact<E>(p.logits + ((size_t)l * p.T + tok0 + f) * E, K, lane);
+      const int e = warp_topk_exact<E / 32>(p.logits + ((size_t)l * p.T + tok0 + f) * E, E, K, lane);
       if (out != nullptr && lane < K) out[(size_t)f * K + lane] = (uint8_t)e;
       if (aff_on) {
 #pragma unroll
