@@ -13,11 +13,12 @@
 //     integer order is the ranking by value (NaN -> 1, the lowest key a
 //     value can take; 0 is reserved for "taken"), and rank_key40() appends
 //     the inverted expert id so that equal values order by id;
-//   * truncated keys for the fast paths: the float's upper 24 bits with an
-//     8-bit inverted position below them, compared as signed ints, sorted
-//     by comparator networks.  These agree with the exact order only on
-//     positive finite values whose truncations differ, which
-//     trunc_top8_uncertain() checks; rows it rejects are redone exactly.
+//   * truncated keys for the fast paths: the float's upper bits with an
+//     inverted position in the low IDX_BITS bits (8, or 7 when E <= 128),
+//     compared as signed ints, sorted by comparator networks.  These agree
+//     with the exact order only on positive finite values whose truncations
+//     differ, which trunc_top8_uncertain() checks; rows it rejects are
+//     redone exactly.
 #pragma once
 
 #include <climits>
@@ -40,11 +41,15 @@ __device__ __forceinline__ uint64_t rank_key40(uint32_t bits, int e) {
 }
 
 // ------------------------------------------------------- truncated keys
-// The float's upper 24 bits with `low` (an inverted position, < 256) below.
-// (The thread-per-row pass forms the same value with a multiply-high and a
-// multiply-add, to keep it off the integer ALU pipe.)
+// The float's upper 32 - IDX_BITS bits with `low` (an inverted position,
+// < 2^IDX_BITS) below.  IDX_BITS = 8 serves any E <= 256; with E <= 128, 7
+// bits leave one more mantissa bit to the value, so fewer rows need the
+// exact path.  (The thread-per-row pass forms the 8-bit form with a
+// multiply-high and a multiply-add, to keep it off the integer ALU pipe.)
+template <int IDX_BITS = 8>
 __device__ __forceinline__ int trunc_key(uint32_t bits, int low) {
-  return (int)(bits & 0xFFFFFF00u) | low;
+  static_assert(IDX_BITS >= 1 && IDX_BITS <= 8, "index field of 1 to 8 bits");
+  return (int)(bits & ~((1u << IDX_BITS) - 1u)) | low;
 }
 
 // ---------------------------------------------------- comparator networks
@@ -106,16 +111,17 @@ __device__ __forceinline__ void merge8(int (&T)[8], const int (&U)[8], int& L9) 
 // True when the truncated-key top-8 T (descending; L9 the best key outside
 // it, used when K == 8) may differ from the exact top-K: a leading key is not
 // a positive finite float (zero, negative, NaN and +-inf all land here), or
-// two of the K + 1 leading keys share their upper 24 bits.
-template <int K>
+// two of the K + 1 leading keys share their value bits.
+template <int K, int IDX_BITS = 8>
 __device__ __forceinline__ bool trunc_top8_uncertain(const int (&T)[8], int L9) {
   static_assert(K >= 1 && K <= 8, "truncated keys serve k <= 8");
+  constexpr int VAL = (int)~((1u << IDX_BITS) - 1u);
   const int nxt = (K == 8) ? L9 : T[K < 8 ? K : 7];
-  bool bad = (T[K - 1] < 256) || (T[0] >= 0x7F800000);
+  bool bad = (T[K - 1] < (1 << IDX_BITS)) || (T[0] >= 0x7F800000);
 #pragma unroll
   for (int i = 0; i < K; ++i) {
     const int b = (i + 1 < K) ? T[i + 1] : nxt;
-    bad = bad || (b >= (T[i] & (int)0xFFFFFF00));
+    bad = bad || (b >= (T[i] & VAL));
   }
   return bad;
 }

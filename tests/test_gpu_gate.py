@@ -90,3 +90,39 @@ def test_gate_small(env, T, H, L, k):
 
 def test_gate_ragged_requests(env):
     _check(env, 777, 512, 3, 8, mask=[1], lengths=[5, 100, 16, 300, 356])
+
+
+def _bf16_bits(a):
+    """Small integers as bf16 bit patterns (exact)."""
+    return (np.asarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("lo,hi,k", [(0, 3, 8), (-2, 3, 8), (0, 2, 6), (-1, 2, 6)])
+def test_gate_integer_ties(env, lo, hi, k):
+    """Hidden states and weights that are small integers give exact integer logits with many
+    ties, so the GPU must reproduce the oracle's ranking on every row: equal logits rank the
+    lower expert first.  Rows of zeros and negative values reach the full exact pass; positive
+    ties reach the candidate-filtered one."""
+    torch, nat = env
+    T, H, L, E = 520, 128, 3, 128
+    rs = np.random.RandomState(100 + lo * 10 + hi + k)
+    xi = rs.randint(lo, hi, size=(T, H))
+    xi[:40] = 0                                                 # all-zero rows: every logit ties at 0
+    wi = rs.randint(0, 2, size=(L, H, E)) * rs.randint(-1 if lo < 0 else 0, 2, size=(L, H, E))
+    x, w = _bf16_bits(xi), _bf16_bits(wi)
+    dims = nat.make_dims(E, k, L, [0], 16)
+    dx = torch.from_numpy(x.view(np.int16)).cuda()
+    dw = torch.from_numpy(w.view(np.int16)).cuda()
+    tab = np.array([(t0, min(16, T - t0)) for t0 in range(0, T, 16)], dtype=np.int32)
+    dtab = torch.from_numpy(tab.reshape(-1)).cuda()
+    logits = torch.empty((L, T, E), dtype=torch.float32, device="cuda")
+    topk = torch.full((L, T, k), 255, dtype=torch.uint8, device="cuda")
+    cnt = torch.zeros((len(tab), 1, E), dtype=torch.uint8, device="cuda")
+    wsb = nat.moer_gate_workspace_bytes(dims, H)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    nat.moer_gate_topk(dims, dx, T, H, dw, dtab, len(tab), logits, topk, cnt, None, ws, wsb)
+    assert nat.moer_ws_status(ws) == 0
+    ref = oracle.get().gate_logits(x, w)
+    lg = logits.cpu().numpy()
+    assert np.array_equal(lg, ref.astype(np.float32)), "integer logits are exact"
+    assert np.array_equal(topk.cpu().numpy(), oracle.get().topk(ref, k))
