@@ -323,7 +323,9 @@ def run_gpu(args):
     rs = pipeline.RoutingStats.for_workload(wl, max_T=b.T, max_nblk=b.nblk, max_R=b.R,
                                             device=device, stream=stream)
     units = wl.L * b.T
-    alg_bytes = wl.L * b.T * (4 * wl.E + wl.k) + b.nblk * wl.m * wl.E
+    # the timed kernel is K1 alone (its call runs without block counts): the logits read and
+    # the top-k ids written; the block counts follow from the ids in the same step
+    alg_bytes = wl.L * b.T * (4 * wl.E + wl.k)
     launches_per_step = 2 + (2 if rs.cache is not None else 1) + 1 + (2 if wl.live else 1)
 
     for _ in range(max(args.warmup, 0)):
@@ -345,8 +347,9 @@ def run_gpu(args):
     for i in range(args.steps):
         rs.ensure(bd.T, bd.nblk, bd.R)
         ev[i][0].record(stream)
-        rs.topk_signature(logits, bd)
+        rs.topk_signature(logits, bd, blk_counts=False)
         ev[i][1].record(stream)
+        rs.ids_signature(bd)
         rs.block_stitch(bd)
         rs.affinity_load()
         rs.route(bd.R)
@@ -408,7 +411,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "frac_of_8tbs": achieved / 8000.0,
-                         "kernel": "k1_tpr_kernel (moer_topk_signature call)", "kernel_ms": k1_ms,
+                         "kernel": "k1_tpr_kernel (moer_topk_signature call, block counts "
+                                   "after it by moer_ids_signature)", "kernel_ms": k1_ms,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
             "gpu_launches": launches_per_step * args.steps,
@@ -433,7 +437,7 @@ def run_gpu(args):
     return 0
 
 
-GATE_LAUNCHES_PER_CALL = 4   # W_gate transpose, GEMM + top-k, co-activation, block counts
+GATE_LAUNCHES_PER_CALL = 4   # W_gate transpose, GEMM + top-k; co-activation, block counts
 
 
 def measure_gate(args, device, dist, stream, steps, with_e2e):
@@ -477,8 +481,9 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
     start.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
-        rs.gate_topk(hidden, w_gate, bd)
+        rs.gate_topk(hidden, w_gate, bd, counts=False)
         ev[i][1].record(stream)
+        rs.ids_signature(bd, blk_counts=True, affinity=True)
         rs.block_stitch(bd)
         rs.affinity_load()
         rs.route(bd.R)
@@ -503,7 +508,9 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "traffic": (recorded_traffic("gate_topk_kernel", "c5")
                                  if args.requests is None else None),
-                     "kernel": "gate_topk_kernel (moer_gate_topk call)", "kernel_ms": call_ms,
+                     "kernel": "gate_pair_kernel (moer_gate_topk call: W_gate transpose and the "
+                               "GEMM with fused top-k; counts after it by moer_ids_signature)",
+                     "kernel_ms": call_ms,
                      "algorithmic_flops_per_launch": flops,
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"},
         "gpu_launches": launches * steps,

@@ -229,6 +229,28 @@ MOER_API moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, 
                                     float* logits, uint8_t* topk, uint8_t* blk_cnt, int32_t* affinity,
                                     void* ws, size_t ws_bytes, moer_stream_t stream);
 
+/* Per-KV-block signature counts and expert co-activation from top-k ids
+ * computed elsewhere -- by the serving engine's own router, or by
+ * moer_topk_signature / moer_gate_topk called without blk_cnt and affinity.
+ *   [ELDR] section "Key idea / structure / operation": the gate is left
+ *   unchanged and the prefill hook records, per KV block, the discrete
+ *   top-k counts over the selected layer mask; [GRACE] section 3 and
+ *   section 4, Figure 2(a): co-activation profiled from the selections.
+ * topk      [L][T][k] uint8, 8-byte aligned: each row's k expert ids.
+ * blk_tab, blk_cnt: as in moer_topk_signature (blk_cnt may be NULL).
+ * affinity  [L][E][E] int32 or NULL, ACCUMULATED (+=) as in
+ *           moer_topk_signature; requires E <= 128 and k in {6, 8}.
+ * The ids are checked as they are read: an id >= E is not counted, and a
+ * row holding an id >= E or a repeated id is left out of the
+ * co-activation (its diagonal assumes k distinct ids); both are recorded
+ * as MOER_EDATA in ws.  A repeated id below E is counted as given in
+ * blk_cnt.
+ * ws        at least 256 bytes, 16-byte aligned (the status word).
+ */
+MOER_API moer_status moer_ids_signature(const moer_dims* d, const uint8_t* topk, int64_t T,
+                                        const int32_t* blk_tab, int32_t nblk, uint8_t* blk_cnt,
+                                        int32_t* affinity, void* ws, size_t ws_bytes, moer_stream_t stream);
+
 /* Expert grouping per MoE layer.  [GRACE-MoE] section 4.1: spectral
  * clustering of the co-activation matrix puts experts that are selected
  * together on the same GPU; the group sizes are held within

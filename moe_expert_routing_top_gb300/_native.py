@@ -58,6 +58,7 @@ def _load():
         "moer_idf_fit": ([dp, vp, i32, vp, vp], ctypes.c_int),
         "moer_gate_workspace_bytes": ([dp, i32], sz),
         "moer_gate_topk": ([dp, vp, i64, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "moer_ids_signature": ([dp, vp, i64, vp, i32, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_spectral_workspace_bytes": ([dp, i32], sz),
         "moer_spectral_groups": ([dp, vp, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "moer_mask_select_workspace_bytes": ([dp, i32], sz),
@@ -81,6 +82,7 @@ LIB = _load()
 EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_noalloc",
            "moer_block_stitch", "moer_affinity_load",
            "moer_route", "moer_idf_fit", "moer_gate_workspace_bytes", "moer_gate_topk",
+           "moer_ids_signature",
            "moer_replication_plan", "moer_kmeans_workspace_bytes", "moer_kmeans_balanced",
            "moer_mask_select_workspace_bytes", "moer_mask_select", "moer_spectral_workspace_bytes",
            "moer_spectral_groups",
@@ -206,6 +208,12 @@ def moer_gate_topk(dims, hidden, T, H, w_gate, blk_tab, nblk, logits, topk, blk_
         ctypes.byref(dims), _ptr(hidden), int(T), int(H), _ptr(w_gate), _ptr(blk_tab), int(nblk),
         _ptr(logits), _ptr(topk), _ptr(blk_cnt), _ptr(affinity), _ptr(ws), int(ws_bytes),
         _stream(stream)))
+
+
+def moer_ids_signature(dims, topk, T, blk_tab, nblk, blk_cnt, affinity, ws, ws_bytes, stream=None) -> None:
+    _check("moer_ids_signature", LIB.moer_ids_signature(
+        ctypes.byref(dims), _ptr(topk), int(T), _ptr(blk_tab), int(nblk), _ptr(blk_cnt), _ptr(affinity),
+        _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
 def moer_ws_status(ws, stream=None) -> int:

@@ -42,10 +42,10 @@ size_t gate_scratch_bytes(const moer_dims* d, int32_t H);
 moer_status gate_topk_launch(const moer_dims* d, const uint16_t* hidden, int64_t T, int32_t H,
                              const uint16_t* w_gate, float* logits, uint8_t* topk, void* ws, cudaStream_t st);
 moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t T, int32_t* affinity,
-                                cudaStream_t st);
+                                cudaStream_t st, uint32_t* status, bool check);
 moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mask_only, int64_t T,
                                 const int32_t* blk_tab, int nblk, uint8_t* blk_cnt, uint32_t* status,
-                                cudaStream_t st);
+                                cudaStream_t st, bool check);
 
 namespace {
 
@@ -235,11 +235,40 @@ moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, int64_t T
   s = gate_topk_launch(d, hidden, T, H, w_gate, logits, topk, ws, st);
   if (s != MOER_OK) return s;
   if (affinity != nullptr) {
-    s = affinity_ids_launch(d, topk, T, affinity, st);
+    s = affinity_ids_launch(d, topk, T, affinity, st, reinterpret_cast<uint32_t*>(ws), false);
     if (s != MOER_OK) return s;
   }
   if (hist)
-    s = block_counts_launch(d, topk, false, T, blk_tab, nblk, blk_cnt, reinterpret_cast<uint32_t*>(ws), st);
+    s = block_counts_launch(d, topk, false, T, blk_tab, nblk, blk_cnt, reinterpret_cast<uint32_t*>(ws), st, false);
+  return s;
+}
+
+moer_status moer_ids_signature(const moer_dims* d, const uint8_t* topk, int64_t T, const int32_t* blk_tab,
+                               int32_t nblk, uint8_t* blk_cnt, int32_t* affinity, void* ws, size_t ws_bytes,
+                               moer_stream_t stream) {
+  moer_status s = check_dims(d, false);
+  if (s != MOER_OK) return s;
+  if (T < 0 || T >= (int64_t(1) << 31) || nblk < 0) return MOER_ERANGE;
+  if (T == 0) return MOER_OK;
+  if (topk == nullptr || !aligned(topk, 8)) return MOER_EINVAL;
+  const bool hist = blk_cnt != nullptr && d->m > 0;
+  if (hist) {
+    if (blk_tab == nullptr || !aligned(blk_tab, 4) || !aligned(blk_cnt, 4)) return MOER_EINVAL;
+    if (nblk < 1 || nblk > T) return MOER_ESHAPE;
+  }
+  if (affinity != nullptr) {
+    if (!aligned(affinity, 4)) return MOER_EINVAL;
+    if (d->E > 128 || (d->k != 8 && d->k != 6)) return MOER_ERANGE;
+  }
+  if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
+  if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  if (affinity != nullptr) {
+    s = affinity_ids_launch(d, topk, T, affinity, st, status, true);
+    if (s != MOER_OK) return s;
+  }
+  if (hist) s = block_counts_launch(d, topk, false, T, blk_tab, nblk, blk_cnt, status, st, true);
   return s;
 }
 

@@ -34,6 +34,9 @@ struct BcParams {
 
 constexpr int BC_MC = 16;  // mask layers counted together (their loads in flight at once)
 
+// CHECK: the ids come from the caller (moer_ids_signature); an id >= E is
+// skipped and recorded as MOER_EDATA instead of being counted.
+template <bool CHECK>
 __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __grid_constant__ BcParams p) {
   extern __shared__ uint32_t bc_smem[];  // [BC_WARPS][BC_MC][E / 4]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,6 +86,10 @@ __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __gri
 #pragma unroll
               for (int by = 0; by < 4; ++by) {
                 const int e = (v[ii] >> (8 * by)) & 0xFF;
+                if (CHECK && e >= p.E) {
+                  atomicOr(p.status, WS_BIT_EDATA);
+                  continue;
+                }
                 atomicAdd(&c[e >> 2], 1u << ((e & 3) * 8));
               }
             }
@@ -94,6 +101,10 @@ __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __gri
           uint32_t* c = cnt + ii * wpb;
           for (int j = lane; j < n; j += 32) {
             const int e = src[j];
+            if (CHECK && e >= p.E) {
+              atomicOr(p.status, WS_BIT_EDATA);
+              continue;
+            }
             atomicAdd(&c[e >> 2], 1u << ((e & 3) * 8));
           }
         }
@@ -110,9 +121,10 @@ __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __gri
 
 // ids: either the caller's [L][T][k] top-k (mask_only = false: row block of
 // mask layer i is mask[i]) or a mask-only [m][T][k] buffer (row block i).
+// check: ids from outside the library, bounded by E as they are read.
 moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mask_only, int64_t T,
                                 const int32_t* blk_tab, int nblk, uint8_t* blk_cnt, uint32_t* status,
-                                cudaStream_t st) {
+                                cudaStream_t st, bool check) {
   BcParams p;
   p.ids = ids;
   p.layer_stride = T * d->k;
@@ -131,7 +143,11 @@ moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mas
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
   const int64_t grid = min64(((int64_t)nblk + BC_WARPS - 1) / BC_WARPS, (int64_t)sms * 8);
-  block_counts_kernel<<<(unsigned)grid, BC_WARPS * 32, BC_WARPS * BC_MC * (d->E / 4) * sizeof(uint32_t), st>>>(p);
+  const size_t smem = BC_WARPS * BC_MC * (d->E / 4) * sizeof(uint32_t);
+  if (check)
+    block_counts_kernel<true><<<(unsigned)grid, BC_WARPS * 32, smem, st>>>(p);
+  else
+    block_counts_kernel<false><<<(unsigned)grid, BC_WARPS * 32, smem, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
@@ -184,10 +200,14 @@ __device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* 
   __syncthreads();
 }
 
-template <int K>
+// CHECK: the ids come from the caller (moer_ids_signature); a row holding an
+// id >= E or a repeated id is left out (the diagonal needs k distinct ids)
+// and recorded as MOER_EDATA.
+template <int K, bool CHECK>
 __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t* __restrict__ ids, int64_t T,
                                                                   int E, int L, int nchunks,
-                                                                  int32_t* __restrict__ affinity) {
+                                                                  int32_t* __restrict__ affinity,
+                                                                  uint32_t* status) {
   extern __shared__ int ai_tile[];  // [E][E + 1] directed counts, then [E] row sums
   const int rs = E + 1;
   int* rsum = ai_tile + E * rs;
@@ -234,6 +254,25 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
         int e[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) e[j] = (w[u][j / 4] >> (8 * (j % 4))) & 0xFF;
+        if constexpr (CHECK) {
+          // K distinct ids below E: their bits in a 256-bit set number exactly K
+          unsigned long long m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+          bool inrange = true;
+#pragma unroll
+          for (int j = 0; j < K; ++j) {
+            inrange = inrange && e[j] < E;
+            const unsigned long long bit = 1ull << (e[j] & 63);
+            const int q = e[j] >> 6;
+            m0 |= q == 0 ? bit : 0ull;
+            m1 |= q == 1 ? bit : 0ull;
+            m2 |= q == 2 ? bit : 0ull;
+            m3 |= q == 3 ? bit : 0ull;
+          }
+          if (!inrange || __popcll(m0) + __popcll(m1) + __popcll(m2) + __popcll(m3) != K) {
+            atomicOr(status, WS_BIT_EDATA);
+            continue;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < K - 1; ++i) {
           int* ra = ai_tile + e[i] * rs;
@@ -250,7 +289,7 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
 // ids [L][T][k] (k = 6 or 8, 8-byte aligned rows for k = 8) -> affinity
 // [L][E][E] accumulated.
 moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t T, int32_t* affinity,
-                                cudaStream_t st) {
+                                cudaStream_t st, uint32_t* status, bool check) {
   if (d->k != 8 && d->k != 6) return MOER_ERANGE;
   if (d->E > 128) return MOER_ERANGE;
   const int nchunks = (int)((T + AI_CHUNK - 1) / AI_CHUNK);
@@ -258,16 +297,22 @@ moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t 
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
   const size_t smem = ((size_t)d->E * (d->E + 1) + d->E) * sizeof(int);
-  static std::atomic<unsigned long long> set8{0}, set6{0};
+  static std::atomic<unsigned long long> set8{0}, set6{0}, set8c{0}, set6c{0};
   const int most = (int)((128 * 129 + 128) * sizeof(int));
-  if (smem_optin(affinity_ids_kernel<8>, most, set8) != cudaSuccess ||
-      smem_optin(affinity_ids_kernel<6>, most, set6) != cudaSuccess)
+  if (smem_optin(affinity_ids_kernel<8, false>, most, set8) != cudaSuccess ||
+      smem_optin(affinity_ids_kernel<6, false>, most, set6) != cudaSuccess ||
+      smem_optin(affinity_ids_kernel<8, true>, most, set8c) != cudaSuccess ||
+      smem_optin(affinity_ids_kernel<6, true>, most, set6c) != cudaSuccess)
     return MOER_ECUDA;
   const int grid = (int)min64(nitems, (int64_t)sms * 2);
-  if (d->k == 8)
-    affinity_ids_kernel<8><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity);
+  if (d->k == 8 && !check)
+    affinity_ids_kernel<8, false><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
+  else if (d->k == 8)
+    affinity_ids_kernel<8, true><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
+  else if (!check)
+    affinity_ids_kernel<6, false><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
   else
-    affinity_ids_kernel<6><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity);
+    affinity_ids_kernel<6, true><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 

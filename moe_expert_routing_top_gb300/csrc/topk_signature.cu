@@ -43,7 +43,7 @@ namespace moer {
 
 moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mask_only, int64_t T,
                                 const int32_t* blk_tab, int nblk, uint8_t* blk_cnt, uint32_t* status,
-                                cudaStream_t st);
+                                cudaStream_t st, bool check);
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -283,7 +283,7 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
     e = k1_launch<8>(p, grid, st);
   if (e != cudaSuccess) return MOER_ECUDA;
   if (!hist) return MOER_OK;
-  return block_counts_launch(d, ids, mask_only, T, blk_tab, nblk, blk_cnt, status, st);
+  return block_counts_launch(d, ids, mask_only, T, blk_tab, nblk, blk_cnt, status, st, false);
 }
 
 }  // namespace moer

@@ -117,17 +117,29 @@ class RoutingStats:
         self.affinity.zero_()
 
     # ------------------------------------------------------------ the step
-    def topk_signature(self, logits, bd: BatchDev, write_topk=True):
+    def topk_signature(self, logits, bd: BatchDev, write_topk=True, blk_counts=True):
+        """Top-k ids and co-activation, plus the block counts unless ``blk_counts`` is False
+        (then ``ids_signature`` can produce them from the ids)."""
         nat.moer_topk_signature(self.dims, logits, bd.T, bd.blk_tab, bd.nblk,
-                                self.topk if write_topk else None, self.blk_cnt, self.affinity,
+                                self.topk if write_topk else None,
+                                self.blk_cnt if blk_counts else None, self.affinity,
                                 self.ws, self.ws_bytes, self.stream)
 
-    def gate_topk(self, hidden, w_gate, bd: BatchDev, logits=None):
-        """hidden bf16 [T][H] x w_gate bf16 [L][H][E] -> top-k, block counts, co-activation."""
+    def gate_topk(self, hidden, w_gate, bd: BatchDev, logits=None, counts=True):
+        """hidden bf16 [T][H] x w_gate bf16 [L][H][E] -> top-k and, unless ``counts`` is False,
+        block counts and co-activation (else ``ids_signature`` produces them from the ids)."""
         H = hidden.shape[-1]
         nat.moer_gate_topk(self.dims, hidden, bd.T, H, w_gate, bd.blk_tab, bd.nblk, logits,
-                           self.topk, self.blk_cnt, self.affinity, self.ws, self.ws_bytes,
+                           self.topk, self.blk_cnt if counts else None,
+                           self.affinity if counts else None, self.ws, self.ws_bytes,
                            self.stream)
+
+    def ids_signature(self, bd: BatchDev, blk_counts=True, affinity=False):
+        """Block counts (and, if asked, co-activation) from the top-k ids in ``self.topk``."""
+        T = bd.T
+        nat.moer_ids_signature(self.dims, self.topk, T, bd.blk_tab, bd.nblk,
+                               self.blk_cnt if blk_counts else None,
+                               self.affinity if affinity else None, self.ws, self.ws_bytes, self.stream)
 
     def block_stitch(self, bd: BatchDev):
         use_cache = self.cache is not None and bd.req_cache_off is not None

@@ -169,3 +169,20 @@ def test_wait_selftest_arguments(nat):
     assert t(64, 100, 1000, None) == 5
     assert t(64, 256, 0, None) == 3
     assert t(64, 256, 1000001, None) == 3
+
+
+def test_ids_signature_arguments(nat):
+    """Host-side validation of moer_ids_signature (no device work: every call is rejected)."""
+    f = nat.moer_ids_signature
+    d = nat.make_dims(128, 8, 4, [0, 2], 16)
+    assert _code(f, d, None, 100, 64, 7, 64, None, 64, 256, 0) == 1          # no ids
+    assert _code(f, d, BADPTR, 100, 64, 7, 64, None, 64, 256, 0) == 1        # misaligned ids
+    assert _code(f, d, 64, 100, None, 7, 64, None, 64, 256, 0) == 1          # counts without a block table
+    assert _code(f, d, 64, 100, 64, 0, 64, None, 64, 256, 0) == 2            # no blocks
+    assert _code(f, d, 64, 100, 64, 7, 64, None, 64, 255, 0) == 5            # status word
+    assert _code(f, d, 64, -1, 64, 7, 64, None, 64, 256, 0) == 3
+    d6 = nat.make_dims(256, 8, 4, [0], 16)
+    assert _code(f, d6, 64, 100, 64, 7, None, 64, 64, 256, 0) == 3           # co-activation needs E <= 128
+    d5 = nat.make_dims(128, 5, 4, [0], 16)
+    assert _code(f, d5, 64, 100, 64, 7, None, 64, 64, 256, 0) == 3           # and k in {6, 8}
+    nat.moer_ids_signature(d, 64, 0, None, 0, None, None, 64, 256, 0)       # T = 0: no-op
