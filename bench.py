@@ -46,9 +46,11 @@ WORKLOAD = {
     "c1": "OLMoE-shaped tiny (E=64,k=8,L=16,R=32)",
     "c2": "DeepSeek-V2-Lite-shaped calibration (E=64,k=6,L=26,R=1000)",
     "c3": "Qwen3-30B-A3B-shaped (E=128,k=8,L=48,R=1000,mask=12,D=16,G=8)",
+    "c4": "online routing stream (E=128,k=8,L=48,R=14000, 30% cached prefixes, live loads, D=16)",
     "c5": "gate GEMM then path (bf16 hidden T=524288 x H=2048, E=128,k=8,L=48,R=256x2048)",
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_full.txt")
+STREAM_TAU = 0.1  # the online stream's locality band
 
 
 def sources_sha(paths) -> str:
@@ -176,7 +178,8 @@ def sum_over_ranks(dist, x: float, device) -> float:
 
 # ------------------------------------------------------------ CPU oracle arm
 def oracle_pass(orc, wl, b, logits):
-    """The plain oracle over one batch: every row of the path, as it stands."""
+    """The plain oracle over one batch: every row of the path, as it stands.  Returns the
+    oracle's distances and decoder choices (the parity sample of the bench line)."""
     tk = orc.topk(logits, wl.k)
     bc = orc.block_counts(tk, wl.E, b.req_off, wl.B, wl.mask)
     cache = np.zeros((max(wl.nslots, 1), wl.m, wl.E), dtype=np.uint8)
@@ -184,7 +187,8 @@ def oracle_pass(orc, wl, b, logits):
     orc.affinity(tk, wl.E)
     orc.loads(tk, wl.E, wl.group_of, wl.G)
     _, dist = orc.sig_dist(rc, wl.idf, wl.centroids)
-    orc.route(dist, wl.tau, wl.loads0, wl.live)
+    choice, _ = orc.route(dist, wl.tau, wl.loads0, wl.live)
+    return dist, choice
 
 
 def cpu_sample(wl, nreq):
@@ -295,6 +299,205 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------- decoder-choice reporting
+BAND_EDGE = 1e-5  # a distance this close to d_min + tau may fall on either side
+
+
+def _edge_rows(dist, tau):
+    d = np.asarray(dist, dtype=np.float64)
+    with np.errstate(invalid="ignore"):
+        dmin = np.fmin.reduce(d, axis=1, keepdims=True)
+        return (np.abs(d - (dmin + tau)) <= BAND_EDGE).any(axis=1)
+
+
+def band_report(dist, tau):
+    """On the timed step's own distances: the requests with a decoder within BAND_EDGE of
+    the band edge, and the histogram of band sizes (entry i: requests whose band holds
+    i + 1 decoders)."""
+    d = np.asarray(dist, dtype=np.float64)
+    with np.errstate(invalid="ignore"):
+        dmin = np.fmin.reduce(d, axis=1, keepdims=True)
+        size = (d <= dmin + tau).sum(axis=1)
+    hist = np.bincount(size, minlength=d.shape[1] + 1)[1:].tolist()
+    return int(_edge_rows(d, tau).sum()), hist
+
+
+def choice_parity(gpu_choice, parity, tau, live):
+    """The GPU's decoder choices against the oracle's (on the oracle's own distances) over
+    the CPU-baseline sample: requests compared, choices that differ, and how many of the
+    sample's requests lie within BAND_EDGE of the band edge.  In live mode a difference
+    at the band edge changes the loads every later choice sees."""
+    if not parity or not parity.get("oracle"):
+        return None
+    n = diff = edge = off_edge = 0
+    first = None
+    for r0, od, oc in sorted(parity["oracle"], key=lambda x: x[0]):
+        g = np.asarray(gpu_choice[r0:r0 + len(oc)])
+        e = _edge_rows(od, tau)
+        dd = g != np.asarray(oc)
+        n += len(oc)
+        diff += int(dd.sum())
+        edge += int(e.sum())
+        off_edge += int((dd & ~e).sum())
+        if first is None and dd.any():
+            first = r0 + int(np.flatnonzero(dd)[0])
+    out = {"requests": n, "choice_diff": diff, "band_edge": edge, "choice_diff_off_band_edge": off_edge}
+    if live:
+        out["first_diff"] = first
+    return out
+
+
+# ------------------------------------------------------ the online stream
+def measure_stream(args, device, dist, stream, with_e2e=False, parity=None):
+    """The online routing stream (c4): 14,000 requests, ~13 M computed tokens, 320 GB of
+    logits, far more than HBM, so it runs in chunks of whole requests (about 8 GB of logits
+    each).  Per chunk the generator fills the logits on the device, untimed; the timed path
+    is moer_topk_signature (K1, top-k ids and co-activation), moer_ids_signature (block
+    counts), moer_block_stitch (signature cache carried across chunks: prefixes hit blocks
+    inserted by earlier chunks), moer_affinity_load and moer_route in live mode (loads
+    carried across chunks).  Per-chunk CUDA-event times are summed."""
+    import torch
+    import gen
+    from moe_expert_routing_top_gb300 import pipeline
+    sh = stream.cuda_stream
+    wl = gen.make_workload("c4", R=args.stream_requests)
+    chunks = wl.chunks(args.stream_chunk_tokens)
+    batches = [wl.batch(a, z) for a, z in chunks]
+    cap_T = max(x.T for x in batches)
+    rs = pipeline.RoutingStats.for_workload(wl, max_T=cap_T, max_nblk=max(x.nblk for x in batches),
+                                            max_R=max(x.R for x in batches), device=device,
+                                            stream=stream)
+    flat = torch.empty(wl.L * cap_T * wl.E, dtype=torch.float32, device=device)
+    bias = torch.from_numpy(wl.bias_mask.reshape(-1)).to(device)
+    # warm-up on a throwaway copy of the state, so the timed stream starts from an empty
+    # signature cache and the initial loads
+    b0 = batches[0]
+    bd0 = pipeline.BatchDev.from_host(b0, device=device)
+    v0 = flat[:wl.L * b0.T * wl.E].view(wl.L, b0.T, wl.E)
+    gen.dev_logits(wl, torch.from_numpy(b0.tok_key).to(device), torch.from_numpy(b0.tok_dom).to(device),
+                   v0, bias, sh)
+    rs_w = pipeline.RoutingStats.for_workload(wl, max_T=b0.T, max_nblk=b0.nblk, max_R=b0.R, device=device,
+                                              stream=stream)
+    for _ in range(max(args.warmup, 3)):
+        rs_w.topk_signature(v0, bd0, blk_counts=False)
+        rs_w.ids_signature(bd0)
+        rs_w.block_stitch(bd0)
+        rs_w.affinity_load()
+        rs_w.route(b0.R)
+    torch.cuda.synchronize()
+    if rs_w.status() != 0:
+        raise RuntimeError("device-side status after the stream warm-up is not OK")
+    del rs_w
+    choice = np.empty(wl.R, dtype=np.int32)
+    gdist = np.empty((wl.R, wl.D), dtype=np.float32)
+    choice_host = torch.empty(max(x.R for x in batches), dtype=torch.int32, pin_memory=True)
+    pinned = torch.empty(wl.L * cap_T * wl.E, dtype=torch.float32, pin_memory=True) if with_e2e else None
+    # per chunk: start, K1 start (after the host copy in the end-to-end run), K1 end, route
+    # start, end
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in batches]
+    clocks = ClockSampler(device.index or 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i, (b, (a, z)) in enumerate(zip(batches, chunks)):
+        bd = pipeline.BatchDev.from_host(b, device=device)
+        view = flat[:wl.L * b.T * wl.E].view(wl.L, b.T, wl.E)
+        gen.dev_logits(wl, torch.from_numpy(b.tok_key).to(device), torch.from_numpy(b.tok_dom).to(device),
+                       view, bias, sh)
+        if with_e2e:  # the chunk's inputs in pinned host memory, untimed
+            pinned[:view.numel()].copy_(view.reshape(-1))
+        rs.ensure(b.T, b.nblk, b.R)
+        e = ev[i]
+        e[0].record(stream)
+        if with_e2e:
+            view.reshape(-1).copy_(pinned[:view.numel()], non_blocking=True)
+        e[1].record(stream)
+        rs.topk_signature(view, bd, blk_counts=False)
+        e[2].record(stream)
+        rs.ids_signature(bd)
+        rs.block_stitch(bd)
+        rs.affinity_load()
+        e[3].record(stream)
+        rs.route(b.R)
+        choice_host[:b.R].copy_(rs.choice[:b.R], non_blocking=True)
+        e[4].record(stream)
+        torch.cuda.synchronize()
+        choice[a:z] = choice_host[:b.R].numpy()
+        gdist[a:z] = rs.dist[:b.R].cpu().numpy()
+    clk = clocks.stop()
+    if rs.status() != 0:
+        raise RuntimeError("device-side status after the stream is not OK")
+    k1 = sum(x[1].elapsed_time(x[2]) for x in ev)
+    path = sum(x[1].elapsed_time(x[4]) for x in ev)
+    route = sum(x[3].elapsed_time(x[4]) for x in ev)
+    e2e_ms = sum(x[0].elapsed_time(x[4]) for x in ev) if with_e2e else None
+    T = sum(x.T for x in batches)
+    units = wl.L * T
+    alg = wl.L * T * (4 * wl.E + wl.k)
+    peaks = measured_peaks()
+    ms_total = max_over_ranks(dist, path, device)
+    achieved = alg / (k1 / 1e3) / 1e9
+    edge, hist = band_report(gdist, wl.tau)
+    out = {
+        "workload": WORKLOAD["c4"] if args.stream_requests is None else f"c4, first {wl.R} requests",
+        "value": sum_over_ranks(dist, units, device) / (ms_total / 1e3), "unit": UNIT,
+        "ms_per_step": ms_total, "steps": 1, "chunks": len(batches), "tokens": T, "layers": wl.L,
+        "requests": wl.R, "kv_blocks": sum(x.nblk for x in batches),
+        "cached_blocks": int(sum(len(x.cache_idx) for x in batches)),
+        "logits_gb": wl.L * T * wl.E * 4 / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "k1_tpr_kernel (moer_topk_signature calls, summed over the chunks)",
+                     "kernel_ms": k1, "algorithmic_bytes_per_launch": alg / len(batches),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "route_live_ms": route, "route_live_share": route / path,
+        "band_edge": edge, "band_size_hist": hist,
+        "gpu_launches": len(batches) * (1 + 1 + 2 + 1 + 2),
+        "clocks": clk,
+        "l2": "inputs larger than L2 (logits %.1f GB per chunk)" % (wl.L * cap_T * wl.E * 4 / 1e9),
+        "gpu_choice": choice,
+    }
+    if with_e2e:
+        h2d = wl.L * T * wl.E * 4
+        out["e2e"] = {"value": units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                      "d2h_bytes_per_step": int(wl.R * 4), "ms_per_step": e2e_ms,
+                      "h2d_gbs": h2d / (e2e_ms / 1e3) / 1e9,
+                      "note": "per chunk: host logits -> device, the path, choices -> host; sequential"}
+    return out
+
+
+def run_stream_main(args, ws, rank, local, device, dist, stream):
+    import gen
+    parity = {}
+    g = measure_stream(args, device, dist, stream, with_e2e=args.e2e, parity=parity)
+    cpu = cpu1 = None
+    if rank == 0 and not args.no_cpu_baseline:
+        wl4 = gen.make_workload("c4", R=args.stream_requests)
+        cpu1 = cpu_baseline(wl4, args.cpu_requests, parity)
+        cpu = cpu_baseline_all_cores("c4", wl4, args.cpu_requests)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": g["value"], "unit": UNIT, "n_gpus": ws,
+            "steps": 1, "warmup": args.warmup, "ms_per_step": g["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+            "data": "synthetic (seeded counter-based generator; stands in for the pages' datasets)",
+            "config": {"workload": g["workload"], "tokens": g["tokens"], "layers": g["layers"],
+                       "requests": g["requests"], "kv_blocks": g["kv_blocks"], "chunks": g["chunks"],
+                       "parallelism": f"replicas x{ws}", "l2": g["l2"]},
+            "roofline": g["roofline"], "gpu_launches": g["gpu_launches"], "clocks": g["clocks"],
+            "e2e": g.get("e2e"), "cpu_baseline": cpu, "cpu_baseline_1core": cpu1,
+            "band_edge": g["band_edge"], "band_size_hist": g["band_size_hist"],
+            "choice_parity": choice_parity(g["gpu_choice"], parity, STREAM_TAU, True),
+            "route_live_ms": g["route_live_ms"], "route_live_share": g["route_live_share"],
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 # --------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -308,6 +511,8 @@ def run_gpu(args):
     sh = stream.cuda_stream
     if args.config == "c5":
         return run_gate_main(args, ws, rank, local, device, dist, stream)
+    if args.config == "c4":
+        return run_stream_main(args, ws, rank, local, device, dist, stream)
     if args.kmeans_only:
         if rank == 0:
             print(json.dumps({"kmeans_fit": measure_kmeans(args, device, stream, rank)}), flush=True)
@@ -365,13 +570,18 @@ def run_gpu(args):
     total_units = sum_over_ranks(dist, units * args.steps, device)
     value = total_units / (ms_total / 1e3)
 
+    # decoder choices of the timed step: band-edge requests and band sizes on its own distances
+    gpu_choice = rs.choice[:b.R].cpu().numpy()
+    band_edge, band_hist = band_report(rs.dist[:b.R].cpu().numpy(), wl.tau)
+
     # end-to-end through the public API: pinned host logits -> device, step, results -> host
     e2e = run_e2e(args, wl, b, bd, rs, logits, stream, device, dist) if args.e2e else None
 
     cpu = cpu1 = None
+    parity = {}
     if rank == 0 and not args.no_cpu_baseline:
-        cpu1 = cpu_baseline(wl, args.cpu_requests)
-        cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests)
+        cpu1 = cpu_baseline(wl, args.cpu_requests, parity)
+        cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests, parity)
 
     logits_gb = logits.numel() * 4 / 1e9
     # GRACE replication plan from this step's loads (per layer, after moer_affinity_load)
@@ -389,11 +599,21 @@ def run_gpu(args):
     mask_sel = measure_mask_select(args, wl, b, bd, rs, device, stream, rank)
     spectral = measure_spectral(args, wl, rs, device, stream, rank)
     kmeans = measure_kmeans(args, device, stream, rank) if args.kmeans else None
-    gate = None
-    if args.gate:
+    gate = stream_line = None
+    if args.gate or args.stream:
         del logits, rs
         torch.cuda.empty_cache()
+    if args.gate:
         gate = measure_gate(args, device, dist, stream, args.gate_steps, with_e2e=False)
+    if args.stream:
+        sparity = {}
+        stream_line = measure_stream(args, device, dist, stream, with_e2e=False)
+        if rank == 0 and not args.no_cpu_baseline:
+            wl4 = gen.make_workload("c4", R=args.stream_requests)
+            stream_line["cpu_baseline_1core"] = cpu_baseline(wl4, args.cpu_requests, sparity)
+            stream_line["choice_parity"] = choice_parity(stream_line["gpu_choice"], sparity, wl4.tau, True)
+        del stream_line["gpu_choice"]
+        torch.cuda.empty_cache()
 
     peaks = measured_peaks()
     achieved = alg_bytes / (k1_ms / 1e3) / 1e9
@@ -421,6 +641,9 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "cpu_baseline_1core": cpu1,
         }
+        line["band_edge"] = band_edge
+        line["band_size_hist"] = band_hist
+        line["choice_parity"] = choice_parity(gpu_choice, parity, wl.tau, wl.live)
         line["replication_plan"] = replication
         line["mask_select"] = mask_sel
         line["spectral_groups"] = spectral
@@ -430,6 +653,8 @@ def run_gpu(args):
             line["gate_path"] = {key: gate[key] for key in
                                  ("workload", "value", "unit", "ms_per_step", "steps", "roofline",
                                   "gpu_launches", "clocks")}
+        if stream_line is not None:
+            line["online_stream"] = stream_line
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -858,13 +1083,18 @@ def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
             "copy_streams": len(copy_streams), "h2d_gbs": h2d / dt / 1e9, "steps": args.e2e_steps}
 
 
-def cpu_baseline(wl, nreq):
+def cpu_baseline(wl, nreq, parity=None):
+    """The oracle single-threaded over the first `nreq` requests.  With `parity` (a dict),
+    the oracle's distances and choices of those requests are left in it as
+    parity["oracle"] = [(r0, dist, choice)]."""
     import oracle
     orc = oracle.get()
     b, logits = cpu_sample(wl, nreq)
     t0 = time.perf_counter()
-    oracle_pass(orc, wl, b, logits)
+    dist, choice = oracle_pass(orc, wl, b, logits)
     dt = time.perf_counter() - t0
+    if parity is not None:
+        parity.setdefault("oracle", []).append((0, dist, choice))
     return {"value": wl.L * b.T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {nreq} requests ({b.T} tokens x {wl.L} layers), one pass, "
                       f"{dt:.1f} s, single thread"}
@@ -881,14 +1111,16 @@ def _cpu_worker(cfg, r0, r1, barrier, results):
     logits = gen.host_logits(wl, b.tok_key, b.tok_dom)
     barrier.wait()
     t0 = time.perf_counter()
-    oracle_pass(orc, wl, b, logits)
-    results.put((b.T, time.perf_counter() - t0))
+    dist, choice = oracle_pass(orc, wl, b, logits)
+    results.put((b.T, time.perf_counter() - t0, r0, dist, choice))
 
 
-def cpu_baseline_all_cores(cfg, wl, nreq_per_core):
+def cpu_baseline_all_cores(cfg, wl, nreq_per_core, parity=None):
     """The oracle on every host core: request ranges split over spawned processes (the
     oracle itself is single-threaded and unchanged), timed from a common start barrier to
-    the last worker's end."""
+    the last worker's end.  With `parity`, each range's oracle distances and choices are
+    added to parity["oracle"] (static routing only: a live range would start from the
+    initial loads)."""
     import multiprocessing as mp
     import oracle
     oracle.get()  # built once here, so the workers only load it
@@ -913,7 +1145,9 @@ def cpu_baseline_all_cores(cfg, wl, nreq_per_core):
     finally:
         for pr in procs:
             pr.join(timeout=60)
-    tokens = sum(t for t, _ in got)
+    tokens = sum(g[0] for g in got)
+    if parity is not None and not wl.live:
+        parity.setdefault("oracle", []).extend((g[2], g[3], g[4]) for g in got)
     return {"value": wl.L * tokens / wall, "unit": UNIT, "cores": ncores, "kind": "oracle",
             "sample": f"first {ncores * nreq_per_core} requests ({tokens} tokens x {wl.L} layers), "
                       f"{nreq_per_core} per process on {ncores} host cores, one pass, "
@@ -926,7 +1160,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["own", "reference"], default="own")
-    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c5"])
+    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--requests", type=int, default=None,
                     help="run a reduced workload with this many requests (profiling)")
     ap.add_argument("--cpu-requests", type=int, default=16)
@@ -950,6 +1184,13 @@ def main(argv=None):
     ap.add_argument("--kmeans-reps", type=int, default=5)
     ap.add_argument("--kmeans-only", action="store_true",
                     help="time only the calibration fit (one JSON object, for profiling)")
+    ap.add_argument("--stream", dest="stream", action="store_true", default=True,
+                    help="also run the online routing stream (c4, chunked) into online_stream")
+    ap.add_argument("--no-stream", dest="stream", action="store_false")
+    ap.add_argument("--stream-requests", type=int, default=None,
+                    help="online stream: the first this many requests only (profiling)")
+    ap.add_argument("--stream-chunk-tokens", type=int, default=320_000,
+                    help="online stream: computed tokens per chunk (48 x 128 x 4 B each)")
     ap.add_argument("--cpu-tokens", type=int, default=512,
                     help="gate path: tokens in the oracle's CPU-baseline sample")
     args = ap.parse_args(argv)
