@@ -196,7 +196,11 @@ MOER_API moer_status moer_affinity_load(const moer_dims* d, const int32_t* affin
  *        the band member with the smallest load, ties to the lowest index.
  * loads [D] int32: live == 0: read only; live == 1: requests are routed in
  *        index order and each adds 1 to its decoder's load (updated in place).
- * ws    at least moer_workspace_bytes(d, 0, 0, R, D) bytes.
+ *        A request without any non-NaN distance gets choice -1 and changes no
+ *        load.
+ * ws    live == 1: at least moer_workspace_bytes(d, 0, 0, R, D) bytes, 16-byte
+ *       aligned (each request's band as a decoder bit mask); live == 0: may
+ *       be NULL.
  */
 MOER_API moer_status moer_route(const moer_dims* d, const int32_t* req_cnt, int32_t R,
                        const float* idf, const float* centroids, int32_t D, float tau,

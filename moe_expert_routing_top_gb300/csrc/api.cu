@@ -33,6 +33,7 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
 moer_status affinity_load_launch(const moer_dims* d, const int32_t* affinity, const int32_t* group_of,
                                  int32_t G, int64_t* W_expert, int64_t* W_group, double* rho_group,
                                  double* rho_expert, cudaStream_t st);
+size_t route_scratch_bytes(int32_t R);
 moer_status route_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, const float* idf,
                          const float* centroids, int32_t D, float tau, int32_t* loads, int32_t live,
                          float* sig, float* dist, int32_t* choice, void* ws, cudaStream_t st);
@@ -102,7 +103,7 @@ size_t moer_workspace_bytes(const moer_dims* d, int64_t T, int32_t nblk, int32_t
   size_t scratch = 0;
   if (d != nullptr && T > 0 && d->m > 0 && d->m <= 256 && d->k > 0) scratch = k1_scratch_bytes(d, T);
   if (R > 0 && D > 0) {
-    const size_t route = round256((size_t)R * (size_t)D * sizeof(float));
+    const size_t route = route_scratch_bytes(R);
     scratch = route > scratch ? route : scratch;
   }
   return WS_HEADER + scratch;
@@ -187,7 +188,7 @@ moer_status moer_route(const moer_dims* d, const int32_t* req_cnt, int32_t R, co
   if (req_cnt == nullptr || idf == nullptr || centroids == nullptr || loads == nullptr ||
       choice == nullptr)
     return MOER_EINVAL;
-  if (live && dist == nullptr) {
+  if (live) {  // the band masks of live routing live in the workspace
     if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
     if (ws_bytes < moer_workspace_bytes(d, 0, 0, R, D)) return MOER_ENOMEM;
   }

@@ -15,8 +15,11 @@
 //                   also picks the decoder.
 //   route_live      one CTA for the whole batch: requests are decided in
 //                   arrival order by warp 0 while the other warps stage the
-//                   next chunk of distances into shared memory; each decision
-//                   adds one to the chosen decoder's load.
+//                   next chunk of band masks into shared memory; each
+//                   decision adds one to the chosen decoder's load.  The band
+//                   does not depend on the loads, so route_sig_dist computes
+//                   each request's band as a decoder bit mask in parallel and
+//                   the sequential part only picks the least-loaded member.
 //   idf_fit         per (mask layer, expert): df over the calibration
 //                   requests and ln((1 + N) / (1 + df)) + 1.
 #include <cfloat>
@@ -45,28 +48,39 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return red[0];
 }
 
-// Decoder choice from D distances: d_min, band {q : d_q <= d_min + tau}, the
-// smallest load in the band, ties to the lowest index.  NaN distances are
-// outside the band and take no part in d_min (fminf skips them); with no
-// finite distance the band is empty and the choice is -1.  Sequential form
-// used by the static path (one thread).
-__device__ __forceinline__ int band_pick(const float* dist, int D, float tau, const int32_t* loads) {
+// The band of D <= 64 distances as a bit mask: d_min, then bit q set when
+// d_q <= d_min + tau.  NaN distances are outside the band and take no part in
+// d_min (fminf skips them); with no non-NaN distance the mask is 0.
+__device__ __forceinline__ unsigned long long band_mask(const float* dist, int D, float tau) {
   float dmin = dist[0];
   for (int q = 1; q < D; ++q) dmin = fminf(dmin, dist[q]);
   const float thr = __fadd_rn(dmin, tau);
+  unsigned long long m = 0ull;
+  for (int q = 0; q < D; ++q)
+    if (dist[q] <= thr) m |= 1ull << q;
+  return m;
+}
+
+// The band member with the smallest load, ties to the lowest index; -1 for
+// an empty band.  Sequential form used by the static path (one thread).
+__device__ __forceinline__ int band_pick(unsigned long long m, const int32_t* loads) {
   int best = -1;
-  for (int q = 0; q < D; ++q) {
-    if (!(dist[q] <= thr)) continue;
+  while (m) {
+    const int q = __ffsll((long long)m) - 1;
+    m &= m - 1;
     if (best < 0 || loads[q] < loads[best]) best = q;
   }
   return best;
 }
 
+// pick = 1 (static): the CTA chooses the decoder; pick = 0 (live): it leaves
+// the band mask in band[r] for route_live.
 template <int DM>
 __global__ void __launch_bounds__(ROUTE_THREADS) route_sig_dist(
     const int32_t* __restrict__ req_cnt, int dim, const float* __restrict__ idf,
     const float* __restrict__ centroids, int D, float tau, const int32_t* __restrict__ loads,
-    int pick, float* __restrict__ sig, float* __restrict__ dist, int32_t* __restrict__ choice) {
+    int pick, float* __restrict__ sig, float* __restrict__ dist, int32_t* __restrict__ choice,
+    unsigned long long* __restrict__ band) {
   __shared__ float red[32];
   __shared__ float part[ROUTE_THREADS / 32][DM];
   __shared__ float dsh[DM];
@@ -107,51 +121,48 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_sig_dist(
   }
   __syncthreads();
   if (threadIdx.x < D && dist) dist[(size_t)r * D + threadIdx.x] = dsh[threadIdx.x];
-  if (pick && threadIdx.x == 0) choice[r] = band_pick(dsh, D, tau, loads);
+  if (threadIdx.x == 0) {
+    const unsigned long long m = band_mask(dsh, D, tau);
+    if (pick)
+      choice[r] = band_pick(m, loads);
+    else
+      band[r] = m;
+  }
 }
 
-// Sequential live routing.  Lane q of warp 0 owns decoders q and q + 32.
-constexpr int LIVE_BUF = 4096;  // floats per staging buffer
+// Sequential live routing over the requests' band masks.  Lane q of warp 0
+// owns decoders q and q + 32; per request one warp minimum of the in-band
+// loads and a ballot for the lowest decoder holding it.
+constexpr int LIVE_BUF = 2048;  // band masks per staging buffer
 
-__global__ void __launch_bounds__(ROUTE_THREADS) route_live(const float* __restrict__ dist, int R, int D,
-                                                            float tau, int32_t* __restrict__ loads,
+template <bool WIDE>  // WIDE: D > 32, lanes also own decoders 32 .. 63
+__global__ void __launch_bounds__(ROUTE_THREADS) route_live(const unsigned long long* __restrict__ band, int R,
+                                                            int D, int32_t* __restrict__ loads,
                                                             int32_t* __restrict__ choice) {
-  __shared__ float buf[2][LIVE_BUF];
-  const int LIVE_CHUNK = LIVE_BUF / D;
+  __shared__ unsigned long long buf[2][LIVE_BUF];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int ld0 = 0, ld1 = 0;
   if (warp == 0) {
     ld0 = lane < D ? loads[lane] : INT_MAX;
-    ld1 = lane + 32 < D ? loads[lane + 32] : INT_MAX;
+    ld1 = WIDE && lane + 32 < D ? loads[lane + 32] : INT_MAX;
   }
-  const int nch = (R + LIVE_CHUNK - 1) / LIVE_CHUNK;
-  // stage chunk 0
-  for (int i = threadIdx.x; i < min(R, LIVE_CHUNK) * D; i += blockDim.x) buf[0][i] = dist[i];
+  const int nch = (R + LIVE_BUF - 1) / LIVE_BUF;
+  for (int i = threadIdx.x; i < min(R, LIVE_BUF); i += blockDim.x) buf[0][i] = band[i];
   __syncthreads();
   for (int c = 0; c < nch; ++c) {
-    const int r0 = c * LIVE_CHUNK;
-    const int nr = min(LIVE_CHUNK, R - r0);
+    const int r0 = c * LIVE_BUF;
+    const int nr = min(LIVE_BUF, R - r0);
     if (warp == 0) {
-      const float* b = buf[c & 1];
+      const unsigned long long* b = buf[c & 1];
       for (int i = 0; i < nr; ++i) {
-        const float d0 = lane < D ? b[i * D + lane] : FLT_MAX;
-        const float d1 = lane + 32 < D ? b[i * D + lane + 32] : FLT_MAX;
-        // distances are non-negative, so their bit patterns order as integers
-        // (+inf included); a NaN distance and an absent decoder take no part
-        // in d_min (as fminf in band_pick)
-        const int k0 = (lane < D && !isnan(d0)) ? __float_as_int(d0) : INT_MAX;
-        const int k1 = (lane + 32 < D && !isnan(d1)) ? __float_as_int(d1) : INT_MAX;
-        const int dm = __reduce_min_sync(FULL, min(k0, k1));
-        // every distance NaN: dm stays INT_MAX, a NaN pattern, so thr is NaN
-        // and the band is empty
-        const float thr = __fadd_rn(__int_as_float(dm), tau);
-        const bool in0 = lane < D && d0 <= thr;
-        const bool in1 = lane + 32 < D && d1 <= thr;
-        const int c0 = in0 ? ld0 : INT_MAX, c1 = in1 ? ld1 : INT_MAX;
-        const int lm = __reduce_min_sync(FULL, min(c0, c1));
+        const unsigned long long m = b[i];
+        // bits only for decoders below D; an empty mask (no non-NaN distance)
+        // leaves every lane out, so the choice is -1 and no load changes
+        const bool in0 = (m >> lane) & 1ull;
+        const bool in1 = WIDE && ((m >> (lane + 32)) & 1ull);
+        const int lm = __reduce_min_sync(FULL, min(in0 ? ld0 : INT_MAX, in1 ? ld1 : INT_MAX));
         const unsigned b0 = __ballot_sync(FULL, in0 && ld0 == lm);
-        const unsigned b1 = __ballot_sync(FULL, in1 && ld1 == lm);
-        // empty band (no finite distance): no decoder, loads unchanged
+        const unsigned b1 = WIDE ? __ballot_sync(FULL, in1 && ld1 == lm) : 0u;
         const int q = b0 ? __ffs(b0) - 1 : (b1 ? 32 + __ffs(b1) - 1 : -1);
         if (lane == 0) choice[r0 + i] = q;
         if (q >= 0 && lane == (q & 31)) {
@@ -162,16 +173,16 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_live(const float* __restr
         }
       }
     } else if (c + 1 < nch) {
-      const int n1 = min(LIVE_CHUNK, R - (r0 + LIVE_CHUNK)) * D;
-      const float* src = dist + (size_t)(r0 + LIVE_CHUNK) * D;
-      float* dstb = buf[(c + 1) & 1];
+      const int n1 = min(LIVE_BUF, R - (r0 + LIVE_BUF));
+      const unsigned long long* src = band + (size_t)(r0 + LIVE_BUF);
+      unsigned long long* dstb = buf[(c + 1) & 1];
       for (int i = threadIdx.x - 32; i < n1; i += blockDim.x - 32) dstb[i] = src[i];
     }
     __syncthreads();
   }
   if (warp == 0) {
     if (lane < D) loads[lane] = ld0;
-    if (lane + 32 < D) loads[lane + 32] = ld1;
+    if (WIDE && lane + 32 < D) loads[lane + 32] = ld1;
   }
 }
 
@@ -183,21 +194,26 @@ __global__ void idf_fit_kernel(const int32_t* __restrict__ req_cnt, int R, int d
   }
 }
 
+size_t route_scratch_bytes(int32_t R) { return ((size_t)R * sizeof(unsigned long long) + 255) / 256 * 256; }
+
 moer_status route_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, const float* idf,
                          const float* centroids, int32_t D, float tau, int32_t* loads, int32_t live,
                          float* sig, float* dist, int32_t* choice, void* ws, cudaStream_t st) {
   const int dim = d->m * d->E;
-  float* dbuf = dist;
-  if (live && dbuf == nullptr) dbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + WS_HEADER);
+  unsigned long long* band =
+      live ? reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + WS_HEADER) : nullptr;
   if (D <= 16)
     route_sig_dist<16><<<R, ROUTE_THREADS, 0, st>>>(req_cnt, dim, idf, centroids, D, tau, loads,
-                                                    live ? 0 : 1, sig, dbuf, choice);
+                                                    live ? 0 : 1, sig, dist, choice, band);
   else
     route_sig_dist<ROUTE_DMAX><<<R, ROUTE_THREADS, 0, st>>>(req_cnt, dim, idf, centroids, D, tau,
-                                                            loads, live ? 0 : 1, sig, dbuf, choice);
+                                                            loads, live ? 0 : 1, sig, dist, choice, band);
   if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
   if (live) {
-    route_live<<<1, ROUTE_THREADS, 0, st>>>(dbuf, R, D, tau, loads, choice);
+    if (D <= 32)
+      route_live<false><<<1, ROUTE_THREADS, 0, st>>>(band, R, D, loads, choice);
+    else
+      route_live<true><<<1, ROUTE_THREADS, 0, st>>>(band, R, D, loads, choice);
     if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
   }
   return MOER_OK;
