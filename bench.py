@@ -498,6 +498,51 @@ def run_stream_main(args, ws, rank, local, device, dist, stream):
     return 0
 
 
+# ------------------------------------------------------ offline calibration
+def calibrate_workload(args, wl, device, stream):
+    """The offline half before the served step (untimed for the line's value): calibration
+    prompts of the same model (same logit stream and expert biases, new prompts) go
+    through pipeline.calibrate -- top-k and co-activation, idf, greedy layer mask,
+    signatures, balanced K-means, spectral groups -- and the served workload takes the
+    resulting mask, idf, centroids and expert groups.  Returns a summary for the line and
+    the arrays the oracle workers need (overrides)."""
+    import torch
+    import gen
+    from moe_expert_routing_top_gb300 import pipeline
+    cal = gen.make_calibration(wl, R=args.calib_requests)
+    cb = cal.batch()
+    logits = torch.empty((wl.L, cb.T, wl.E), dtype=torch.float32, device=device)
+    gen.dev_logits(cal, torch.from_numpy(cb.tok_key).to(device), torch.from_numpy(cb.tok_dom).to(device),
+                   logits, torch.from_numpy(cal.bias_mask.reshape(-1)).to(device), stream.cuda_stream)
+    seed_rows = gen.kmeans_seed_rows(cal.R, wl.D)
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    got = pipeline.calibrate(wl.E, wl.k, wl.L, wl.B, logits,
+                             pipeline.BatchDev.from_host(cb, device=device, with_cache=False), cb.req_off,
+                             m=int(wl.mask.shape[0]), D=wl.D, G=wl.G, seed_rows=seed_rows, tau=wl.tau,
+                             device=device, stream=stream)
+    z.record(stream)
+    torch.cuda.synchronize()
+    del logits
+    torch.cuda.empty_cache()
+    over = {"mask": got.mask.astype(np.int32), "idf": got.idf.cpu().numpy(),
+            "centroids": got.centroids.cpu().numpy(), "group_of": got.group_of.cpu().numpy()}
+    apply_overrides(wl, over)
+    sizes = np.bincount(got.assign.cpu().numpy(), minlength=wl.D)
+    summary = {"prompts": cal.R, "tokens": cb.T, "ms": a.elapsed_time(z),
+               "mask_in_order": got.mask_order.tolist(), "mask": got.mask.tolist(),
+               "kmeans_steps": int(got.kmeans_info[0]), "cluster_sizes": sizes.tolist(),
+               "group_knee_j": got.knee.tolist()}
+    return summary, over
+
+
+def apply_overrides(wl, over):
+    """The served workload takes the calibrated mask, idf, centroids and expert groups."""
+    if over:
+        wl.mask, wl.idf = over["mask"], over["idf"]
+        wl.centroids, wl.group_of = over["centroids"], over["group_of"]
+
+
 # --------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -519,6 +564,8 @@ def run_gpu(args):
         return 0
 
     wl = gen.make_workload(args.config, R=args.requests)
+    calib, over = (calibrate_workload(args, wl, device, stream)
+                   if args.calibrate and args.config in ("c2", "c3") else (None, None))
     b = wl.batch()
     bd = pipeline.BatchDev.from_host(b, device=device)
     logits = torch.empty((wl.L, b.T, wl.E), dtype=torch.float32, device=device)
@@ -581,7 +628,7 @@ def run_gpu(args):
     parity = {}
     if rank == 0 and not args.no_cpu_baseline:
         cpu1 = cpu_baseline(wl, args.cpu_requests, parity)
-        cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests, parity)
+        cpu = cpu_baseline_all_cores(args.config, wl, args.cpu_requests, parity, over)
 
     logits_gb = logits.numel() * 4 / 1e9
     # GRACE replication plan from this step's loads (per layer, after moer_affinity_load)
@@ -641,6 +688,11 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "cpu_baseline_1core": cpu1,
         }
+        if calib is not None:
+            line["calibration"] = calib
+            line["config"]["mask"] = "greedy selection on %d calibration prompts" % calib["prompts"]
+            line["config"]["centroids"] = "balanced K-means of the calibration signatures"
+            line["config"]["groups"] = "spectral grouping of the calibration co-activation"
         line["band_edge"] = band_edge
         line["band_size_hist"] = band_hist
         line["choice_parity"] = choice_parity(gpu_choice, parity, wl.tau, wl.live)
@@ -1100,13 +1152,14 @@ def cpu_baseline(wl, nreq, parity=None):
                       f"{dt:.1f} s, single thread"}
 
 
-def _cpu_worker(cfg, r0, r1, barrier, results):
+def _cpu_worker(cfg, r0, r1, barrier, results, over=None):
     """One host core's share of the all-cores oracle run: its requests' inputs are made
     first (untimed), then every worker starts the oracle pass at the same barrier."""
     import gen
     import oracle
     orc = oracle.get()
     wl = gen.make_workload(cfg)
+    apply_overrides(wl, over)
     b = wl.batch(r0, r1)
     logits = gen.host_logits(wl, b.tok_key, b.tok_dom)
     barrier.wait()
@@ -1115,7 +1168,7 @@ def _cpu_worker(cfg, r0, r1, barrier, results):
     results.put((b.T, time.perf_counter() - t0, r0, dist, choice))
 
 
-def cpu_baseline_all_cores(cfg, wl, nreq_per_core, parity=None):
+def cpu_baseline_all_cores(cfg, wl, nreq_per_core, parity=None, over=None):
     """The oracle on every host core: request ranges split over spawned processes (the
     oracle itself is single-threaded and unchanged), timed from a common start barrier to
     the last worker's end.  With `parity`, each range's oracle distances and choices are
@@ -1133,7 +1186,7 @@ def cpu_baseline_all_cores(cfg, wl, nreq_per_core, parity=None):
     barrier = ctx.Barrier(ncores + 1)
     results = ctx.Queue()
     procs = [ctx.Process(target=_cpu_worker,
-                         args=(cfg, i * nreq_per_core, (i + 1) * nreq_per_core, barrier, results))
+                         args=(cfg, i * nreq_per_core, (i + 1) * nreq_per_core, barrier, results, over))
              for i in range(ncores)]
     for pr in procs:
         pr.start()
@@ -1184,6 +1237,11 @@ def main(argv=None):
     ap.add_argument("--kmeans-reps", type=int, default=5)
     ap.add_argument("--kmeans-only", action="store_true",
                     help="time only the calibration fit (one JSON object, for profiling)")
+    ap.add_argument("--calibrate", dest="calibrate", action="store_true", default=True,
+                    help="c2/c3: calibrate mask, idf, centroids and expert groups on the GPU first")
+    ap.add_argument("--no-calibrate", dest="calibrate", action="store_false")
+    ap.add_argument("--calib-requests", type=int, default=1000,
+                    help="calibration prompts (lognormal lengths, median 512)")
     ap.add_argument("--stream", dest="stream", action="store_true", default=True,
                     help="also run the online routing stream (c4, chunked) into online_stream")
     ap.add_argument("--no-stream", dest="stream", action="store_false")

@@ -87,6 +87,7 @@ class Workload:
     nslots: int
     hidden_dim: int = 0         # gate-GEMM workloads: H
     wgate_scale: float = 0.02
+    key_owner_base: int = 0     # token keys of request r are owned by key_owner_base + r
 
     @property
     def m(self) -> int:
@@ -107,7 +108,7 @@ class Workload:
             owner[:cut] = d
             cur = d
             cut = min(cut, int(self.cached_blocks[cur]) * self.B)
-        keys[:] = (owner << KEY_POS_BITS) | pos
+        keys[:] = ((owner + self.key_owner_base) << KEY_POS_BITS) | pos
         return keys
 
     def computed_tokens(self, r: int) -> int:
@@ -298,6 +299,32 @@ def make_workload(name: str, R: Optional[int] = None, seed: Optional[int] = None
                     bias_mask=bias_mask, mask=mask, D=D, tau=tau, centroids=centroids,
                     loads0=loads0, live=live, G=G, group_of=group_of, idf=idf,
                     slot_of_block=slot_of_block, nslots=nslots, hidden_dim=H)
+
+
+CALIB_OWNER_BASE = 1 << 24  # calibration prompts never share a token key with served requests
+
+
+def make_calibration(wl: Workload, R: int = 1000, seed: Optional[int] = None) -> Workload:
+    """The offline calibration prompts of the model that `wl` serves: the same logit
+    stream (seed), expert biases per domain and shapes, with R new prompts -- lengths
+    lognormal(ln 512, 0.75) clipped to [32, 4096] as in the calibration config, domains
+    uniform, no prefix reuse -- whose token keys are distinct from every served request's.
+    Every layer is in the mask (the calibration chooses the serving mask)."""
+    rs = np.random.RandomState((wl.seed if seed is None else seed) ^ 0xCA11B)
+    plen = _lognormal_lengths(rs, R, 512, 0.75, 32, 4096)
+    dom = (rs.randint(0, wl.ndom, size=R).astype(np.int32) if wl.ndom > 0
+           else np.full(R, -1, dtype=np.int32))
+    cached = np.zeros(R, dtype=np.int64)
+    donor = np.full(R, -1, dtype=np.int64)
+    slot_of_block, nslots = _slots(plen, cached, donor, wl.B)
+    mask = np.arange(wl.L, dtype=np.int32)
+    return Workload(name=wl.name + "-calibration", seed=wl.seed, E=wl.E, k=wl.k, L=wl.L, B=wl.B, R=R,
+                    prompt_len=plen, cached_blocks=cached, donor=donor, dom=dom, ndom=wl.ndom,
+                    bias=wl.bias, bias_mask=wl.bias_mask, mask=mask, D=wl.D, tau=wl.tau,
+                    centroids=np.zeros((wl.D, wl.L * wl.E), dtype=np.float32), loads0=wl.loads0,
+                    live=False, G=wl.G, group_of=wl.group_of,
+                    idf=np.ones((wl.L, wl.E), dtype=np.float32), slot_of_block=slot_of_block,
+                    nslots=nslots, hidden_dim=wl.hidden_dim, key_owner_base=CALIB_OWNER_BASE)
 
 
 def make_custom(E: int, k: int, L: int, lengths, *, B: int = 16, mask=None, ndom: int = 2,

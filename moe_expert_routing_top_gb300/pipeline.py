@@ -212,3 +212,100 @@ class RoutingStats:
                             centroids=wl.centroids, idf=wl.idf, loads=wl.loads0, live=wl.live,
                             G=wl.G, group_of=wl.group_of, nslots=wl.nslots, max_T=max_T,
                             max_nblk=max_nblk, max_R=max_R, device=device, stream=stream)
+
+
+@dataclasses.dataclass
+class Calibration:
+    """What the offline half of the method hands to serving (device tensors unless noted)."""
+    mask: np.ndarray          # host [m] sorted layer ids: the signature's layer mask
+    mask_order: np.ndarray    # host [m] the layers in the order the greedy selection chose them
+    quality: np.ndarray       # host [m] fp64 proxy quality after each addition
+    idf: torch.Tensor         # [m][E] fp32 idf of the mask layers
+    sig: torch.Tensor         # [N][m*E] fp32 signatures of the calibration prompts
+    centroids: torch.Tensor   # [D][m*E] fp32 balanced K-means centroids: one per decoder
+    assign: torch.Tensor      # [N] int32 cluster of each calibration prompt
+    kmeans_info: np.ndarray   # host [3] steps, cancellations, step-bound flag
+    affinity: torch.Tensor    # [L][E][E] int32 co-activation over the calibration prompts
+    group_of: torch.Tensor    # [L][E] int32 spectral expert groups
+    knee: np.ndarray          # host [L] knee grid point of each layer's grouping
+
+
+def calibrate(E, k, L, block, logits, bd: BatchDev, req_off, *, m, D, G, seed_rows, max_iter=100,
+              tau=0.1, device="cuda", stream=None) -> Calibration:
+    """The offline calibration on the GPU, call by call: the prompts' top-k ids, per-block
+    counts and co-activation over every layer (moer_topk_signature), their request counts
+    (moer_block_stitch) and idf (moer_idf_fit); the greedy layer mask (moer_mask_select);
+    the counts, idf and count.idf signatures over that mask (moer_ids_signature,
+    moer_block_stitch, moer_idf_fit, moer_route with one zero centroid, whose choice is
+    not used); the balanced K-means centroids from the rows `seed_rows` of those
+    signatures (moer_kmeans_balanced); and the spectral expert groups of the
+    co-activation (moer_spectral_groups).  This function orders calls and holds buffers;
+    the arithmetic is the library's.
+
+    logits [L][T][E] fp32 (device) and bd / req_off (host [R+1]) describe the calibration
+    prompts, one request each, without prefix reuse."""
+    dev = torch.device(device)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    f32, i32, u8 = torch.float32, torch.int32, torch.uint8
+    T, R, nblk = bd.T, bd.R, bd.nblk
+    d_all = nat.make_dims(E, k, L, list(range(L)), block)
+    topk = torch.empty((L, T, k), dtype=u8, device=dev)
+    blk_all = torch.empty((nblk, L, E), dtype=u8, device=dev)
+    aff = torch.zeros((L, E, E), dtype=i32, device=dev)
+    wsb = nat.moer_workspace_bytes(d_all, T, nblk, R, 1)
+    ws = torch.zeros(wsb, dtype=u8, device=dev)
+    nat.moer_topk_signature(d_all, logits, T, bd.blk_tab, nblk, topk, blk_all, aff, ws, wsb, st)
+    req_all = torch.empty((R, L, E), dtype=i32, device=dev)
+    nat.moer_block_stitch(d_all, blk_all, bd.blk_tab, nblk, bd.req_blk_off, R, None, 0, None, None, 0,
+                          None, req_all, ws, wsb, st)
+    del blk_all
+    idf_all = torch.empty((L, E), dtype=f32, device=dev)
+    nat.moer_idf_fit(d_all, req_all, R, idf_all, st)
+    del req_all
+    # the greedy layer mask
+    d_sel = nat.make_dims(E, k, L, [], block)
+    mask_order = torch.empty(m, dtype=i32, device=dev)
+    quality = torch.empty(m, dtype=torch.float64, device=dev)
+    msb = nat.moer_mask_select_workspace_bytes(d_sel, R)
+    ms_ws = torch.zeros(msb, dtype=u8, device=dev)
+    off = torch.as_tensor(np.asarray(req_off, dtype=np.int32)).to(dev)
+    nat.moer_mask_select(d_sel, topk, T, off, R, idf_all, m, mask_order, quality, ms_ws, msb, st)
+    order = mask_order.cpu().numpy()
+    mask = np.sort(order)  # the dims take the mask as a sorted host array
+    # counts, idf and signatures over the mask
+    d_m = nat.make_dims(E, k, L, mask.tolist(), block)
+    blk_m = torch.empty((nblk, m, E), dtype=u8, device=dev)
+    nat.moer_ids_signature(d_m, topk, T, bd.blk_tab, nblk, blk_m, None, ws, wsb, st)
+    req_m = torch.empty((R, m, E), dtype=i32, device=dev)
+    nat.moer_block_stitch(d_m, blk_m, bd.blk_tab, nblk, bd.req_blk_off, R, None, 0, None, None, 0, None,
+                          req_m, ws, wsb, st)
+    idf_m = torch.empty((m, E), dtype=f32, device=dev)
+    nat.moer_idf_fit(d_m, req_m, R, idf_m, st)
+    sig = torch.empty((R, m * E), dtype=f32, device=dev)
+    zero_c = torch.zeros((1, m * E), dtype=f32, device=dev)
+    zero_l = torch.zeros(1, dtype=i32, device=dev)
+    unused = torch.empty(R, dtype=i32, device=dev)
+    nat.moer_route(d_m, req_m, R, idf_m, zero_c, 1, tau, zero_l, 0, sig, None, unused, None, 0, st)
+    # balanced K-means from the caller's seed rows
+    init = sig.index_select(0, torch.as_tensor(np.asarray(seed_rows, dtype=np.int64)).to(dev)).contiguous()
+    cent = torch.empty((D, m * E), dtype=f32, device=dev)
+    assign = torch.empty(R, dtype=i32, device=dev)
+    info = torch.zeros(3, dtype=i32, device=dev)
+    kmb = nat.moer_kmeans_workspace_bytes(R, m * E, D)
+    km_ws = torch.zeros(kmb, dtype=u8, device=dev)
+    nat.moer_kmeans_balanced(sig, R, m * E, D, init, max_iter, cent, assign, info, None, km_ws, kmb, st)
+    # spectral expert groups of the co-activation
+    group_of = torch.empty((L, E), dtype=i32, device=dev)
+    knee = torch.empty(L, dtype=i32, device=dev)
+    u = torch.empty((L, 17), dtype=torch.float64, device=dev)
+    s = torch.empty((L, 17), dtype=torch.float64, device=dev)
+    spb = nat.moer_spectral_workspace_bytes(d_all, G)
+    sp_ws = torch.zeros(spb, dtype=u8, device=dev)
+    nat.moer_spectral_groups(d_all, aff, G, group_of, knee, u, s, sp_ws, spb, st)
+    for w in (ws, ms_ws, km_ws, sp_ws):
+        code = nat.moer_ws_status(w, st)
+        if code != 0:
+            raise nat.MoerError("calibrate", code, nat.moer_status_str(code))
+    return Calibration(mask=mask, mask_order=order, quality=quality.cpu().numpy(), idf=idf_m, sig=sig,
+                       centroids=cent, assign=assign, kmeans_info=info.cpu().numpy(), affinity=aff,
+                       group_of=group_of, knee=knee.cpu().numpy())
