@@ -113,54 +113,3 @@ def test_gate_path_reduced(env):
         assert np.array_equal(gA, A) and np.array_equal(gW, W)
         assert np.array_equal(gu.host(rs.Wg), Wg)
         assert np.array_equal(gu.host(rs.rho_g), rg) and np.array_equal(gu.host(rs.rho_e), re)
-
-
-def test_gate_path_full(env):
-    torch, pipeline, gu = env
-    orc = oracle.get()
-    wl = gen.make_workload("c5")
-    b = wl.batch()
-    H, k, E = wl.hidden_dim, wl.k, wl.E
-    dx, dw = _device_inputs(torch, wl, b.T)
-    rs = pipeline.RoutingStats.for_workload(wl, max_T=b.T, max_nblk=b.nblk, max_R=b.R)
-    bd = pipeline.BatchDev.from_host(b)
-    rs.gate_step(dx, dw, bd)
-    torch.cuda.synchronize()
-    assert rs.status() == 0
-    del dx
-    tk = gu.host(rs.topk_for(b.T))
-    # sampled tokens, every layer, against the oracle's fp64 logits
-    rng = np.random.RandomState(11)
-    toks = np.sort(rng.choice(b.T, size=48, replace=False))
-    x = np.concatenate([gen.host_hidden(wl.seed, int(t), 1, H) for t in toks])
-    w = gen.host_wgate(wl.seed, wl.L, H, E, wl.wgate_scale)
-    ref = gu.oracle_gate_logits(x, w)
-    otk = orc.topk(ref, k)
-    order_ok, set_ok = _margins(ref, k)
-    got = tk[:, toks]
-    assert np.array_equal(got[order_ok], otk[order_ok]), "ordered top-k"
-    assert np.array_equal(np.sort(got[set_ok], axis=1), np.sort(otk[set_ok], axis=1)), "top-k sets"
-    # properties over everything
-    assert (np.sort(tk, axis=2)[:, :, 1:] != np.sort(tk, axis=2)[:, :, :-1]).all(), "distinct ids"
-    A = gu.host(rs.affinity).astype(np.int64)
-    W = gu.host(rs.W)
-    assert np.array_equal(A, A.transpose(0, 2, 1))
-    assert np.array_equal(np.diagonal(A, axis1=1, axis2=2), W)
-    assert np.array_equal(A.sum(axis=2), k * W)
-    assert (W.sum(axis=1) == k * b.T).all()
-    for layer in (0, wl.L - 1):
-        assert np.array_equal(W[layer], np.bincount(tk[layer].reshape(-1), minlength=E))
-    lens = b.blk_tab[:, 1].astype(np.int64)
-    gbc = gu.host(rs.blk_cnt[:b.nblk])
-    assert (gbc.sum(axis=2, dtype=np.int64) == (k * lens)[:, None]).all()
-    i = wl.m // 2
-    layer = int(wl.mask[i])
-    for j in rng.choice(b.nblk, size=64, replace=False):
-        t0, ln = b.blk_tab[j]
-        assert np.array_equal(gbc[j, i], np.bincount(tk[layer, t0:t0 + ln].reshape(-1), minlength=E))
-    grc = gu.host(rs.req_cnt[:b.R]).astype(np.int64)
-    assert (grc.sum(axis=2) == (k * np.diff(b.req_off))[:, None]).all()
-    gdist = gu.host(rs.dist[:b.R]).astype(np.float64)
-    gch = gu.host(rs.choice[:b.R])
-    for r in range(b.R):
-        assert gu.valid_choice(int(gch[r]), gdist[r], wl.tau, wl.loads0), r
