@@ -49,7 +49,7 @@ WORKLOAD = {
     "c4": "online routing stream (E=128,k=8,L=48,R=14000, 30% cached prefixes, live loads, D=16)",
     "c5": "gate GEMM then path (bf16 hidden T=524288 x H=2048, E=128,k=8,L=48,R=256x2048)",
 }
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_full.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 STREAM_TAU = 0.1  # the online stream's locality band
 
 
@@ -61,9 +61,11 @@ def sources_sha(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, config: str):
-    """DRAM bytes per launch from the committed ncu record, or None when the record is
-    missing or the kernel's sources changed since it was taken."""
+def recorded_traffic(kernel: str, config: str, rows: float):
+    """DRAM bytes of one launch over `rows` token x layer pairs, from the committed ncu record
+    of a small case of the same workload scaled by rows (the part that does not grow with
+    rows, `fixed_bytes`, kept once); None when the record is missing or the kernel's
+    sources changed since it was taken."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
@@ -73,10 +75,13 @@ def recorded_traffic(kernel: str, config: str):
             tr = json.loads(ln)
             if tr.get("kernel") == kernel and tr.get("config") == config:
                 try:
-                    if sources_sha(tr["sources"]) == tr.get("kernel_sha"):
-                        return tr.get("dram_bytes_per_launch")
+                    if sources_sha(tr["sources"]) != tr.get("kernel_sha"):
+                        return None
                 except OSError:
                     return None
+                fixed = tr.get("fixed_bytes", 0.0)
+                case = tr["dram_bytes_read"] + tr["dram_bytes_write"] - fixed
+                return case * rows / tr["case_rows"] + fixed
     return None
 
 
@@ -447,7 +452,8 @@ def measure_stream(args, device, dist, stream, with_e2e=False, parity=None):
         "cached_blocks": int(sum(len(x.cache_idx) for x in batches)),
         "logits_gb": wl.L * T * wl.E * 4 / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("k1_tpr_kernel", "c3", units / len(batches)),
                      "kernel": "k1_tpr_kernel (moer_topk_signature calls, summed over the chunks)",
                      "kernel_ms": k1, "algorithmic_bytes_per_launch": alg / len(batches),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
@@ -664,7 +670,7 @@ def run_gpu(args):
 
     peaks = measured_peaks()
     achieved = alg_bytes / (k1_ms / 1e3) / 1e9
-    traffic = recorded_traffic("k1_tpr_kernel", args.config) if args.requests is None else None
+    traffic = recorded_traffic("k1_tpr_kernel", "c3", units) if args.config == "c3" else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -783,8 +789,7 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "traffic": (recorded_traffic("gate_topk_kernel", "c5")
-                                 if args.requests is None else None),
+                     "traffic": recorded_traffic("gate_pair_kernel", "c5", wl.L * b.T),
                      "kernel": "gate_pair_kernel (moer_gate_topk call: W_gate transpose and the "
                                "GEMM with fused top-k; counts after it by moer_ids_signature)",
                      "kernel_ms": call_ms,
