@@ -12,6 +12,8 @@
 // insert copies one block record per warp, and a request's record of m*E
 // counts is summed by one CTA whose threads own consecutive words, so every
 // load and store is coalesced.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace moer {
@@ -52,14 +54,20 @@ __device__ __forceinline__ void accv(uint32_t (&a)[16], uint4 v) {
   acc4(*reinterpret_cast<uint32_t(*)[4]>(q + 12), v.w);
 }
 
-// One CTA per request: thread w owns word w of the record (16 or 4 bytes of
-// packed 8-bit counts) and sums it over the request's cached and computed
-// blocks, four block loads in flight at a time.
-template <typename V, int NB>
-__global__ void stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t* __restrict__ req_blk_off,
+// One CTA per request, S groups of TW threads: thread (s, w) sums word w of
+// the record (16 or 4 bytes of packed 8-bit counts) over the request's cached
+// blocks s, s + S, ... and computed blocks s, s + S, ..., four block loads in
+// flight; group 0 adds the S partial sums (through shared memory, laid out
+// [S][NB][TW] so every access is conflict-free) and writes the request's row.
+// With S groups a request's ~80 blocks keep S times as many loads in flight.
+template <typename V, int NB, int S>
+__global__ void __launch_bounds__(1024) stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t* __restrict__ req_blk_off,
                            const int32_t* __restrict__ cache_idx, int ncached,
                            const int32_t* __restrict__ req_cache_off, const V* __restrict__ cache_w, int nslots,
                            int rec_v, int32_t* __restrict__ req_cnt, uint32_t* status) {
+  extern __shared__ uint32_t part[];  // [S][NB][TW] partial sums
+  const int TW = blockDim.x / S;
+  const int grp = threadIdx.x / TW, wl = threadIdx.x - grp * TW;
   const int r = blockIdx.x;
   const int b0 = req_blk_off[r], b1 = req_blk_off[r + 1];
   int c0 = cache_w ? req_cache_off[r] : 0, c1 = cache_w ? req_cache_off[r + 1] : 0;
@@ -68,39 +76,55 @@ __global__ void stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t*
   const bool bad_cache = c0 < 0 || c1 < c0 || c1 > ncached;
   if ((bad_blocks || bad_cache) && threadIdx.x == 0 && status != nullptr) atomicOr(status, WS_BIT_EDATA);
   if (bad_cache) c0 = c1 = 0;
-  for (int w = threadIdx.x; w < rec_v; w += blockDim.x) {
+  for (int w0 = 0; w0 < rec_v; w0 += TW) {
+    const int w = w0 + wl;
     uint32_t a[NB];
 #pragma unroll
     for (int i = 0; i < NB; ++i) a[i] = 0u;
-    for (int c = c0; c < c1; ++c) {
-      const int slot = cache_idx[c];
-      if (slot < 0 || slot >= nslots) {
-        if (status != nullptr && w == 0) atomicOr(status, WS_BIT_EDATA);
-        continue;
+    if (w < rec_v) {
+      for (int c = c0 + grp; c < c1; c += S) {
+        const int slot = cache_idx[c];
+        if (slot < 0 || slot >= nslots) {
+          if (status != nullptr) atomicOr(status, WS_BIT_EDATA);
+          continue;
+        }
+        accv(a, cache_w[(size_t)slot * rec_v + w]);
       }
-      accv(a, cache_w[(size_t)slot * rec_v + w]);
-    }
-    if (!bad_blocks) {
-      int b = b0;
-      for (; b + 4 <= b1; b += 4) {
-        const V v0 = blk_w[(size_t)b * rec_v + w], v1 = blk_w[(size_t)(b + 1) * rec_v + w];
-        const V v2 = blk_w[(size_t)(b + 2) * rec_v + w], v3 = blk_w[(size_t)(b + 3) * rec_v + w];
-        accv(a, v0);
-        accv(a, v1);
-        accv(a, v2);
-        accv(a, v3);
+      if (!bad_blocks) {
+        int b = b0 + grp;
+        for (; b + 3 * S < b1; b += 4 * S) {
+          const V v0 = blk_w[(size_t)b * rec_v + w], v1 = blk_w[(size_t)(b + S) * rec_v + w];
+          const V v2 = blk_w[(size_t)(b + 2 * S) * rec_v + w], v3 = blk_w[(size_t)(b + 3 * S) * rec_v + w];
+          accv(a, v0);
+          accv(a, v1);
+          accv(a, v2);
+          accv(a, v3);
+        }
+        for (; b < b1; b += S) accv(a, blk_w[(size_t)b * rec_v + w]);
       }
-      for (; b < b1; ++b) accv(a, blk_w[(size_t)b * rec_v + w]);
     }
-    int32_t* dst = req_cnt + (size_t)r * rec_v * NB + (size_t)w * NB;
-    if constexpr (NB == 16) {
-      int4* d4 = reinterpret_cast<int4*>(dst);
+    if constexpr (S > 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        d4[i] = make_int4((int)a[4 * i], (int)a[4 * i + 1], (int)a[4 * i + 2], (int)a[4 * i + 3]);
-    } else {
+      for (int i = 0; i < NB; ++i) part[((size_t)grp * NB + i) * TW + wl] = a[i];
+      __syncthreads();
+      if (grp == 0) {
+        for (int q = 1; q < S; ++q)
 #pragma unroll
-      for (int i = 0; i < NB; ++i) dst[i] = (int32_t)a[i];
+          for (int i = 0; i < NB; ++i) a[i] += part[((size_t)q * NB + i) * TW + wl];
+      }
+      __syncthreads();  // the next word range reuses the partial sums
+    }
+    if (grp == 0 && w < rec_v) {
+      int32_t* dst = req_cnt + (size_t)r * rec_v * NB + (size_t)w * NB;
+      if constexpr (NB == 16) {
+        int4* d4 = reinterpret_cast<int4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_int4((int)a[4 * i], (int)a[4 * i + 1], (int)a[4 * i + 2], (int)a[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) dst[i] = (int32_t)a[i];
+      }
     }
   }
 }
@@ -128,20 +152,29 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
                                                     nslots, rec_bytes / 4, status);
     if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
   }
-  if (v16) {
-    const int rec_v = rec_bytes / 16;
-    const int threads = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
-    stitch_sum<uint4, 16><<<R, threads, 0, st>>>(reinterpret_cast<const uint4*>(blk_cnt), nblk, req_blk_off,
-                                                 cache_idx, ncached, req_cache_off, reinterpret_cast<const uint4*>(cache),
-                                                 nslots, rec_v, req_cnt, status);
-  } else {
-    const int rec_v = rec_bytes / 4;
-    const int threads = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
-    stitch_sum<uint32_t, 4><<<R, threads, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), nblk, req_blk_off,
-                                                   cache_idx, ncached, req_cache_off,
-                                                   reinterpret_cast<const uint32_t*>(cache), nslots, rec_v,
-                                                   req_cnt, status);
-  }
+  // TW threads per group cover the record's words; four groups when the partial sums fit
+  // in 48 KB of shared memory, else two
+  auto launch_sum = [&](auto vtag, auto nbtag) {
+    using V = decltype(vtag);
+    constexpr int NB = decltype(nbtag)::value;
+    const int rec_v = rec_bytes / (int)sizeof(V);
+    const int tw = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
+    const size_t smem4 = (size_t)4 * NB * tw * sizeof(uint32_t);
+    if (smem4 <= 48 * 1024)
+      stitch_sum<V, NB, 4><<<R, 4 * tw, smem4, st>>>(reinterpret_cast<const V*>(blk_cnt), nblk, req_blk_off,
+                                                    cache_idx, ncached, req_cache_off,
+                                                    reinterpret_cast<const V*>(cache), nslots, rec_v, req_cnt,
+                                                    status);
+    else
+      stitch_sum<V, NB, 2><<<R, 2 * tw, smem4 / 2, st>>>(reinterpret_cast<const V*>(blk_cnt), nblk,
+                                                        req_blk_off, cache_idx, ncached, req_cache_off,
+                                                        reinterpret_cast<const V*>(cache), nslots, rec_v,
+                                                        req_cnt, status);
+  };
+  if (v16)
+    launch_sum(uint4{}, std::integral_constant<int, 16>{});
+  else
+    launch_sum(uint32_t{}, std::integral_constant<int, 4>{});
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
