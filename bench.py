@@ -495,8 +495,11 @@ def run_stream_main(args, ws, rank, local, device, dist, stream):
             "e2e": g.get("e2e"), "cpu_baseline": cpu, "cpu_baseline_1core": cpu1,
             "band_edge": g["band_edge"], "band_size_hist": g["band_size_hist"],
             "choice_parity": choice_parity(g["gpu_choice"], parity, STREAM_TAU, True),
+            "choice_diff": None,
             "route_live_ms": g["route_live_ms"], "route_live_share": g["route_live_share"],
         }
+        if line["choice_parity"]:
+            line["choice_diff"] = line["choice_parity"]["choice_diff"]
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -665,6 +668,8 @@ def run_gpu(args):
             wl4 = gen.make_workload("c4", R=args.stream_requests)
             stream_line["cpu_baseline_1core"] = cpu_baseline(wl4, args.cpu_requests, sparity)
             stream_line["choice_parity"] = choice_parity(stream_line["gpu_choice"], sparity, wl4.tau, True)
+            if stream_line["choice_parity"]:
+                stream_line["choice_diff"] = stream_line["choice_parity"]["choice_diff"]
         del stream_line["gpu_choice"]
         torch.cuda.empty_cache()
 
@@ -702,6 +707,7 @@ def run_gpu(args):
         line["band_edge"] = band_edge
         line["band_size_hist"] = band_hist
         line["choice_parity"] = choice_parity(gpu_choice, parity, wl.tau, wl.live)
+        line["choice_diff"] = line["choice_parity"]["choice_diff"] if line["choice_parity"] else None
         line["replication_plan"] = replication
         line["mask_select"] = mask_sel
         line["spectral_groups"] = spectral
