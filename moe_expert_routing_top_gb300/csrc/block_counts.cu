@@ -211,6 +211,8 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
   extern __shared__ int ai_tile[];  // [E][E + 1] directed counts, then [E] row sums
   const int rs = E + 1;
   int* rsum = ai_tile + E * rs;
+  const uint32_t tile_base = smem_u32(ai_tile);
+  const uint32_t row_bytes = (uint32_t)rs * 4u;
   const int64_t nitems = (int64_t)L * nchunks;
   const int64_t i0 = (int64_t)blockIdx.x * nitems / gridDim.x;
   const int64_t i1 = ((int64_t)blockIdx.x + 1) * nitems / gridDim.x;
@@ -273,11 +275,19 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
             continue;
           }
         }
+        // shared address of D[a][b] = tile + 4 b + a * row pitch: one
+        // multiply-add per pair (FMA pipe) rather than integer-ALU adds
+        uint32_t colb[K];
+#pragma unroll
+        for (int j = 1; j < K; ++j) colb[j] = tile_base + 4u * (uint32_t)e[j];
 #pragma unroll
         for (int i = 0; i < K - 1; ++i) {
-          int* ra = ai_tile + e[i] * rs;
 #pragma unroll
-          for (int j = i + 1; j < K; ++j) atomicAdd(ra + e[j], 1);
+          for (int j = i + 1; j < K; ++j) {
+            uint32_t addr;
+            asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(addr) : "r"((uint32_t)e[i]), "r"(row_bytes), "r"(colb[j]));
+            asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr) : "memory");
+          }
         }
       }
     }

@@ -24,6 +24,9 @@ struct K1Params {
   // being folded into a logic op on the integer ALU pipe, which the
   // comparator networks already saturate
   uint32_t key_hi_mul, key_lo_mul;
+  // bytes between rows of the co-activation tile, at run time for the same
+  // reason: each pair's shared address is then one multiply-add (FMA pipe)
+  uint32_t aff_row_bytes;
   int16_t slot_of_layer[256];  // mask slot of each layer, -1 if not a mask layer
 };
 

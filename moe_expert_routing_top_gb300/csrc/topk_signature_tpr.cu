@@ -208,6 +208,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   const int rot = lane & 7;
   float* ring = reinterpret_cast<float*>(smem + G::OFF_ROWS) + (size_t)warp * R * SLICE_FLOATS;
   uint32_t* aff = reinterpret_cast<uint32_t*>(smem + G::OFF_AFF);
+  const uint32_t aff_base = smem_u32(aff);
   int* rsum = reinterpret_cast<int*>(smem + G::OFF_RSUM);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR) + warp * R;
   const bool aff_on = p.affinity != nullptr;
@@ -320,11 +321,20 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
       if (aff_on) {
         // directed pairs (rank i above rank j): k(k-1)/2 adds per row
         if constexpr (G::W32) {
+          // shared address of D[a][b] = tile + 4 b + a * row pitch: one
+          // multiply-add per pair (FMA pipe), the pitch known only at run time
+          // so that it is not folded into integer-ALU shifts and adds
+          uint32_t colb[K];
+#pragma unroll
+          for (int j = 1; j < K; ++j) colb[j] = aff_base + 4u * (uint32_t)idx[j];
 #pragma unroll
           for (int i = 0; i < K - 1; ++i) {
-            uint32_t* ra = aff + idx[i] * G::RS;
 #pragma unroll
-            for (int j = i + 1; j < K; ++j) atomicAdd(ra + idx[j], 1u);
+            for (int j = i + 1; j < K; ++j) {
+              uint32_t addr;
+              asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(addr) : "r"((uint32_t)idx[i]), "r"(p.aff_row_bytes), "r"(colb[j]));
+              asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr) : "memory");
+            }
           }
         } else {
           int wj[K];
