@@ -11,24 +11,25 @@
 // Design (GB300, sm_103a):
 //   * The weights are transposed once per call into the workspace,
 //     Wt[l*128 + e][h], so both operands are K-major.
-//   * One CTA per SM, persistent over tiles of 128 tokens x 2 layers
-//     (M = 128, N = 256 experts), K = H in blocks of 64.  Tiles, token block
-//     major, are handed out in order from a global counter, so the grid
-//     works on a few token blocks at a time: each hidden-state panel is read
-//     from HBM once and shared through L2; the 25 MB of weights stay in L2.
-//   * Warp 0 streams both operands with TMA (cp.async.bulk.tensor, 128-byte
-//     swizzle) into a 4-stage ring of 48 KB stages (mbarrier full/empty).
-//   * Warp 1 owns a 512-column TMEM allocation (two fp32 128 x 256
-//     accumulators); one elected thread issues tcgen05.mma.cta_group::1
-//     .kind::f16 (4 per K block) and releases stages and accumulators with
-//     tcgen05.commit.
-//   * Warps 2-5 drain an accumulator with tcgen05.ld while the next tile's
-//     MMAs run: each thread owns one token row (one TMEM lane), reads its 128
-//     logits per layer, optionally stores them, and selects the row's top-k
-//     with the same comparator networks as the logits pass (unique truncated
-//     keys; certified, else redone exactly with 40-bit keys).
+//   * Clusters of two CTAs on the two SMs of a TPC, persistent over tiles of
+//     256 tokens x 2 layers (UMMA M = 256, N = 256 experts) computed with
+//     tcgen05.mma.cta_group::2, K = H in blocks of 64.  Each CTA loads its
+//     own 128 tokens and one layer's 128 weight rows per K block (32 KB, six
+//     stages, 128-byte swizzled TMA) and receives its 128 tokens x 256
+//     columns in TMEM.  Tiles, token block major, are handed out in order
+//     from a global counter, so the grid works on a few token blocks at a
+//     time: each hidden-state panel is read from HBM once and shared through
+//     L2; the 25 MB of weights stay in L2.
+//   * Per CTA: warp 0 loads (in the leader, rank 0, it also takes the tile
+//     ids and posts both CTAs' transaction bytes); warp 1 allocates two
+//     256-column fp32 accumulators (both CTAs, collectively) and, in the
+//     leader, one elected thread issues the MMAs and multicasts its commits
+//     to both CTAs; warps 2-5 drain an accumulator with tcgen05.ld while the
+//     next tile's MMAs run: each thread owns one token row (one TMEM lane)
+//     and selects its top-k per layer with comparator networks on truncated
+//     keys (rank.cuh), certified, else redone exactly.
 //   * Every wait is bounded; on expiry the kernel records MOER_ETIMEOUT,
-//     drains what it issued and frees its TMEM before returning.
+//     waits for its copies in flight and frees its TMEM before returning.
 #include <cuda.h>
 #include <climits>
 #include <mutex>
@@ -38,40 +39,13 @@
 
 namespace moer {
 
-// Kernel used by moer_gate_topk: 1 = the CTA-pair kernel (cta_group::2),
-// 0 = the single-CTA kernel (cta_group::1).
-#ifndef MOER_GATE_PAIR
-#define MOER_GATE_PAIR 1
-#endif
-
-constexpr int GK_BM = 128;   // tokens per tile (UMMA M)
-constexpr int GK_BN = 256;   // experts per tile: two layers of 128 (UMMA N)
-constexpr int GK_BK = 64;    // K per stage (128 bytes of bf16: one swizzle row)
-constexpr int GK_STAGES = 4;
-constexpr int GK_A_BYTES = GK_BM * GK_BK * 2;  // 16 KB
-constexpr int GK_B_BYTES = GK_BN * GK_BK * 2;  // 32 KB
-constexpr int GK_STAGE_BYTES = GK_A_BYTES + GK_B_BYTES;
-constexpr int GK_THREADS = 6 * 32;
-constexpr int GK_TMEM_COLS = 512;
-// Tile ids travel from the producer to the MMA and epilogue warps through a
-// ring of GK_TRING slots.  The producer leads the epilogue by at most
-// GK_STAGES + 2 tiles (stages in flight, two accumulators), so a slot is never
-// rewritten before every reader has taken it.
-constexpr int GK_TRING = 16;
-static_assert(GK_TRING > GK_STAGES + 2, "tile-id ring shorter than the pipeline's lead");
-constexpr size_t GK_OFF_BAR = (size_t)GK_STAGES * GK_STAGE_BYTES;
-// barriers (full, empty, tfull, tempty, drain, tile ids), the TMEM address, the tile-id ring
-constexpr size_t GK_BAR_BYTES = (2 * GK_STAGES + 2 + 2 + 1 + GK_TRING) * 8 + 16 + GK_TRING * 4;
-constexpr size_t GK_SMEM = GK_OFF_BAR + 512 + 1024;  // + barrier area, + 1 KB alignment slack
-static_assert(GK_BAR_BYTES <= 512, "barrier area");
-
 struct GateParams {
   CUtensorMap tmx;  // hidden [T][H] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap tmw;  // Wt [L*128][H] bf16, box 64 x 256, 128B swizzle
+  CUtensorMap tmw;  // Wt [L*128][H] bf16, box 64 x 128, 128B swizzle
   int64_t T;
   int H, L, k;
   int npairs;       // ceil(L / 2)
-  int64_t ntiles;   // ceil(T / 128) * npairs
+  int64_t ntiles;   // ceil(T / 256) * npairs
   float* logits;    // [L][T][128] or nullptr
   uint8_t* topk;    // [L][T][k]
   uint32_t* status;
@@ -79,14 +53,6 @@ struct GateParams {
 };
 
 // ------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(tm), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // UMMA shared-memory descriptor: K-major operand tile with 128-byte swizzle
 // (rows of 128 bytes, 8-row groups 1024 bytes apart), sm_100 descriptor version.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
@@ -97,22 +63,6 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)1 << 46;                    // descriptor version
   d |= (uint64_t)2 << 61;                    // 128-byte swizzle
   return d;
-}
-
-// Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = 256.
-constexpr uint32_t GK_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GK_BN >> 3) << 17) |
-                              ((uint32_t)(GK_BM >> 4) << 24);
-
-__device__ __forceinline__ void umma_bf16(uint32_t dt, uint64_t a, uint64_t b, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
-      "l"(a), "l"(b), "r"(GK_IDESC), "r"(accum));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -253,145 +203,6 @@ template <int K>
 __device__ __forceinline__ void gate_drain_rows(const GateParams& p, uint32_t tacc, int64_t tok, int pair) {
 #pragma unroll 1
   for (int hl = 0; hl < 2; ++hl) gate_drain_layer<K>(p, tacc + (uint32_t)(hl * 128), tok, 2 * pair + hl);
-}
-
-// ----------------------------------------------------------------- kernel
-template <int K>
-__global__ void __launch_bounds__(GK_THREADS, 1) gate_topk_kernel(const __grid_constant__ GateParams p) {
-  extern __shared__ __align__(1024) char gsm_raw[];
-  // 1024-byte alignment of the stage ring (required by the 128-byte swizzle atoms)
-  char* gsm = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(gsm + GK_OFF_BAR);
-  uint64_t* empty = full + GK_STAGES;
-  uint64_t* tfull = empty + GK_STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint64_t* tid_full = drain + 1;  // [GK_TRING]: slot j % GK_TRING holds tile j's id
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tid_full + GK_TRING);
-  int* tile_ring = reinterpret_cast<int*>(tmem_slot + 4);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Tiles are handed out in order from one global counter, so at any moment
-  // the grid works on ~gridDim.x consecutive tiles, i.e. on few token blocks:
-  // each hidden-state panel comes from HBM once and is shared through L2 by
-  // the CTAs on its layers, however unevenly the CTAs progress.
-  const int nkb = p.H / GK_BK;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < GK_STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
-    }
-    mbar_init(drain, 1);
-    for (int i = 0; i < GK_TRING; ++i) mbar_init(&tid_full[i], 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(GK_TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      int64_t g = 0;
-      bool ok = true;
-      for (int64_t j = 0;; ++j) {
-        int t = ok ? (int)atomicAdd(p.tile_ctr, 1u) : -1;
-        if (t >= p.ntiles) t = -1;
-        tile_ring[j % GK_TRING] = t;
-        mbar_arrive(&tid_full[j % GK_TRING]);  // release: the id is visible to the waiters
-        if (t < 0) break;
-        const int mt = t / p.npairs, pair = t - mt * p.npairs;
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const int s = (int)(g % GK_STAGES);
-          if (g >= GK_STAGES && !mbar_wait(&empty[s], (uint32_t)((g / GK_STAGES - 1) & 1), p.status)) {
-            ok = false;
-            break;
-          }
-          char* st = gsm + (size_t)s * GK_STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[s], GK_STAGE_BYTES);
-          tma_load_2d(st, &p.tmx, kb * GK_BK, mt * GK_BM, &full[s]);
-          tma_load_2d(st + GK_A_BYTES, &p.tmw, kb * GK_BK, pair * GK_BN, &full[s]);
-        }
-      }
-      if (!ok) {
-        // wait (bounded) for the loads still in flight before leaving
-        for (int64_t q = (g > GK_STAGES ? g - GK_STAGES : 0); q < g; ++q)
-          mbar_wait(&full[q % GK_STAGES], (uint32_t)((q / GK_STAGES) & 1), nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    // --------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int64_t g = 0;
-      bool ok = true;
-      for (int64_t j = 0; ok; ++j) {
-        if (!mbar_wait(&tid_full[j % GK_TRING], (uint32_t)((j / GK_TRING) & 1), p.status)) {
-          ok = false;
-          break;
-        }
-        if (tile_ring[j % GK_TRING] < 0) break;
-        const int a = (int)(j & 1);
-        if (j >= 2 && !mbar_wait(&tempty[a], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t dt = tmem + (uint32_t)(a * GK_BN);
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const int s = (int)(g % GK_STAGES);
-          if (!mbar_wait(&full[s], (uint32_t)((g / GK_STAGES) & 1), p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(gsm + (size_t)s * GK_STAGE_BYTES);
-          const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + GK_A_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < GK_BK / 16; ++kk)  // K = 16 per instruction: 32 bytes along the row
-            umma_bf16(dt, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), (kb | kk) ? 1u : 0u);
-          umma_commit(&empty[s]);
-        }
-        if (ok) umma_commit(&tfull[a]);
-      }
-      // all MMAs this thread issued have completed once this commit arrives
-      umma_commit(drain);
-      mbar_wait(drain, 0, nullptr);
-    }
-  } else {
-    // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;   // token row within the tile
-    for (int64_t j = 0;; ++j) {
-      if (!mbar_wait(&tid_full[j % GK_TRING], (uint32_t)((j / GK_TRING) & 1), p.status)) break;
-      const int t = tile_ring[j % GK_TRING];
-      if (t < 0) break;
-      const int a = (int)(j & 1);
-      if (!mbar_wait(&tfull[a], (uint32_t)((j >> 1) & 1), p.status)) break;
-      tc_fence_after();
-      const int mt = t / p.npairs, pair = t - mt * p.npairs;
-      const int64_t tok = (int64_t)mt * GK_BM + row;
-      gate_drain_rows<K>(p, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * GK_BN), tok, pair);
-      // accumulator drained: hand it back to the MMA warp
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[a]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(GK_TMEM_COLS));
 }
 
 // ------------------------------------------------- CTA-pair (cta_group::2)
@@ -759,20 +570,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)GK_BK, box_rows};
+  const cuuint32_t box[2] = {(cuuint32_t)GP_BK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int K>
-cudaError_t gate_launch_k(const GateParams& p, int grid, cudaStream_t st) {
-  static std::atomic<unsigned long long> set{0};
-  const cudaError_t e = smem_optin(gate_topk_kernel<K>, (int)GK_SMEM, set);
-  if (e != cudaSuccess) return e;
-  gate_topk_kernel<K><<<grid, GK_THREADS, GK_SMEM, st>>>(p);
-  return cudaGetLastError();
 }
 
 cudaLaunchConfig_t pair_config(int clusters, cudaStream_t st, cudaLaunchAttribute* at) {
@@ -834,16 +636,10 @@ moer_status gate_topk_launch(const moer_dims* d, const uint16_t* hidden, int64_t
   gate_transpose_kernel<<<tg, tb, 0, st>>>(w_gate, wt, d->L, H, 128);
   if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
   GateParams p;
-#if MOER_GATE_PAIR
   // CTA pairs: 256 tokens per tile, each CTA loads its 128 tokens and one layer's weights
   if (!make_map(&p.tmx, hidden, (uint64_t)T, (uint64_t)H, GP_BM)) return MOER_ECUDA;
   if (!make_map(&p.tmw, wt, (uint64_t)d->L * 128, (uint64_t)H, GP_BN / 2)) return MOER_ECUDA;
   const int64_t tile_tokens = 2 * GP_BM;
-#else
-  if (!make_map(&p.tmx, hidden, (uint64_t)T, (uint64_t)H, GK_BM)) return MOER_ECUDA;
-  if (!make_map(&p.tmw, wt, (uint64_t)d->L * 128, (uint64_t)H, GK_BN)) return MOER_ECUDA;
-  const int64_t tile_tokens = GK_BM;
-#endif
   p.T = T;
   p.H = H;
   p.L = d->L;
@@ -859,12 +655,7 @@ moer_status gate_topk_launch(const moer_dims* d, const uint16_t* hidden, int64_t
   // the counter runs past ntiles by at most one fetch per producer
   if (p.ntiles + sms >= (int64_t(1) << 31)) return MOER_ERANGE;
   if (cudaMemsetAsync(p.tile_ctr, 0, sizeof(uint32_t), st) != cudaSuccess) return MOER_ECUDA;
-#if MOER_GATE_PAIR
   const cudaError_t e = d->k == 8 ? gate_pair_launch_k<8>(p, st) : gate_pair_launch_k<6>(p, st);
-#else
-  const int grid = (int)min64(p.ntiles, sms);
-  const cudaError_t e = d->k == 8 ? gate_launch_k<8>(p, grid, st) : gate_launch_k<6>(p, grid, st);
-#endif
   return e == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
