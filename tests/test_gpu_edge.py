@@ -198,3 +198,48 @@ def test_stitch_bad_cache_offsets_are_reported(env, rco_vals):
     nat.moer_block_stitch(dims, blk, tab, 2, rbo, 1, cidx, 1, rco, cache, 3, None, out, ws, 256)
     assert nat.moer_ws_status(ws) == 0
     assert (out == 11).all()
+
+
+@pytest.mark.parametrize("m,E", [(26, 128), (3, 4), (2, 8), (12, 128)])
+def test_stitch_record_shapes(env, m, E):
+    """moer_block_stitch against O3 on records of every launch shape: 26 x 128 counts
+    (3,328 B: two thread groups per request), 3 x 4 and 2 x 8 (12 and 16 B: 4-byte words /
+    16-byte words with one word per record), and 12 x 128 (the path's).  Ragged requests,
+    cached prefixes read from pre-filled slots, full blocks inserted into fresh slots."""
+    torch, nat = env
+    orc = oracle.get()
+    B, R = 16, 50
+    rs = np.random.RandomState(m * 1000 + E)
+    lens = rs.randint(1, 120, size=R)
+    req_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tab, rbo = [], [0]
+    for r in range(R):
+        for t0 in range(req_off[r], req_off[r + 1], B):
+            tab.append((t0, min(B, req_off[r + 1] - t0)))
+        rbo.append(len(tab))
+    tab = np.array(tab, dtype=np.int32)
+    nblk = len(tab)
+    blk = rs.randint(0, B + 1, size=(nblk, m, E)).astype(np.uint8)
+    npre = 40
+    ncache = rs.randint(0, 6, size=R)
+    rco = np.concatenate([[0], np.cumsum(ncache)]).astype(np.int32)
+    cidx = rs.randint(0, npre, size=int(rco[-1])).astype(np.int32)
+    full = tab[:, 1] == B
+    ins = np.full(nblk, -1, dtype=np.int32)
+    ins[full] = npre + np.arange(int(full.sum()))
+    ins[rs.random_sample(nblk) < 0.2] = -1                 # some full blocks are not cached
+    nslots = npre + int(full.sum())
+    cache0 = np.zeros((nslots, m, E), dtype=np.uint8)
+    cache0[:npre] = rs.randint(0, B + 1, size=(npre, m, E))
+    dims = nat.make_dims(E, 1, m, list(range(m)), B)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    cache = d(cache0)
+    out = torch.empty((R, m, E), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    nat.moer_block_stitch(dims, d(blk), d(tab.reshape(-1)), nblk, d(np.array(rbo, np.int32)), R,
+                          d(cidx), len(cidx), d(rco), cache, nslots, d(ins), out, ws, 256)
+    assert nat.moer_ws_status(ws) == 0
+    ocache = cache0.copy()
+    ref = orc.stitch(blk, req_off, B, cidx, rco, ocache, ins)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert np.array_equal(cache.cpu().numpy(), ocache)

@@ -55,13 +55,18 @@ def _run(env, cnt, idf, cen, tau, loads, live):
     return sig.cpu().numpy(), dist.cpu().numpy(), ch.cpu().numpy(), dl.cpu().numpy()
 
 
-CASES = [  # (tau, D, live, equal loads)
+CASES = [  # (tau, D, live, equal loads); D > 16 and D > 32 take the wider kernels
     (0.0, 8, False, False),
     (1e6, 8, False, False),
     (0.1, 1, False, False),
     (0.1, 16, False, True),
     (0.05, 16, True, True),
     (1e6, 4, True, False),
+    (0.1, 40, False, False),
+    (0.1, 40, True, False),
+    (0.3, 64, False, True),
+    (0.3, 64, True, True),
+    (1e6, 64, True, False),
 ]
 
 
@@ -126,3 +131,21 @@ def test_route_undefined_distances(env, live):
     assert np.array_equal(loads, loads0)
     och, oloads = orc.route(dist.astype(np.float64), 0.1, loads0, live)
     assert (och == -1).all() and np.array_equal(oloads, loads0)
+
+
+@pytest.mark.parametrize("D", [16, 48])
+def test_route_live_across_staging_buffers(env, D):
+    """5,000 requests in one live call: route_live stages the band masks 2,048 at a time in
+    two alternating buffers, so decisions cross two buffer hand-overs.  Loads start unequal;
+    every pick must follow the oracle until the first band-edge divergence."""
+    orc = oracle.get()
+    R, m, E = 5000, 2, 64
+    cnt, idf, cen = _inputs(900 + D, R, m, E, D)
+    loads0 = np.random.RandomState(D).randint(0, 40, size=D).astype(np.int32)
+    sig, dist, ch, loads = _run(env, cnt, idf, cen, 0.1, loads0, True)
+    _, odist = orc.sig_dist(cnt, idf, cen)
+    gu.assert_close(dist, odist, "distance")
+    och, oloads = orc.route(odist, 0.1, loads0, True)
+    gu.check_live_route(ch, odist, 0.1, loads0, och)
+    assert np.array_equal(np.bincount(ch, minlength=D) + loads0, loads)
+    assert loads.sum() == loads0.sum() + R
