@@ -99,13 +99,16 @@ def measured_peaks() -> dict:
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    """nvidia-smi every 50 ms while the bench runs; samples are timestamped, and those taken
+    between mark_start() and mark_stop() (the timed region) are the ones reported."""
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
         self.path = os.path.join("/tmp", f"moer_clocks_{os.getpid()}.csv")
 
     def start(self):
@@ -113,39 +116,53 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
+    def mark_start(self):
+        import datetime
+        self.t0 = datetime.datetime.now()
+
+    def mark_stop(self):
+        import datetime
+        self.t1 = datetime.datetime.now()
+
     def stop(self) -> dict:
+        import datetime
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)  # one more sample after the region
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for ln in f:
                 c = [x.strip() for x in ln.split(",")]
-                if len(c) < 9:
+                if len(c) < 10:
                     continue
                 try:
-                    sm.append(float(c[1]))
-                    smax.append(float(c[2]))
+                    ts = datetime.datetime.strptime(c[0], "%Y/%m/%d %H:%M:%S.%f")
+                    rows.append((ts, float(c[2]), float(c[3]), float(c[4]),
+                                 {n for n, v in zip(names, c[6:10]) if v.lower().startswith("active")}))
                 except ValueError:
                     continue
-                for n, v in zip(names, c[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
-                "reasons": sorted(reasons)}
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1 + datetime.timedelta(milliseconds=50)]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = sorted(set().union(*[r[4] for r in use]))
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "power_w_max": max(r[3] for r in use), "samples": len(use),
+                "samples_in_timed_region": len(inside), "reasons": reasons}
 
 
 # ------------------------------------------------------------- distributed
@@ -405,6 +422,7 @@ def measure_stream(args, device, dist, stream, with_e2e=False, parity=None):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    clocks.mark_start()
     for i, (b, (a, z)) in enumerate(zip(batches, chunks)):
         bd = pipeline.BatchDev.from_host(b, device=device)
         view = flat[:wl.L * b.T * wl.E].view(wl.L, b.T, wl.E)
@@ -430,6 +448,7 @@ def measure_stream(args, device, dist, stream, with_e2e=False, parity=None):
         torch.cuda.synchronize()
         choice[a:z] = choice_host[:b.R].numpy()
         gdist[a:z] = rs.dist[:b.R].cpu().numpy()
+    clocks.mark_stop()
     clk = clocks.stop()
     if rs.status() != 0:
         raise RuntimeError("device-side status after the stream is not OK")
@@ -604,6 +623,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    clocks.mark_start()
     start.record(stream)
     for i in range(args.steps):
         rs.ensure(bd.T, bd.nblk, bd.R)
@@ -616,6 +636,7 @@ def run_gpu(args):
         rs.route(bd.R)
     stop.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_stop()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
@@ -767,6 +788,7 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    clocks.mark_start()
     start.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
@@ -778,6 +800,7 @@ def measure_gate(args, device, dist, stream, steps, with_e2e):
         rs.route(bd.R)
     stop.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_stop()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
@@ -1221,7 +1244,7 @@ def cpu_baseline_all_cores(cfg, wl, nreq_per_core, parity=None, over=None):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["own", "reference"], default="own")
     ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
@@ -1241,7 +1264,7 @@ def main(argv=None):
     ap.add_argument("--gate", dest="gate", action="store_true", default=True,
                     help="also measure the gate path (moer_gate_topk first) into gate_path")
     ap.add_argument("--no-gate", dest="gate", action="store_false")
-    ap.add_argument("--gate-steps", type=int, default=10)
+    ap.add_argument("--gate-steps", type=int, default=30)
     ap.add_argument("--kmeans", dest="kmeans", action="store_true", default=True,
                     help="also time the calibration fit (balanced K-means) into kmeans_fit")
     ap.add_argument("--no-kmeans", dest="kmeans", action="store_false")
