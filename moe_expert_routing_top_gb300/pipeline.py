@@ -309,3 +309,63 @@ def calibrate(E, k, L, block, logits, bd: BatchDev, req_off, *, m, D, G, seed_ro
     return Calibration(mask=mask, mask_order=order, quality=quality.cpu().numpy(), idf=idf_m, sig=sig,
                        centroids=cent, assign=assign, kmeans_info=info.cpu().numpy(), affinity=aff,
                        group_of=group_of, knee=knee.cpu().numpy())
+
+
+# ---------------------------------------------------------------- artefacts
+CALIB_MAGIC = b"MOERCAL1"
+CALIB_VERSION = 1
+_CALIB_HEADER = "<8s8Id"  # magic, version, E, k, L, m, D, G, block, tau
+
+
+def save_calibration(path, cal: Calibration, *, E, k, L, block, G, tau) -> None:
+    """Writes what serving needs from a calibration, as little-endian binary: a header
+    (magic, version, E, k, L, m, D, G, block, tau), then the mask int32 [m], idf fp32 [m][E],
+    centroids fp32 [D][m*E] and expert groups int32 [L][E], then a CRC-32 of all of it.
+    The calibration must be refitted when the model, the traffic or the decoder count changes;
+    the file only carries it from the offline fit to the serving process."""
+    import struct
+    import zlib
+    mask = np.ascontiguousarray(cal.mask, dtype="<i4")
+    idf = np.ascontiguousarray(cal.idf.cpu().numpy() if torch.is_tensor(cal.idf) else cal.idf, dtype="<f4")
+    cen = np.ascontiguousarray(cal.centroids.cpu().numpy() if torch.is_tensor(cal.centroids) else cal.centroids,
+                               dtype="<f4")
+    grp = np.ascontiguousarray(cal.group_of.cpu().numpy() if torch.is_tensor(cal.group_of) else cal.group_of,
+                               dtype="<i4")
+    m, D = int(mask.shape[0]), int(cen.shape[0])
+    if idf.shape != (m, E) or cen.shape != (D, m * E) or grp.shape != (L, E):
+        raise ValueError("calibration arrays do not match E, L and the mask")
+    if grp.size and (grp.min() < 0 or grp.max() >= G):
+        raise ValueError("expert group ids outside [0, G)")
+    body = struct.pack(_CALIB_HEADER, CALIB_MAGIC, CALIB_VERSION, E, k, L, m, D, G, block, float(tau))
+    body += mask.tobytes() + idf.tobytes() + cen.tobytes() + grp.tobytes()
+    with open(path, "wb") as f:
+        f.write(body + struct.pack("<I", zlib.crc32(body)))
+
+
+def load_calibration(path) -> dict:
+    """Reads a file written by save_calibration; raises ValueError when the magic, the
+    version, the sizes or the CRC do not match.  Returns the header fields and host arrays
+    (mask, idf, centroids, group_of), ready for RoutingStats."""
+    import struct
+    import zlib
+    with open(path, "rb") as f:
+        data = f.read()
+    hs = struct.calcsize(_CALIB_HEADER)
+    if len(data) < hs + 4:
+        raise ValueError("calibration file too short")
+    magic, ver, E, k, L, m, D, G, block, tau = struct.unpack_from(_CALIB_HEADER, data, 0)
+    if magic != CALIB_MAGIC or ver != CALIB_VERSION:
+        raise ValueError("not a calibration file of this version")
+    sizes = [m * 4, m * E * 4, D * m * E * 4, L * E * 4]
+    if len(data) != hs + sum(sizes) + 4:
+        raise ValueError("calibration file size does not match its header")
+    (crc,) = struct.unpack_from("<I", data, len(data) - 4)
+    if zlib.crc32(data[:-4]) != crc:
+        raise ValueError("calibration file checksum mismatch")
+    off = hs
+    out = {"E": E, "k": k, "L": L, "m": m, "D": D, "G": G, "block": block, "tau": tau}
+    for name, n, dt, shape in (("mask", sizes[0], "<i4", (m,)), ("idf", sizes[1], "<f4", (m, E)),
+                               ("centroids", sizes[2], "<f4", (D, m * E)), ("group_of", sizes[3], "<i4", (L, E))):
+        out[name] = np.frombuffer(data, dtype=dt, count=n // 4, offset=off).reshape(shape).astype(dt[1:])
+        off += n
+    return out

@@ -11,7 +11,9 @@ plan (GRACE-MoE sections 4.2-4.3).
 
 The oracle chain runs on the same inputs: O1 -> O2/O3 -> O9 -> the mask oracle ->
 O2/O3/O9 -> O4 -> the K-means oracle; O7 -> the grouping oracle; then O1-O8 and the
-replication oracle on the served requests.  Where the greedy mask meets a near-tie (two
+replication oracle on the served requests.  The calibrated mask, idf, centroids and
+groups reach the serving side through the artefact file (save_calibration /
+load_calibration), as they would between the offline fit and the server.  Where the greedy mask meets a near-tie (two
 layers within 1e-12), the oracle chain adopts the GPU's layer and goes on; K-means runs
 on the GPU's fp32 signatures on both sides (they agree with the oracle's to 1e-5), so its
 assignments must be identical.
@@ -55,7 +57,7 @@ def _mask_agrees(tk, req_off, E, m, idf32, got_order):
 
 
 @pytest.mark.parametrize("cfg,ncal,nserve", [("c3", 96, 10), ("c2", 64, 12)])
-def test_calibration_chain(env, cfg, ncal, nserve):
+def test_calibration_chain(env, cfg, ncal, nserve, tmp_path):
     torch, pipeline, gu = env
     orc = oracle.get()
     served = gen.make_workload(cfg, R=nserve)
@@ -105,9 +107,15 @@ def test_calibration_chain(env, cfg, ncal, nserve):
     print(f"{cfg} calibration: mask {mask.tolist()}, K-means {steps} steps, "
           f"{gapped} of {L} layers with a clear eigengap")
 
-    # ---- online, with the calibrated inputs
-    served.mask, served.idf = mask.astype(np.int32), gu.host(got.idf)
-    served.centroids, served.group_of = cent, groups
+    # ---- online, with the calibrated inputs carried through the artefact file
+    path = tmp_path / f"{cfg}.cal"
+    pipeline.save_calibration(path, got, E=E, k=k, L=L, block=B, G=G, tau=served.tau)
+    art = pipeline.load_calibration(path)
+    assert (art["E"], art["k"], art["L"], art["m"], art["D"], art["block"]) == (E, k, L, m, D, B)
+    assert np.array_equal(art["mask"], mask) and np.array_equal(art["idf"], gu.host(got.idf))
+    assert np.array_equal(art["centroids"], cent) and np.array_equal(art["group_of"], groups)
+    served.mask, served.idf = art["mask"], art["idf"]
+    served.centroids, served.group_of = art["centroids"], art["group_of"]
     b = served.batch()
     rs = pipeline.RoutingStats.for_workload(served, max_T=b.T, max_nblk=b.nblk, max_R=b.R)
     rs.step(gu.device_logits(served, b), pipeline.BatchDev.from_host(b))
