@@ -9,12 +9,18 @@
 // the KV blocks; per block the warp reads the block's top-k ids of up to sixteen
 // mask layers at once (contiguous uint8, len * k bytes per layer, as 4-byte
 // words when k is a multiple of 4), counts them into private shared-memory
-// rows of packed 8-bit counters (four
-// experts per 32-bit word; a count never exceeds B <= 255) and writes the row
-// out with coalesced 32-bit stores.  No global atomics, no pre-zeroing.  The
-// block table is validated on the fly: a block whose length is outside
-// [1, B], that runs past T or that does not start where the previous block
-// ends is skipped and recorded as MOER_EDATA.
+// rows of packed 8-bit counters (four experts per 32-bit word; a count never
+// exceeds B <= 255) and writes the row out with coalesced 32-bit stores.  No
+// global atomics, no pre-zeroing.
+//
+// Each layer's row is 256 bytes whatever E is, so the counter word of id e
+// sits at byte (e & ~3) of the row for every byte value e: an id >= E lands
+// in the row's tail, which the checked form reads back as MOER_EDATA instead
+// of testing every id.  With 256-byte-aligned rows, the address of an id's
+// word is one byte permute of the row base and the id word, and its increment
+// (1 << 8 (e & 3)) one funnel shift.  The block table is validated on the fly:
+// a block whose length is outside [1, B], that runs past T or that does not
+// start where the previous block ends is skipped and recorded as MOER_EDATA.
 #include "common.cuh"
 
 namespace moer {
@@ -34,17 +40,55 @@ struct BcParams {
 
 constexpr int BC_MC = 16;  // mask layers counted together (their loads in flight at once)
 
+constexpr int BC_ROW = 256;  // bytes per layer row of counters (64 words)
+
+// red.shared.add of `inc` at shared address `addr` + IMM
+template <int IMM>
+__device__ __forceinline__ void bc_add(uint32_t addr, uint32_t inc) {
+  asm volatile("red.shared.add.u32 [%0+%1], %2;" ::"r"(addr), "n"(IMM), "r"(inc) : "memory");
+}
+
+// The four ids packed in `v` counted into the layer row at `row` (256-aligned).
+template <int IMM>
+__device__ __forceinline__ void bc_count_word(uint32_t row, uint32_t v) {
+  const uint32_t offs = v & 0xFCFCFCFCu;          // byte offset of each id's counter word
+  const uint32_t shp = (v << 3) & 0x18181818u;    // 8 (e & 3) in each byte
+  // byte j of offs into the low byte of the row base
+  const uint32_t a0 = __byte_perm(offs, row, 0x7650), a1 = __byte_perm(offs, row, 0x7651);
+  const uint32_t a2 = __byte_perm(offs, row, 0x7652), a3 = __byte_perm(offs, row, 0x7653);
+  // 1 << (shift & 31): the wrapping funnel shift reads only the low five bits of its amount
+  bc_add<IMM>(a0, __funnelshift_l(0u, 1u, shp));
+  bc_add<IMM>(a1, __funnelshift_l(0u, 1u, shp >> 8));
+  bc_add<IMM>(a2, __funnelshift_l(0u, 1u, shp >> 16));
+  bc_add<IMM>(a3, __funnelshift_l(0u, 1u, shp >> 24));
+}
+
+template <int II>
+__device__ __forceinline__ void bc_count_layers(uint32_t base, const uint32_t (&v)[BC_MC], int nl, bool in) {
+  if constexpr (II < BC_MC) {
+    if (II < nl && in) bc_count_word<II * BC_ROW>(base, v[II]);
+    bc_count_layers<II + 1>(base, v, nl, in);
+  }
+}
+
 // CHECK: the ids come from the caller (moer_ids_signature); an id >= E is
-// skipped and recorded as MOER_EDATA instead of being counted.
+// not counted (it lands in the row's tail) and is recorded as MOER_EDATA.
 template <bool CHECK>
 __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __grid_constant__ BcParams p) {
-  extern __shared__ uint32_t bc_smem[];  // [BC_WARPS][BC_MC][E / 4]
+  extern __shared__ uint8_t bc_raw[];  // [BC_WARPS][min(m, BC_MC)][256 bytes], 256-byte aligned
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wpb = p.E / 4;
-  uint32_t* cnt = bc_smem + warp * BC_MC * wpb;
+  const int nrows = min(p.m, BC_MC);
+  const uint32_t base = ((smem_u32(bc_raw) + (BC_ROW - 1)) & ~(uint32_t)(BC_ROW - 1)) + warp * nrows * BC_ROW;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(bc_raw + (base - smem_u32(bc_raw)));
+  constexpr int RW = BC_ROW / 4;  // words per layer row
+  const int wpb = p.E / 4;        // words holding the E experts
+  const int rw = CHECK ? RW : wpb;  // words written, read back and cleared per row
+  for (int w = lane; w < nrows * RW; w += 32) cnt[w] = 0u;
+  __syncwarp();
   const int64_t stride = (int64_t)gridDim.x * BC_WARPS;
   // 4-byte loads when every block's id row starts on a 4-byte boundary
   const bool vec = (p.k % 4) == 0;
+  uint32_t bad = 0u;
   // persistent warps, one KV block at a time, all mask layers of the block
   for (int64_t bb = (int64_t)blockIdx.x * BC_WARPS + warp; bb < p.nblk; bb += stride) {
     const int b = (int)bb;
@@ -64,8 +108,6 @@ __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __gri
     const int n = ln * p.k;
     for (int i0 = 0; i0 < p.m; i0 += BC_MC) {
       const int nl = min(BC_MC, p.m - i0);
-      for (int w = lane; w < nl * wpb; w += 32) cnt[w] = 0u;
-      __syncwarp();
       if (vec) {
         const int nw = n >> 2;
         for (int q0 = 0; q0 < nw; q0 += 32) {
@@ -79,44 +121,34 @@ __global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __gri
               v[ii] = reinterpret_cast<const uint32_t*>(src)[q];
             }
           }
-#pragma unroll
-          for (int ii = 0; ii < BC_MC; ++ii) {
-            if (ii < nl && q < nw) {
-              uint32_t* c = cnt + ii * wpb;
-#pragma unroll
-              for (int by = 0; by < 4; ++by) {
-                const int e = (v[ii] >> (8 * by)) & 0xFF;
-                if (CHECK && e >= p.E) {
-                  atomicOr(p.status, WS_BIT_EDATA);
-                  continue;
-                }
-                atomicAdd(&c[e >> 2], 1u << ((e & 3) * 8));
-              }
-            }
-          }
+          bc_count_layers<0>(base, v, nl, q < nw);
         }
       } else {
         for (int ii = 0; ii < nl; ++ii) {
           const uint8_t* src = p.ids + (int64_t)p.layer_row[i0 + ii] * p.layer_stride + (int64_t)t0 * p.k;
-          uint32_t* c = cnt + ii * wpb;
+          const uint32_t row = base + ii * BC_ROW;
           for (int j = lane; j < n; j += 32) {
-            const int e = src[j];
-            if (CHECK && e >= p.E) {
-              atomicOr(p.status, WS_BIT_EDATA);
-              continue;
-            }
-            atomicAdd(&c[e >> 2], 1u << ((e & 3) * 8));
+            const uint32_t e = src[j];
+            bc_add<0>(row + (e & ~3u), 1u << ((e & 3u) * 8u));
           }
         }
       }
       __syncwarp();
       for (int ii = 0; ii < nl; ++ii) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(p.blk_cnt + ((size_t)b * p.m + i0 + ii) * p.E);
-        for (int w = lane; w < wpb; w += 32) dst[w] = cnt[ii * wpb + w];
+        for (int w = lane; w < rw; w += 32) {
+          const uint32_t c = cnt[ii * RW + w];
+          cnt[ii * RW + w] = 0u;
+          if (w < wpb)
+            dst[w] = c;
+          else
+            bad |= c;
+        }
       }
       __syncwarp();
     }
   }
+  if (CHECK && bad != 0u) atomicOr(p.status, WS_BIT_EDATA);
 }
 
 // ids: either the caller's [L][T][k] top-k (mask_only = false: row block of
@@ -143,7 +175,7 @@ moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mas
   const int sms = device_sm_count();
   if (sms <= 0) return MOER_ECUDA;
   const int64_t grid = min64(((int64_t)nblk + BC_WARPS - 1) / BC_WARPS, (int64_t)sms * 8);
-  const size_t smem = BC_WARPS * BC_MC * (d->E / 4) * sizeof(uint32_t);
+  const size_t smem = (size_t)BC_WARPS * min(d->m, BC_MC) * BC_ROW + BC_ROW;  // + alignment slack
   if (check)
     block_counts_kernel<true><<<(unsigned)grid, BC_WARPS * 32, smem, st>>>(p);
   else
@@ -198,6 +230,40 @@ __device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* 
   }
   for (int c = threadIdx.x; c < E * rs; c += AI_THREADS) tile[c] = 0;
   __syncthreads();
+}
+
+// Any byte of x zero: the classic borrow test, exact as an "any" test (a false
+// high bit only ever appears above a real zero byte).  Accumulated with OR and
+// masked once: acc |= (x - 0x01010101) & ~x.
+__device__ __forceinline__ uint32_t zero_byte_acc(uint32_t acc, uint32_t x) {
+  return acc | ((x - 0x01010101u) & ~x);
+}
+
+// A row of K = 6 or 8 ids packed in two words (ids 0-3 in w0, ids 4.. in w1)
+// is usable for the co-activation when every id is below E (<= 128) and the K
+// ids are distinct.  Range: per byte, (x | 0x80) - E keeps the high bit only
+// when x & 0x7F >= E; x >= 128 is caught by x's own high bit.  Distinctness:
+// every pair of bytes compared once by XOR against byte rotations of the
+// words (within a word by 8 and 16 bits, across the words by 0, 8, 16 and 24
+// bits) and a zero-byte test.  With K = 6 the two unused bytes of w1 hold
+// 0xFE and 0xFF, which differ from each other and from every id below E.
+template <int K>
+__device__ __forceinline__ bool ids_row_ok(uint32_t w0, uint32_t w1, int E) {
+  static_assert(K == 6 || K == 8, "rows of 6 or 8 ids");
+  if constexpr (K == 6) w1 &= 0xFFFFu;
+  const uint32_t E4 = (uint32_t)E * 0x01010101u;
+  const uint32_t hi = (((w0 | 0x80808080u) - E4) | w0) | (((w1 | 0x80808080u) - E4) | w1);
+  if constexpr (K == 6) w1 |= 0xFFFE0000u;
+  uint32_t z = 0u;
+  z = zero_byte_acc(z, w0 ^ __funnelshift_l(w0, w0, 8));
+  z = zero_byte_acc(z, w0 ^ __funnelshift_l(w0, w0, 16));
+  z = zero_byte_acc(z, w1 ^ __funnelshift_l(w1, w1, 8));
+  z = zero_byte_acc(z, w1 ^ __funnelshift_l(w1, w1, 16));
+  z = zero_byte_acc(z, w0 ^ w1);
+  z = zero_byte_acc(z, w0 ^ __funnelshift_l(w1, w1, 8));
+  z = zero_byte_acc(z, w0 ^ __funnelshift_l(w1, w1, 16));
+  z = zero_byte_acc(z, w0 ^ __funnelshift_l(w1, w1, 24));
+  return ((hi | z) & 0x80808080u) == 0u;
 }
 
 // CHECK: the ids come from the caller (moer_ids_signature); a row holding an
@@ -257,20 +323,7 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
 #pragma unroll
         for (int j = 0; j < K; ++j) e[j] = (w[u][j / 4] >> (8 * (j % 4))) & 0xFF;
         if constexpr (CHECK) {
-          // K distinct ids below E: their bits in a 256-bit set number exactly K
-          unsigned long long m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-          bool inrange = true;
-#pragma unroll
-          for (int j = 0; j < K; ++j) {
-            inrange = inrange && e[j] < E;
-            const unsigned long long bit = 1ull << (e[j] & 63);
-            const int q = e[j] >> 6;
-            m0 |= q == 0 ? bit : 0ull;
-            m1 |= q == 1 ? bit : 0ull;
-            m2 |= q == 2 ? bit : 0ull;
-            m3 |= q == 3 ? bit : 0ull;
-          }
-          if (!inrange || __popcll(m0) + __popcll(m1) + __popcll(m2) + __popcll(m3) != K) {
+          if (!ids_row_ok<K>(w[u][0], w[u][1], E)) {
             atomicOr(status, WS_BIT_EDATA);
             continue;
           }

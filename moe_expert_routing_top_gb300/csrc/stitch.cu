@@ -12,6 +12,7 @@
 // insert copies one block record per warp, and a request's record of m*E
 // counts is summed by one CTA whose threads own consecutive words, so every
 // load and store is coalesced.
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -39,6 +40,11 @@ __global__ void stitch_insert(const V* __restrict__ blk_w, const int32_t* __rest
   }
 }
 
+// block loads in flight per thread: 8 words of 4 bytes or 4 of 16 bytes (the
+// sixteen 32-bit sums of a 16-byte word leave no registers for more)
+template <typename V>
+__host__ __device__ constexpr int stitch_su() { return sizeof(V) == 16 ? 4 : 8; }
+
 __device__ __forceinline__ void acc4(uint32_t (&a)[4], uint32_t v) {
   a[0] += v & 0xFFu;
   a[1] += (v >> 8) & 0xFFu;
@@ -56,16 +62,18 @@ __device__ __forceinline__ void accv(uint32_t (&a)[16], uint4 v) {
 
 // One CTA per request, S groups of TW threads: thread (s, w) sums word w of
 // the record (16 or 4 bytes of packed 8-bit counts) over the request's cached
-// blocks s, s + S, ... and computed blocks s, s + S, ..., four block loads in
+// blocks s, s + S, ... and computed blocks s, s + S, ..., SU block loads in
 // flight; group 0 adds the S partial sums (through shared memory, laid out
 // [S][NB][TW] so every access is conflict-free) and writes the request's row.
-// With S groups a request's ~80 blocks keep S times as many loads in flight.
+// The kernel's length is set by its longest requests (a few hundred blocks):
+// S groups with SU loads each keep S * SU of their blocks in flight at once.
 template <typename V, int NB, int S>
 __global__ void __launch_bounds__(1024) stitch_sum(const V* __restrict__ blk_w, int nblk, const int32_t* __restrict__ req_blk_off,
                            const int32_t* __restrict__ cache_idx, int ncached,
                            const int32_t* __restrict__ req_cache_off, const V* __restrict__ cache_w, int nslots,
                            int rec_v, int32_t* __restrict__ req_cnt, uint32_t* status) {
   extern __shared__ uint32_t part[];  // [S][NB][TW] partial sums
+  constexpr int SU = stitch_su<V>();
   const int TW = blockDim.x / S;
   const int grp = threadIdx.x / TW, wl = threadIdx.x - grp * TW;
   const int r = blockIdx.x;
@@ -82,23 +90,32 @@ __global__ void __launch_bounds__(1024) stitch_sum(const V* __restrict__ blk_w, 
 #pragma unroll
     for (int i = 0; i < NB; ++i) a[i] = 0u;
     if (w < rec_v) {
-      for (int c = c0 + grp; c < c1; c += S) {
-        const int slot = cache_idx[c];
-        if (slot < 0 || slot >= nslots) {
-          if (status != nullptr) atomicOr(status, WS_BIT_EDATA);
-          continue;
+      // cached prefix blocks: SU slot numbers, then their SU records, in flight together
+      for (int c = c0 + grp; c < c1; c += SU * S) {
+        int slot[SU];
+#pragma unroll
+        for (int u = 0; u < SU; ++u) slot[u] = c + u * S < c1 ? cache_idx[c + u * S] : -2;
+        V v[SU];
+#pragma unroll
+        for (int u = 0; u < SU; ++u)
+          if (slot[u] >= 0 && slot[u] < nslots) v[u] = cache_w[(size_t)slot[u] * rec_v + w];
+#pragma unroll
+        for (int u = 0; u < SU; ++u) {
+          if (slot[u] >= 0 && slot[u] < nslots) {
+            accv(a, v[u]);
+          } else if (slot[u] != -2 && status != nullptr) {
+            atomicOr(status, WS_BIT_EDATA);
+          }
         }
-        accv(a, cache_w[(size_t)slot * rec_v + w]);
       }
       if (!bad_blocks) {
         int b = b0 + grp;
-        for (; b + 3 * S < b1; b += 4 * S) {
-          const V v0 = blk_w[(size_t)b * rec_v + w], v1 = blk_w[(size_t)(b + S) * rec_v + w];
-          const V v2 = blk_w[(size_t)(b + 2 * S) * rec_v + w], v3 = blk_w[(size_t)(b + 3 * S) * rec_v + w];
-          accv(a, v0);
-          accv(a, v1);
-          accv(a, v2);
-          accv(a, v3);
+        for (; b + (SU - 1) * S < b1; b += SU * S) {
+          V v[SU];
+#pragma unroll
+          for (int u = 0; u < SU; ++u) v[u] = blk_w[(size_t)(b + u * S) * rec_v + w];
+#pragma unroll
+          for (int u = 0; u < SU; ++u) accv(a, v[u]);
         }
         for (; b < b1; b += S) accv(a, blk_w[(size_t)b * rec_v + w]);
       }
@@ -152,30 +169,34 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
                                                     nslots, rec_bytes / 4, status);
     if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
   }
-  // TW threads per group cover the record's words; four groups when the partial sums fit
-  // in 48 KB of shared memory, else two
-  auto launch_sum = [&](auto vtag, auto nbtag) {
+  // TW threads per group cover the record's words, four groups (at most 1,024 threads,
+  // partial sums within 64 KB of shared memory).  Eight groups of up to 96 threads were
+  // slower on the Qwen3-shaped batch (0.096 against 0.088 ms for the stitch call): fewer
+  // requests resident per SM.
+  auto launch_sum = [&](auto vtag, auto nbtag) -> cudaError_t {
     using V = decltype(vtag);
     constexpr int NB = decltype(nbtag)::value;
     const int rec_v = rec_bytes / (int)sizeof(V);
     const int tw = rec_v >= 256 ? 256 : ((rec_v + 31) / 32) * 32;
-    const size_t smem4 = (size_t)4 * NB * tw * sizeof(uint32_t);
-    if (smem4 <= 48 * 1024)
-      stitch_sum<V, NB, 4><<<R, 4 * tw, smem4, st>>>(reinterpret_cast<const V*>(blk_cnt), nblk, req_blk_off,
-                                                    cache_idx, ncached, req_cache_off,
-                                                    reinterpret_cast<const V*>(cache), nslots, rec_v, req_cnt,
-                                                    status);
-    else
-      stitch_sum<V, NB, 2><<<R, 2 * tw, smem4 / 2, st>>>(reinterpret_cast<const V*>(blk_cnt), nblk,
-                                                        req_blk_off, cache_idx, ncached, req_cache_off,
-                                                        reinterpret_cast<const V*>(cache), nslots, rec_v,
-                                                        req_cnt, status);
+    const size_t part1 = (size_t)NB * tw * sizeof(uint32_t);
+    auto go = [&](auto stag) -> cudaError_t {
+      constexpr int S = decltype(stag)::value;
+      // the attribute is a ceiling kept for the process: set it once to the most any call
+      // of this instance may ask for (64 KB), never to one call's size
+      static std::atomic<unsigned long long> opted{0};
+      cudaError_t e = smem_optin(stitch_sum<V, NB, S>, 64 * 1024, opted);
+      if (e != cudaSuccess) return e;
+      stitch_sum<V, NB, S><<<R, S * tw, S * part1, st>>>(reinterpret_cast<const V*>(blk_cnt), nblk, req_blk_off,
+                                                       cache_idx, ncached, req_cache_off,
+                                                       reinterpret_cast<const V*>(cache), nslots, rec_v,
+                                                       req_cnt, status);
+      return cudaGetLastError();
+    };
+    return go(std::integral_constant<int, 4>{});  // tw <= 256 and part1 <= 16 KB always fit
   };
-  if (v16)
-    launch_sum(uint4{}, std::integral_constant<int, 16>{});
-  else
-    launch_sum(uint32_t{}, std::integral_constant<int, 4>{});
-  return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
+  const cudaError_t e = v16 ? launch_sum(uint4{}, std::integral_constant<int, 16>{})
+                            : launch_sum(uint32_t{}, std::integral_constant<int, 4>{});
+  return e == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
 }  // namespace moer

@@ -101,3 +101,40 @@ def test_ids_signature_rejects_bad_ids(env, k):
     # the ids alone, no co-activation asked: counts the same, still reported
     status, cnt2, _ = _run(env, wl, b, bad, want_aff=False)
     assert status == 6 and np.array_equal(cnt2, cnt)
+
+
+@pytest.mark.parametrize("E,k", [(64, 8), (100, 8), (128, 8), (100, 6), (128, 6)])
+def test_ids_signature_many_bad_rows(env, E, k):
+    """Every slot pair repeated and every slot pushed to E, E + 1 ... 255, across many
+    rows and mask layers: the co-activation keeps exactly the good rows, the block counts
+    every id below E, and the status reads MOER_EDATA."""
+    orc = oracle.get()
+    L, B = 3, 16
+    wl = gen.make_custom(E, k, L, [300, 77, 161], B=B, mask=[0, 2])
+    b = wl.batch()
+    tk = orc.topk(gen.host_logits(wl, b.tok_key, b.tok_dom), k)
+    bad = tk.copy()
+    rs = np.random.RandomState(E * 10 + k)
+    keep = np.ones((L, b.T), dtype=bool)
+    pairs = [(i, j) for i in range(k) for j in range(k) if i != j]
+    rows = rs.choice(b.T, size=(L, 120), replace=False)
+    for l in range(L):
+        for n, t in enumerate(rows[l]):
+            if n < len(pairs):                       # repeated id, every ordered slot pair
+                i, j = pairs[n]
+                bad[l, t, i] = bad[l, t, j]
+            else:                                    # an id at or above E in some slot
+                bad[l, t, rs.randint(k)] = rs.choice([E, E + 1, 127 if E < 127 else 255, 128, 255])
+            keep[l, t] = False
+    status, cnt, aff = _run(env, wl, b, bad)
+    assert status == 6
+    ref_aff = np.zeros((L, E, E), dtype=np.int64)
+    for l in range(L):
+        ref_aff[l] = orc.affinity(tk[l][keep[l]][None], E)[0]
+    assert np.array_equal(aff, ref_aff)
+    ref_cnt = np.zeros_like(cnt, dtype=np.int64)
+    for i, layer in enumerate(wl.mask):
+        for j, (t0, ln) in enumerate(b.blk_tab):
+            ids = bad[layer, t0:t0 + ln].reshape(-1)
+            ref_cnt[j, i] = np.bincount(ids[ids < E], minlength=E)
+    assert np.array_equal(cnt.astype(np.int64), ref_cnt)
