@@ -74,7 +74,8 @@ __device__ __forceinline__ void bc_count_layers(uint32_t base, const uint32_t (&
 // CHECK: the ids come from the caller (moer_ids_signature); an id >= E is
 // not counted (it lands in the row's tail) and is recorded as MOER_EDATA.
 template <bool CHECK>
-__global__ void __launch_bounds__(BC_WARPS * 32) block_counts_kernel(const __grid_constant__ BcParams p) {
+// Six CTAs per SM (at most 40 registers a thread; 24.8 KB of shared memory at m = 12).
+__global__ void __launch_bounds__(BC_WARPS * 32, 6) block_counts_kernel(const __grid_constant__ BcParams p) {
   extern __shared__ uint8_t bc_raw[];  // [BC_WARPS][min(m, BC_MC)][256 bytes], 256-byte aligned
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nrows = min(p.m, BC_MC);
