@@ -21,6 +21,10 @@
  *     the offending work and record MOER_EDATA in the workspace's status
  *     word; moer_ws_status reports it.  No kernel traps.
  *   - Device waits are bounded; an expired wait records MOER_ETIMEOUT.
+ *   - Checked mode (off by default; see moer_set_extent_checks): before
+ *     launching, every entry point verifies that each buffer's device
+ *     allocation can hold the bytes the call would touch, and returns
+ *     MOER_EEXTENT otherwise.
  *   - Limits: 4 <= E <= 256 with E % 4 == 0; 1 <= k <= min(E, 32);
  *     1 <= L <= 256; 0 <= m <= L; 1 <= B <= 255; 1 <= D <= 64;
  *     T < 2^31 per call; every count fits in int32.
@@ -53,7 +57,8 @@ typedef enum moer_status {
   MOER_ECUDA = 4,    /* a CUDA runtime call or kernel launch failed           */
   MOER_ENOMEM = 5,   /* the workspace passed is smaller than required         */
   MOER_EDATA = 6,    /* device-side validation rejected input data            */
-  MOER_ETIMEOUT = 7  /* a bounded device-side wait expired                    */
+  MOER_ETIMEOUT = 7, /* a bounded device-side wait expired                    */
+  MOER_EEXTENT = 8   /* checked mode: a buffer's allocation is too small      */
 } moer_status;
 
 /* Shape of the routing problem. */
@@ -403,6 +408,26 @@ MOER_API moer_status moer_ws_status(void* ws, moer_stream_t stream);
  * Returns MOER_EINVAL / MOER_ENOMEM / MOER_ERANGE for bad arguments (nothing
  * launched), MOER_ECUDA if the launch fails, else MOER_OK. */
 MOER_API moer_status moer_wait_selftest(void* ws, size_t ws_bytes, uint32_t limit_us, moer_stream_t stream);
+
+/* Checked mode.  With `on` non-zero, every entry point first asks the CUDA
+ * driver (cuMemGetAddressRange) for the allocation that holds each buffer it
+ * is given and returns MOER_EEXTENT, launching nothing, when that allocation
+ * does not contain [p, p + bytes) for the bytes the call would read or write
+ * (the extents follow each argument's layout above; the workspace's extent is
+ * ws_bytes), or when a pointer is not in any device allocation.  It turns a
+ * buffer that is too small into an error instead of a memory fault.  The
+ * check sees allocation ends only: a buffer carved from a larger allocation
+ * (a framework's memory pool) can still overrun into its neighbour.  Cost:
+ * one driver query per buffer per call.  Off by default; the environment
+ * variable MOER_CHECK_EXTENTS=1 turns it on at the process's first call.
+ * Process-wide; takes effect for calls made after it returns. */
+MOER_API void moer_set_extent_checks(int32_t on);
+/* 1 when checked mode is on, else 0. */
+MOER_API int32_t moer_extent_checks(void);
+/* The test checked mode applies, for one buffer: 1 when [p, p + bytes) lies
+ * inside one device allocation (bytes 0 is taken as 1), else 0 (also for a
+ * NULL or non-device pointer).  Host-side; launches nothing. */
+MOER_API int32_t moer_buffer_holds(const void* p, size_t bytes);
 
 /* Static description of a status code. */
 MOER_API const char* moer_status_str(moer_status s);

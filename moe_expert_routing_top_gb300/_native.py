@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("MOER_LIBRARY", os.path.join(HERE, "_build", "libmoeroute.so"))
 
 STATUS = {0: "MOER_OK", 1: "MOER_EINVAL", 2: "MOER_ESHAPE", 3: "MOER_ERANGE", 4: "MOER_ECUDA",
-          5: "MOER_ENOMEM", 6: "MOER_EDATA", 7: "MOER_ETIMEOUT"}
+          5: "MOER_ENOMEM", 6: "MOER_EDATA", 7: "MOER_ETIMEOUT", 8: "MOER_EEXTENT"}
 
 
 class MoerError(RuntimeError):
@@ -70,6 +70,9 @@ def _load():
         "moer_wait_selftest": ([vp, sz, ctypes.c_uint32, vp], ctypes.c_int),
         "moer_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "moer_version": ([], ctypes.c_int32),
+        "moer_set_extent_checks": ([i32], None),
+        "moer_extent_checks": ([], ctypes.c_int32),
+        "moer_buffer_holds": ([vp, sz], ctypes.c_int32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -87,7 +90,8 @@ EXPORTS = ("moer_workspace_bytes", "moer_topk_signature", "moer_topk_signature_n
            "moer_mask_select_workspace_bytes", "moer_mask_select", "moer_spectral_workspace_bytes",
            "moer_spectral_groups",
            "moer_ws_status", "moer_wait_selftest",
-           "moer_status_str", "moer_version")
+           "moer_status_str", "moer_version", "moer_set_extent_checks", "moer_extent_checks",
+           "moer_buffer_holds")
 
 
 def _ptr(x):
@@ -233,3 +237,16 @@ def moer_status_str(code: int) -> str:
 
 def moer_version() -> int:
     return int(LIB.moer_version())
+
+
+def moer_set_extent_checks(on: bool) -> None:
+    LIB.moer_set_extent_checks(1 if on else 0)
+
+
+def moer_extent_checks() -> bool:
+    return bool(LIB.moer_extent_checks())
+
+
+def moer_buffer_holds(p, nbytes: int) -> bool:
+    """Host-side: whether one device allocation holds [p, p + nbytes)."""
+    return bool(LIB.moer_buffer_holds(_ptr(p), nbytes))

@@ -1,9 +1,14 @@
 // api.cu -- the extern "C" entry points of libmoeroute: argument validation,
 // workspace accounting and dispatch to the kernels.  Nothing here computes
 // routing statistics; every step runs on the GPU.
+#include <cuda.h>
+
+#include <atomic>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
+#include "extent.h"
 
 namespace moer {
 size_t spectral_workspace_bytes(int L, int E, int G);
@@ -52,7 +57,59 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+// ---------------------------------------------------------- checked mode
+// Off by default; on with moer_set_extent_checks(1) or MOER_CHECK_EXTENTS=1 in
+// the environment (read at the first call).  -1: not read yet.
+std::atomic<int> g_extent_checks{-1};
+
+bool extent_checks_on() {
+  int v = g_extent_checks.load(std::memory_order_acquire);
+  if (v < 0) {
+    const char* e = std::getenv("MOER_CHECK_EXTENTS");
+    const int want = (e != nullptr && e[0] != '\0' && e[0] != '0') ? 1 : 0;
+    int expected = -1;
+    g_extent_checks.compare_exchange_strong(expected, want, std::memory_order_acq_rel);
+    v = g_extent_checks.load(std::memory_order_acquire);
+  }
+  return v == 1;
+}
+
+using AddrRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+// The driver's cuMemGetAddressRange, resolved through the runtime (the library
+// does not link libcuda directly).
+AddrRangeFn addr_range_fn() {
+  static const AddrRangeFn fn = []() -> AddrRangeFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<AddrRangeFn>(f);
+  }();
+  return fn;
+}
+
+bool device_range(uintptr_t p, uintptr_t* base, size_t* size) {
+  const AddrRangeFn fn = addr_range_fn();
+  if (fn == nullptr) return false;
+  CUdeviceptr b = 0;
+  size_t n = 0;
+  if (fn(&b, &n, static_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return false;
+  *base = static_cast<uintptr_t>(b);
+  *size = n;
+  return true;
+}
+
+// MOER_EEXTENT when checked mode is on and a buffer's allocation cannot hold
+// its extent, else MOER_OK.  Sizes are computed by the caller in size_t.
+moer_status check_extents(std::initializer_list<Extent> list) {
+  if (!extent_checks_on()) return MOER_OK;
+  return first_bad_extent(list, device_range) < 0 ? MOER_OK : MOER_EEXTENT;
+}
+
+size_t sz(int64_t a) { return a > 0 ? static_cast<size_t>(a) : 0; }
+
 
 moer_status check_dims(const moer_dims* d, bool need_mask) {
   if (d == nullptr) return MOER_EINVAL;
@@ -69,6 +126,19 @@ moer_status check_dims(const moer_dims* d, bool need_mask) {
     }
   }
   return MOER_OK;
+}
+
+// Extents of the logits-pass buffers (moer_topk_signature and its no-alloc form).
+moer_status topk_signature_extents(const moer_dims* d, const float* logits, int64_t T, const int32_t* blk_tab,
+                                   int32_t nblk, const uint8_t* topk, const uint8_t* blk_cnt,
+                                   const int32_t* affinity, const void* ws, size_t ws_bytes, bool hist) {
+  const size_t L = sz(d->L), E = sz(d->E), k = sz(d->k), m = sz(d->m), t = sz(T), nb = sz(nblk);
+  return check_extents({{logits, L * t * E * 4},
+                        {hist ? blk_tab : nullptr, nb * 2 * 4},
+                        {topk, L * t * k},
+                        {hist ? blk_cnt : nullptr, nb * m * E},
+                        {affinity, L * E * E * 4},
+                        {ws, ws_bytes}});
 }
 
 }  // namespace
@@ -91,6 +161,15 @@ moer_status topk_signature_check(const moer_dims* d, const float* logits, int64_
     if (nblk < 1 || nblk > T) return MOER_ESHAPE;
   }
   return MOER_OK;
+}
+
+// Checked mode's extents for moer_topk_signature_noalloc (after its own
+// argument and staging-size checks, as in the workspace form).
+moer_status topk_signature_noalloc_extents(const moer_dims* d, const float* logits, int64_t T,
+                                           const int32_t* blk_tab, int32_t nblk, const uint8_t* topk,
+                                           const uint8_t* blk_cnt, const int32_t* affinity) {
+  const bool hist = blk_cnt != nullptr && d->m > 0;
+  return topk_signature_extents(d, logits, T, blk_tab, nblk, topk, blk_cnt, affinity, nullptr, 0, hist);
 }
 }  // namespace moer
 
@@ -128,6 +207,8 @@ moer_status moer_topk_signature(const moer_dims* d, const float* logits, int64_t
   }
   if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
   if (ws_bytes < moer_workspace_bytes(d, T, nblk, 0, 0)) return MOER_ENOMEM;
+  s = topk_signature_extents(d, logits, T, blk_tab, nblk, topk, blk_cnt, affinity, ws, ws_bytes, hist);
+  if (s != MOER_OK) return s;
   return topk_signature_launch(d, logits, T, blk_tab, nblk, topk, blk_cnt, affinity, ws,
                                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -153,6 +234,19 @@ moer_status moer_block_stitch(const moer_dims* d, const uint8_t* blk_cnt, const 
     return MOER_EINVAL;
   }
   if (ws != nullptr && (!aligned(ws, 16) || ws_bytes < WS_HEADER)) return MOER_ENOMEM;
+  {
+    const size_t rec = sz(d->m) * sz(d->E), nb = sz(nblk), r1 = sz(R) + 1;
+    s = check_extents({{blk_cnt, nb * rec},
+                       {(has_cache && insert_slot != nullptr) ? blk_tab : nullptr, nb * 2 * 4},
+                       {req_blk_off, r1 * 4},
+                       {cache_idx, sz(ncached) * 4},
+                       {req_cache_off, r1 * 4},
+                       {cache, sz(nslots) * rec},
+                       {insert_slot, nb * 4},
+                       {req_cnt, sz(R) * rec * 4},
+                       {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return block_stitch_launch(d, blk_cnt, blk_tab, nblk, req_blk_off, R, cache_idx, ncached, req_cache_off,
                              cache, nslots, insert_slot, req_cnt,
                              ws ? reinterpret_cast<uint32_t*>(ws) : nullptr,
@@ -170,6 +264,17 @@ moer_status moer_affinity_load(const moer_dims* d, const int32_t* affinity, cons
     if (G < 1 || G > 4096) return MOER_ERANGE;
   }
   if (G < 1) G = 1;
+  {
+    const size_t L = sz(d->L), E = sz(d->E), g = sz(G);
+    const bool groups = W_group != nullptr || rho_group != nullptr;
+    s = check_extents({{affinity, L * E * E * 4},
+                       {groups ? group_of : nullptr, L * E * 4},
+                       {W_expert, L * E * 8},
+                       {W_group, L * g * 8},
+                       {rho_group, L * 8},
+                       {rho_expert, L * 8}});
+    if (s != MOER_OK) return s;
+  }
   return affinity_load_launch(d, affinity, group_of, G, W_expert, W_group, rho_group, rho_expert,
                               reinterpret_cast<cudaStream_t>(stream));
 }
@@ -192,6 +297,18 @@ moer_status moer_route(const moer_dims* d, const int32_t* req_cnt, int32_t R, co
     if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
     if (ws_bytes < moer_workspace_bytes(d, 0, 0, R, D)) return MOER_ENOMEM;
   }
+  {
+    const size_t dim = sz(d->m) * sz(d->E), r = sz(R), nd = sz(D);
+    s = check_extents({{req_cnt, r * dim * 4},
+                       {idf, dim * 4},
+                       {centroids, nd * dim * 4},
+                       {loads, nd * 4},
+                       {sig, r * dim * 4},
+                       {dist, r * nd * 4},
+                       {choice, r * 4},
+                       {live ? ws : nullptr, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return route_launch(d, req_cnt, R, idf, centroids, D, tau, loads, live, sig, dist, choice, ws,
                       reinterpret_cast<cudaStream_t>(stream));
 }
@@ -203,6 +320,8 @@ moer_status moer_idf_fit(const moer_dims* d, const int32_t* req_cnt, int32_t R, 
   if (d->m < 1) return MOER_ERANGE;
   if (R < 1) return MOER_ERANGE;
   if (req_cnt == nullptr || idf == nullptr) return MOER_EINVAL;
+  s = check_extents({{req_cnt, sz(R) * sz(d->m) * sz(d->E) * 4}, {idf, sz(d->m) * sz(d->E) * 4}});
+  if (s != MOER_OK) return s;
   return idf_fit_launch(d, req_cnt, R, idf, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -232,6 +351,18 @@ moer_status moer_gate_topk(const moer_dims* d, const uint16_t* hidden, int64_t T
   }
   if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
   if (ws_bytes < moer_gate_workspace_bytes(d, H)) return MOER_ENOMEM;
+  {
+    const size_t L = sz(d->L), E = sz(d->E), k = sz(d->k), m = sz(d->m), t = sz(T), h = sz(H), nb = sz(nblk);
+    s = check_extents({{hidden, t * h * 2},
+                       {w_gate, L * h * E * 2},
+                       {hist ? blk_tab : nullptr, nb * 2 * 4},
+                       {logits, L * t * E * 4},
+                       {topk, L * t * k},
+                       {hist ? blk_cnt : nullptr, nb * m * E},
+                       {affinity, L * E * E * 4},
+                       {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   s = gate_topk_launch(d, hidden, T, H, w_gate, logits, topk, ws, st);
   if (s != MOER_OK) return s;
@@ -263,6 +394,15 @@ moer_status moer_ids_signature(const moer_dims* d, const uint8_t* topk, int64_t 
   }
   if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
   if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
+  {
+    const size_t L = sz(d->L), E = sz(d->E), k = sz(d->k), m = sz(d->m), t = sz(T), nb = sz(nblk);
+    s = check_extents({{topk, L * t * k},
+                       {hist ? blk_tab : nullptr, nb * 2 * 4},
+                       {hist ? blk_cnt : nullptr, nb * m * E},
+                       {affinity, L * E * E * 4},
+                       {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   if (affinity != nullptr) {
@@ -287,6 +427,12 @@ moer_status moer_replication_plan(const moer_dims* d, const int64_t* W, const in
     return MOER_EINVAL;
   if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
   if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
+  {
+    const size_t L = sz(d->L), E = sz(d->E), g = sz(G);
+    s = check_extents({{W, L * E * 8}, {group_of, L * E * 4}, {n_rep, L * 4}, {src, L * 4}, {hot, L * E},
+                       {dst, L * g * 4}, {w_pred, L * g * 8}, {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return moer::replication_plan_launch(d, W, group_of, G, n_rep, src, hot, dst, w_pred,
                                        reinterpret_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream));
 }
@@ -308,6 +454,12 @@ moer_status moer_mask_select(const moer_dims* d, const uint8_t* topk, int64_t T,
     return MOER_EINVAL;
   if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
   if (ws_bytes < moer_mask_select_workspace_bytes(d, R)) return MOER_ENOMEM;
+  {
+    const size_t L = sz(d->L), E = sz(d->E), k = sz(d->k), t = sz(T), mm = sz(m);
+    s = check_extents({{topk, L * t * k}, {req_off, (sz(R) + 1) * 4}, {idf, L * E * 4}, {mask_out, mm * 4},
+                       {quality_out, mm * 8}, {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return moer::mask_select_launch(d, topk, T, req_off, R, idf, m, mask_out, quality_out, ws,
                                   reinterpret_cast<cudaStream_t>(stream));
 }
@@ -330,6 +482,12 @@ moer_status moer_spectral_groups(const moer_dims* d, const int32_t* affinity, in
     return MOER_EINVAL;
   if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
   if (ws_bytes < moer_spectral_workspace_bytes(d, G)) return MOER_ENOMEM;
+  {
+    const size_t L = sz(d->L), E = sz(d->E);
+    s = check_extents({{affinity, L * E * E * 4}, {group_of, L * E * 4}, {knee, L * 4}, {u_curve, L * 17 * 8},
+                       {s_curve, L * 17 * 8}, {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return moer::spectral_launch(d, affinity, G, group_of, knee, u_curve, s_curve, ws,
                                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -352,6 +510,12 @@ moer_status moer_kmeans_balanced(const float* sig, int32_t N, int32_t dim, int32
     return MOER_EINVAL;
   if (ws == nullptr || !aligned(ws, 256)) return MOER_EINVAL;
   if (ws_bytes < moer_kmeans_workspace_bytes(N, dim, D)) return MOER_ENOMEM;
+  {
+    const size_t n = sz(N), dm = sz(dim), nd = sz(D);
+    const moer_status s = check_extents({{sig, n * dm * 4}, {init_centroids, nd * dm * 4}, {centroids, nd * dm * 4},
+                                         {assign, n * 4}, {info, 3 * 4}, {objective, 8}, {ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return moer::kmeans_launch(sig, N, dim, D, init_centroids, max_iter, centroids, assign, info, objective, ws,
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -360,11 +524,19 @@ moer_status moer_wait_selftest(void* ws, size_t ws_bytes, uint32_t limit_us, moe
   if (ws == nullptr || !aligned(ws, 16)) return MOER_EINVAL;
   if (ws_bytes < WS_HEADER) return MOER_ENOMEM;
   if (limit_us < 1 || limit_us > 1000000) return MOER_ERANGE;
+  {
+    const moer_status s = check_extents({{ws, ws_bytes}});
+    if (s != MOER_OK) return s;
+  }
   return moer::wait_selftest_launch(ws, limit_us, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moer_status moer_ws_status(void* ws, moer_stream_t stream) {
   if (ws == nullptr) return MOER_EINVAL;
+  {
+    const moer_status s = check_extents({{ws, 8}});
+    if (s != MOER_OK) return s;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint32_t h[2] = {0u, 0u};
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOER_ECUDA;
@@ -385,10 +557,20 @@ const char* moer_status_str(moer_status s) {
     case MOER_ENOMEM: return "workspace too small";
     case MOER_EDATA: return "device-side validation rejected input data";
     case MOER_ETIMEOUT: return "bounded device wait expired";
+    case MOER_EEXTENT: return "checked mode: a buffer's allocation cannot hold what the call would touch";
   }
   return "unknown status";
 }
 
 int32_t moer_version(void) { return 100; }
+
+void moer_set_extent_checks(int32_t on) { g_extent_checks.store(on ? 1 : 0, std::memory_order_release); }
+
+int32_t moer_buffer_holds(const void* p, size_t bytes) {
+  if (p == nullptr) return 0;
+  return first_bad_extent({{p, bytes == 0 ? 1 : bytes}}, device_range) < 0 ? 1 : 0;
+}
+
+int32_t moer_extent_checks(void) { return extent_checks_on() ? 1 : 0; }
 
 }  // extern "C"

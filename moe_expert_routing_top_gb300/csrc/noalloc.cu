@@ -18,6 +18,9 @@ namespace moer {
 moer_status topk_signature_check(const moer_dims* d, const float* logits, int64_t T,
                                  const int32_t* blk_tab, int32_t nblk, const uint8_t* topk,
                                  const uint8_t* blk_cnt, const int32_t* affinity);
+moer_status topk_signature_noalloc_extents(const moer_dims* d, const float* logits, int64_t T,
+                                           const int32_t* blk_tab, int32_t nblk, const uint8_t* topk,
+                                           const uint8_t* blk_cnt, const int32_t* affinity);
 moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64_t T,
                                   const int32_t* blk_tab, int32_t nblk, uint8_t* topk,
                                   uint8_t* blk_cnt, int32_t* affinity, void* ws, cudaStream_t st);
@@ -94,6 +97,8 @@ extern "C" MOER_API moer_status moer_topk_signature_noalloc(const moer_dims* d, 
   if (topk == nullptr && blk_cnt != nullptr && d->m > 0 &&
       (uint64_t)d->m * (uint64_t)T * (uint64_t)d->k > (uint64_t)MOER_NOALLOC_IDS_BYTES)
     return MOER_ENOMEM;
+  s = topk_signature_noalloc_extents(d, logits, T, blk_tab, nblk, topk, blk_cnt, affinity);
+  if (s != MOER_OK) return s;
   void* ws = scratch_in_current_context();
   if (ws == nullptr) return MOER_ECUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
