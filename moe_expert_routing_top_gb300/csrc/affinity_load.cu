@@ -7,6 +7,7 @@
 // holds e); a group's load sums its experts' loads; the mean is taken over
 // all G groups (E experts for the per-expert skew).
 #include "common.cuh"
+#include "pdl.cuh"
 
 namespace moer {
 
@@ -16,6 +17,7 @@ __global__ void affinity_load_kernel(const int32_t* __restrict__ affinity, int E
                                      double* __restrict__ rho_group, double* __restrict__ rho_expert) {
   extern __shared__ unsigned long long gsum[];  // [G]
   __shared__ unsigned long long red_sum[8], red_max[8];
+  pdl_wait();
   const int l = blockIdx.x;
   for (int g = threadIdx.x; g < G; g += blockDim.x) gsum[g] = 0ull;
   __syncthreads();
@@ -56,14 +58,15 @@ __global__ void affinity_load_kernel(const int32_t* __restrict__ affinity, int E
   }
   if (W_group)
     for (int g = threadIdx.x; g < G; g += blockDim.x) W_group[(size_t)l * G + g] = (int64_t)gsum[g];
+  pdl_release();
 }
 
 moer_status affinity_load_launch(const moer_dims* d, const int32_t* affinity, const int32_t* group_of,
                                  int32_t G, int64_t* W_expert, int64_t* W_group, double* rho_group,
                                  double* rho_expert, cudaStream_t st) {
-  affinity_load_kernel<<<d->L, 256, (size_t)G * sizeof(unsigned long long), st>>>(
-      affinity, d->E, group_of, G, W_expert, W_group, rho_group, rho_expert);
-  return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
+  const cudaError_t e = launch_pdl(affinity_load_kernel, dim3(d->L), dim3(256), (size_t)G * sizeof(unsigned long long),
+                                   st, affinity, d->E, group_of, G, W_expert, W_group, rho_group, rho_expert);
+  return e == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 
 }  // namespace moer

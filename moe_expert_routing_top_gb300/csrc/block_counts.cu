@@ -22,6 +22,7 @@
 // a block whose length is outside [1, B], that runs past T or that does not
 // start where the previous block ends is skipped and recorded as MOER_EDATA.
 #include "common.cuh"
+#include "pdl.cuh"
 
 namespace moer {
 
@@ -77,6 +78,7 @@ template <bool CHECK>
 // Six CTAs per SM (at most 40 registers a thread; 24.8 KB of shared memory at m = 12).
 __global__ void __launch_bounds__(BC_WARPS * 32, 6) block_counts_kernel(const __grid_constant__ BcParams p) {
   extern __shared__ uint8_t bc_raw[];  // [BC_WARPS][min(m, BC_MC)][256 bytes], 256-byte aligned
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nrows = min(p.m, BC_MC);
   const uint32_t base = ((smem_u32(bc_raw) + (BC_ROW - 1)) & ~(uint32_t)(BC_ROW - 1)) + warp * nrows * BC_ROW;
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(BC_WARPS * 32, 6) block_counts_kernel(const __
     }
   }
   if (CHECK && bad != 0u) atomicOr(p.status, WS_BIT_EDATA);
+  pdl_release();
 }
 
 // ids: either the caller's [L][T][k] top-k (mask_only = false: row block of
@@ -177,6 +180,8 @@ moer_status block_counts_launch(const moer_dims* d, const uint8_t* ids, bool mas
   if (sms <= 0) return MOER_ECUDA;
   const int64_t grid = min64(((int64_t)nblk + BC_WARPS - 1) / BC_WARPS, (int64_t)sms * 8);
   const size_t smem = (size_t)BC_WARPS * min(d->m, BC_MC) * BC_ROW + BC_ROW;  // + alignment slack
+  // a normal launch: the persistent grid's static split wants every SM free when it
+  // starts (pdl.cuh); the kernel still releases its successor at its end
   if (check)
     block_counts_kernel<true><<<(unsigned)grid, BC_WARPS * 32, smem, st>>>(p);
   else
@@ -276,6 +281,7 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
                                                                   int32_t* __restrict__ affinity,
                                                                   uint32_t* status) {
   extern __shared__ int ai_tile[];  // [E][E + 1] directed counts, then [E] row sums
+  pdl_wait();
   const int rs = E + 1;
   int* rsum = ai_tile + E * rs;
   const uint32_t tile_base = smem_u32(ai_tile);
@@ -348,6 +354,7 @@ __global__ void __launch_bounds__(AI_THREADS) affinity_ids_kernel(const uint8_t*
   }
   __syncthreads();
   affinity_ids_flush(ai_tile, rsum, E, K, affinity + (size_t)cur * E * E);
+  pdl_release();
 }
 
 // ids [L][T][k] (k = 6 or 8, 8-byte aligned rows for k = 8) -> affinity
@@ -369,14 +376,10 @@ moer_status affinity_ids_launch(const moer_dims* d, const uint8_t* ids, int64_t 
       smem_optin(affinity_ids_kernel<6, true>, most, set6c) != cudaSuccess)
     return MOER_ECUDA;
   const int grid = (int)min64(nitems, (int64_t)sms * 2);
-  if (d->k == 8 && !check)
-    affinity_ids_kernel<8, false><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
-  else if (d->k == 8)
-    affinity_ids_kernel<8, true><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
-  else if (!check)
-    affinity_ids_kernel<6, false><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
-  else
-    affinity_ids_kernel<6, true><<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
+  auto kernel = d->k == 8 ? (check ? affinity_ids_kernel<8, true> : affinity_ids_kernel<8, false>)
+                          : (check ? affinity_ids_kernel<6, true> : affinity_ids_kernel<6, false>);
+  // a normal launch, as for the block counts: two CTAs per SM split the items statically
+  kernel<<<grid, AI_THREADS, smem, st>>>(ids, T, d->E, d->L, nchunks, affinity, status);
   return cudaGetLastError() == cudaSuccess ? MOER_OK : MOER_ECUDA;
 }
 

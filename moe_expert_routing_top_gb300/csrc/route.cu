@@ -26,6 +26,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "pdl.cuh"
 
 namespace moer {
 
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_sig_dist(
   __shared__ float red[32];
   __shared__ float part[ROUTE_THREADS / 32][DM];
   __shared__ float dsh[DM];
+  pdl_wait();
   const int r = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* cnt = req_cnt + (size_t)r * dim;
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_sig_dist(
     else
       band[r] = m;
   }
+  pdl_release();
 }
 
 // Sequential live routing over the requests' band masks.  Lane q of warp 0
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_live(const unsigned long 
                                                             int D, int32_t* __restrict__ loads,
                                                             int32_t* __restrict__ choice) {
   __shared__ unsigned long long buf[2][LIVE_BUF];
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int ld0 = 0, ld1 = 0;
   if (warp == 0) {
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_live(const unsigned long 
     if (lane < D) loads[lane] = ld0;
     if (WIDE && lane + 32 < D) loads[lane + 32] = ld1;
   }
+  pdl_release();
 }
 
 __global__ void idf_fit_kernel(const int32_t* __restrict__ req_cnt, int R, int dim, float* __restrict__ idf) {
@@ -202,19 +207,18 @@ moer_status route_launch(const moer_dims* d, const int32_t* req_cnt, int32_t R, 
   const int dim = d->m * d->E;
   unsigned long long* band =
       live ? reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + WS_HEADER) : nullptr;
-  if (D <= 16)
-    route_sig_dist<16><<<R, ROUTE_THREADS, 0, st>>>(req_cnt, dim, idf, centroids, D, tau, loads,
-                                                    live ? 0 : 1, sig, dist, choice, band);
-  else
-    route_sig_dist<ROUTE_DMAX><<<R, ROUTE_THREADS, 0, st>>>(req_cnt, dim, idf, centroids, D, tau,
-                                                            loads, live ? 0 : 1, sig, dist, choice, band);
-  if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
+  const int pick = live ? 0 : 1;
+  cudaError_t e = D <= 16 ? launch_pdl(route_sig_dist<16>, dim3(R), dim3(ROUTE_THREADS), 0, st, req_cnt, dim, idf,
+                                       centroids, D, tau, loads, pick, sig, dist, choice, band)
+                          : launch_pdl(route_sig_dist<ROUTE_DMAX>, dim3(R), dim3(ROUTE_THREADS), 0, st, req_cnt,
+                                       dim, idf, centroids, D, tau, loads, pick, sig, dist, choice, band);
+  if (e != cudaSuccess) return MOER_ECUDA;
   if (live) {
-    if (D <= 32)
-      route_live<false><<<1, ROUTE_THREADS, 0, st>>>(band, R, D, loads, choice);
-    else
-      route_live<true><<<1, ROUTE_THREADS, 0, st>>>(band, R, D, loads, choice);
-    if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
+    e = D <= 32 ? launch_pdl(route_live<false>, dim3(1), dim3(ROUTE_THREADS), 0, st, (const unsigned long long*)band,
+                             R, D, loads, choice)
+                : launch_pdl(route_live<true>, dim3(1), dim3(ROUTE_THREADS), 0, st, (const unsigned long long*)band,
+                             R, D, loads, choice);
+    if (e != cudaSuccess) return MOER_ECUDA;
   }
   return MOER_OK;
 }

@@ -16,6 +16,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "pdl.cuh"
 
 namespace moer {
 
@@ -25,6 +26,7 @@ template <typename V>
 __global__ void stitch_insert(const V* __restrict__ blk_w, const int32_t* __restrict__ blk_tab, int nblk, int B,
                               const int32_t* __restrict__ insert_slot, V* __restrict__ cache_w, int nslots,
                               int rec_v, uint32_t* status) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblk; b += stride) {
@@ -38,6 +40,7 @@ __global__ void stitch_insert(const V* __restrict__ blk_w, const int32_t* __rest
     V* dst = cache_w + (size_t)slot * rec_v;
     for (int w = lane; w < rec_v; w += 32) dst[w] = src[w];
   }
+  pdl_release();
 }
 
 // block loads in flight per thread: 8 words of 4 bytes or 4 of 16 bytes (the
@@ -73,6 +76,7 @@ __global__ void __launch_bounds__(1024) stitch_sum(const V* __restrict__ blk_w, 
                            const int32_t* __restrict__ req_cache_off, const V* __restrict__ cache_w, int nslots,
                            int rec_v, int32_t* __restrict__ req_cnt, uint32_t* status) {
   extern __shared__ uint32_t part[];  // [S][NB][TW] partial sums
+  pdl_wait();
   constexpr int SU = stitch_su<V>();
   const int TW = blockDim.x / S;
   const int grp = threadIdx.x / TW, wl = threadIdx.x - grp * TW;
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(1024) stitch_sum(const V* __restrict__ blk_w, 
       }
     }
   }
+  pdl_release();
 }
 
 moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, const int32_t* blk_tab,
@@ -159,15 +164,14 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
   if (sms <= 0) return MOER_ECUDA;
   if (cache != nullptr && insert_slot != nullptr && nblk > 0) {
     const int grid = (int)min64(((int64_t)nblk + 7) / 8, (int64_t)sms * 8);
-    if (v16)
-      stitch_insert<uint4><<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(blk_cnt), blk_tab, nblk, d->block,
-                                                 insert_slot, reinterpret_cast<uint4*>(cache), nslots,
-                                                 rec_bytes / 16, status);
-    else
-      stitch_insert<uint32_t><<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(blk_cnt), blk_tab, nblk,
-                                                    d->block, insert_slot, reinterpret_cast<uint32_t*>(cache),
-                                                    nslots, rec_bytes / 4, status);
-    if (cudaGetLastError() != cudaSuccess) return MOER_ECUDA;
+    const cudaError_t e =
+        v16 ? launch_pdl(stitch_insert<uint4>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const uint4*>(blk_cnt),
+                         blk_tab, nblk, d->block, insert_slot, reinterpret_cast<uint4*>(cache), nslots, rec_bytes / 16,
+                         status)
+            : launch_pdl(stitch_insert<uint32_t>, dim3(grid), dim3(256), 0, st,
+                         reinterpret_cast<const uint32_t*>(blk_cnt), blk_tab, nblk, d->block, insert_slot,
+                         reinterpret_cast<uint32_t*>(cache), nslots, rec_bytes / 4, status);
+    if (e != cudaSuccess) return MOER_ECUDA;
   }
   // TW threads per group cover the record's words, four groups (at most 1,024 threads,
   // partial sums within 64 KB of shared memory).  Eight groups of up to 96 threads were
@@ -186,11 +190,9 @@ moer_status block_stitch_launch(const moer_dims* d, const uint8_t* blk_cnt, cons
       static std::atomic<unsigned long long> opted{0};
       cudaError_t e = smem_optin(stitch_sum<V, NB, S>, 64 * 1024, opted);
       if (e != cudaSuccess) return e;
-      stitch_sum<V, NB, S><<<R, S * tw, S * part1, st>>>(reinterpret_cast<const V*>(blk_cnt), nblk, req_blk_off,
-                                                       cache_idx, ncached, req_cache_off,
-                                                       reinterpret_cast<const V*>(cache), nslots, rec_v,
-                                                       req_cnt, status);
-      return cudaGetLastError();
+      return launch_pdl(stitch_sum<V, NB, S>, dim3(R), dim3(S * tw), S * part1, st,
+                        reinterpret_cast<const V*>(blk_cnt), nblk, req_blk_off, cache_idx, ncached, req_cache_off,
+                        reinterpret_cast<const V*>(cache), nslots, rec_v, req_cnt, status);
     };
     return go(std::integral_constant<int, 4>{});  // tw <= 256 and part1 <= 16 KB always fit
   };
