@@ -185,6 +185,29 @@ MOER_API moer_status moer_block_stitch(const moer_dims* d, const uint8_t* blk_cn
                               int32_t* req_cnt, void* ws, size_t ws_bytes,
                               moer_stream_t stream);
 
+/* Expert loads, group loads and load skew per MoE layer.
+ *   [GRACE] section 4 "Method" (profiling yields the load statistics),
+ *   section 4.2 "Expert replication" (the load skew rho = W_max / W_mean
+ *   decides the replica count) and section 7 (glossary: load skew).  The
+ *   load of expert e at layer l is the diagonal of the co-activation matrix
+ *   (the tokens whose top-k holds e); a group's load sums its experts'
+ *   loads; the mean runs over all G groups, empty ones included (over the E
+ *   experts for the per-expert skew); a layer with no load has skew 0.
+ * affinity  [L][E][E] int32, 4-byte aligned (moer_topk_signature's
+ *           co-activation); only the diagonal is read.
+ * group_of  [L][E] int32: the group of each expert, in [0, G); required
+ *           when W_group or rho_group is asked for, else may be NULL.  An
+ *           expert whose group id is outside [0, G) counts in no group.
+ * G         1 <= G <= 4096 when group outputs are asked for.
+ * W_expert  [L][E] int64 out or NULL: W[l][e] = affinity[l][e][e].
+ * W_group   [L][G] int64 out or NULL: the sum of W over each group's experts.
+ * rho_group [L] fp64 out or NULL: max_g W_group / mean_g W_group.
+ * rho_expert [L] fp64 out or NULL: max_e W / mean_e W.
+ * Caller-owned device buffers; nothing is accumulated (outputs are
+ * overwritten).  Returns MOER_EINVAL for a NULL affinity (or a NULL
+ * group_of when group outputs are asked for), MOER_ERANGE for G outside
+ * its limits, MOER_ECUDA if the launch fails.
+ */
 MOER_API moer_status moer_affinity_load(const moer_dims* d, const int32_t* affinity,
                                const int32_t* group_of, int32_t G, int64_t* W_expert,
                                int64_t* W_group, double* rho_group, double* rho_expert,
