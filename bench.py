@@ -198,6 +198,20 @@ def sum_over_ranks(dist, x: float, device) -> float:
     return float(t.item())
 
 
+def pinned_on_all_ranks(shape, dtype, dist, device):
+    """A pinned host buffer, or None on every rank when any rank cannot pin its own (each
+    replica pins its full step input; a node's host memory may not hold them all)."""
+    import torch
+    try:
+        buf = torch.empty(shape, dtype=dtype, pin_memory=True)
+        ok = 1.0
+    except RuntimeError:
+        buf, ok = None, 0.0
+    if dist is not None:
+        ok = -max_over_ranks(dist, -ok, device)  # the minimum over ranks
+    return buf if ok >= 1.0 else None
+
+
 # ------------------------------------------------------------ CPU oracle arm
 def oracle_pass(orc, wl, b, logits):
     """The plain oracle over one batch: every row of the path, as it stands.  Returns the
@@ -413,7 +427,9 @@ def measure_stream(args, device, dist, stream, with_e2e=False, parity=None):
     choice = np.empty(wl.R, dtype=np.int32)
     gdist = np.empty((wl.R, wl.D), dtype=np.float32)
     choice_host = torch.empty(max(x.R for x in batches), dtype=torch.int32, pin_memory=True)
-    pinned = torch.empty(wl.L * cap_T * wl.E, dtype=torch.float32, pin_memory=True) if with_e2e else None
+    pinned = pinned_on_all_ranks(wl.L * cap_T * wl.E, torch.float32, dist, device) if with_e2e else None
+    e2e_unavailable = with_e2e and pinned is None
+    with_e2e = with_e2e and pinned is not None
     # per chunk: start, K1 start (after the host copy in the end-to-end run), K1 end, route
     # start, end
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in batches]
@@ -483,6 +499,9 @@ def measure_stream(args, device, dist, stream, with_e2e=False, parity=None):
         "l2": "inputs larger than L2 (logits %.1f GB per chunk)" % (wl.L * cap_T * wl.E * 4 / 1e9),
         "gpu_choice": choice,
     }
+    if e2e_unavailable:
+        out["e2e"] = {"unavailable": "pinned host memory for a chunk's input (%.1f GB per replica) could not be "
+                                     "allocated on every rank" % (wl.L * cap_T * wl.E * 4 / 1e9)}
     if with_e2e:
         h2d = wl.L * T * wl.E * 4
         out["e2e"] = {"value": units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
@@ -878,7 +897,10 @@ def run_gate_e2e(args, wl, b, rs, hidden, w_gate, stream, device, dist):
     bounds = np.linspace(0, wl.R, nch + 1).astype(int)
     batches = [wl.batch(int(a), int(z)) for a, z in zip(bounds[:-1], bounds[1:])]
     H = wl.hidden_dim
-    pinned = torch.empty((b.T, H), dtype=torch.int16, pin_memory=True)
+    pinned = pinned_on_all_ranks((b.T, H), torch.int16, dist, device)
+    if pinned is None:
+        return {"unavailable": "pinned host memory for the step input (%.1f GB per replica) could not be "
+                               "allocated on every rank" % (b.T * H * 2 / 1e9)}
     pinned.copy_(hidden)  # untimed: the host copy of the same inputs
     offs = np.concatenate([[0], np.cumsum([x.T for x in batches])]).astype(int)
     copy_streams = [torch.cuda.Stream(device) for _ in range(max(args.e2e_copy_streams, 1))]
@@ -1126,7 +1148,10 @@ def run_e2e(args, wl, b, bd, rs, logits, stream, device, dist):
     bounds = np.linspace(0, wl.R, nch + 1).astype(int)
     batches = [wl.batch(int(a), int(z)) for a, z in zip(bounds[:-1], bounds[1:])]
     host_bytes = logits.numel() * 4
-    pinned = torch.empty((wl.L, b.T, wl.E), dtype=torch.float32, pin_memory=True)
+    pinned = pinned_on_all_ranks((wl.L, b.T, wl.E), torch.float32, dist, device)
+    if pinned is None:
+        return {"unavailable": "pinned host memory for the step input (%.1f GB per replica) could not be "
+                               "allocated on every rank" % (host_bytes / 1e9)}
     pinned.copy_(logits)  # untimed: the host copy of the same inputs
     chunk_views, off = [], 0
     for bb in batches:

@@ -72,3 +72,46 @@ def test_reference_arm_under_torchrun_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _pin_rank(rank, world, port, fail_rank, out):
+    import torch
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    real_empty = torch.empty
+
+    def fake_empty(*a, pin_memory=False, **k):
+        # this host has no GPU: a "pinned" buffer is a plain one, except on the failing rank
+        if pin_memory and rank == fail_rank:
+            raise RuntimeError("cannot pin")
+        return real_empty(*a, **k)
+
+    torch.empty = fake_empty
+    ws, r, local = bench.dist_env()
+    dist = bench.init_dist(ws, "gloo")
+    buf = bench.pinned_on_all_ranks((16,), torch.float32, dist, torch.device("cpu"))
+    dist.barrier()
+    dist.destroy_process_group()
+    out.put((r, buf is None))
+
+
+@pytest.mark.parametrize("fail_rank", [-1, 1])
+def test_pinned_input_agreed_over_ranks(fail_rank):
+    """The end-to-end legs pin each replica's whole step input; when one rank cannot, every
+    rank drops the leg together (none is left waiting in a collective)."""
+    pytest.importorskip("torch")
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_pin_rank, args=(r, 2, port, fail_rank, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(out.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    none = fail_rank >= 0
+    assert got == [(0, none), (1, none)]
