@@ -313,11 +313,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* t
       : "memory");
 }
 
-__device__ __forceinline__ void umma_bf16_pair(uint32_t dt, uint64_t a, uint64_t b, uint32_t accum) {
+// The operand descriptors come as 32-bit halves: the high half is the same for
+// every stage, so the issuing thread only advances the low half (start
+// address) with 32-bit adds.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t dt, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi,
+                                               uint32_t accum) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
-      "l"(a), "l"(b), "r"(GP_IDESC), "r"(accum));
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(dt),
+      "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(GP_IDESC), "r"(accum));
 }
 
 // Arrives on the barrier at this offset in both CTAs once every MMA issued so
@@ -380,7 +386,10 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_c
     // ---------------------------------------------------------- producers
     if (lane == 0) {
       const uint32_t bar0 = mapa_u32(smem_u32(full), 0);  // the leader's full[0]
-      int64_t g = 0;
+      int64_t g = 0;  // stages filled so far
+      int s = 0;      // next stage (g mod STAGES) and its round (g / STAGES)
+      int64_t round = 0;
+      uint32_t ph = 0;  // parity of the release that round `round` >= 1 waits for: (round - 1) & 1
       bool ok = true;
       // the leader fetches each tile id one tile ahead, so the atomic's round
       // trip overlaps the previous tile's loads
@@ -408,8 +417,7 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_c
         const int arow = mt * (2 * GP_BM) + (int)rank * GP_BM;
         const int brow = (2 * pair + (int)rank) * 128;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const int s = (int)(g % GP_STAGES);
-          if (g >= GP_STAGES && !mbar_wait_cl(&empty[s], (uint32_t)((g / GP_STAGES - 1) & 1), p.status)) {
+          if (g >= GP_STAGES && !mbar_wait_cl(&empty[s], ph, p.status)) {
             ok = false;
             break;
           }
@@ -418,6 +426,11 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_c
           const uint32_t barc = bar0 + (uint32_t)(s * 8);
           tma_load_2d_pair(st, &p.tmx, kb * GP_BK, arow, barc);
           tma_load_2d_pair(st + GP_A_BYTES, &p.tmw, kb * GP_BK, brow, barc);
+          if (++s == GP_STAGES) {  // the next round waits on the releases of this one
+            s = 0;
+            ++round;
+            ph = (uint32_t)((round - 1) & 1);
+          }
         }
         // after an expired wait the leader's next turn publishes the end
         // marker (-1), so the readers stop; the peer has nothing to publish
@@ -437,7 +450,13 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_c
     if (lane == 0) {
       bool ok = true;
       if (leader) {
-        int64_t g = 0;
+        // stage s, its full-barrier parity, and stage 0's descriptors: a stage's
+        // descriptors differ from stage 0's only in the start address (low half)
+        int s = 0;
+        uint32_t ph = 0;
+        const uint64_t d0 = umma_desc_sw128(smem_u32(gsm));
+        const uint32_t d0_lo = (uint32_t)d0, d_hi = (uint32_t)(d0 >> 32);
+        constexpr uint32_t STAGE_STEP = GP_STAGE_BYTES >> 4, B_STEP = GP_A_BYTES >> 4;
         for (int64_t j = 0; ok; ++j) {
           if (!mbar_wait_cl(&tid_full[j % GP_TRING], (uint32_t)((j / GP_TRING) & 1), p.status)) {
             ok = false;
@@ -451,19 +470,21 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_c
           }
           tc_fence_after();
           const uint32_t dt = tmem + (uint32_t)(a * GP_BN);
-          for (int kb = 0; kb < nkb; ++kb, ++g) {
-            const int s = (int)(g % GP_STAGES);
-            if (!mbar_wait_cl(&full[s], (uint32_t)((g / GP_STAGES) & 1), p.status)) {
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait_cl(&full[s], ph, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t sa = smem_u32(gsm + (size_t)s * GP_STAGE_BYTES);
-            const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + GP_A_BYTES);
+            const uint32_t a_lo = d0_lo + (uint32_t)s * STAGE_STEP, b_lo = a_lo + B_STEP;
 #pragma unroll
             for (int kk = 0; kk < GP_BK / 16; ++kk)  // K = 16 per instruction: 32 bytes along the row
-              umma_bf16_pair(dt, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), (kb | kk) ? 1u : 0u);
+              umma_bf16_pair(dt, a_lo + 2u * kk, b_lo + 2u * kk, d_hi, (kb | kk) ? 1u : 0u);
             umma_commit_pair(&empty[s]);
+            if (++s == GP_STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
           if (ok) umma_commit_pair(&tfull[a]);
         }
