@@ -9,8 +9,8 @@
 // Figure 2(a) (per-layer expert co-activation).
 //
 // Design (GB300):
-//   * Persistent grid, one CTA per SM, sixteen warps, no producer warp.  Work
-//     items are (layer, 32-token tile); tile n of the CTA goes to warp n % 16.
+//   * Persistent grid, one CTA per SM, twenty warps, no producer warp.  Work
+//     items are (layer, 32-token tile); tile n of the CTA goes to warp n % 20.
 //     A tile is fetched in column slices (32 rows x 32 experts, 4 KB) by 3-D
 //     TMA tensor copies ([L][T][E] logits, rows past T zero-filled) into two
 //     slice buffers that the warp owns: as soon as the warp has folded a
@@ -52,7 +52,7 @@ namespace moer {
 
 // Geometry (compile-time tunables with the measured defaults).
 #ifndef MOER_TPR_CW
-#define MOER_TPR_CW 16  // warps per CTA
+#define MOER_TPR_CW 20  // warps per CTA (the most whose slice buffers fit beside the 32-bit tile)
 #endif
 #ifndef MOER_TPR_RING
 #define MOER_TPR_RING 2  // slice buffers per warp
