@@ -11,7 +11,13 @@ stream:
 
 or, when the router logits are not materialised, `moer_gate_topk` (the bf16
 gate GEMM with top-k, block counts and co-activation fused behind it) in
-place of the first call.
+place of the first call.  `moer_ids_signature` derives the block counts and
+co-activation from top-k ids already produced (the bench uses it to time the
+dominant kernel's call alone).
+
+`calibrate` runs the offline half (idf, greedy layer mask, balanced K-means
+centroids, spectral expert groups) call by call on the GPU, and
+`save_calibration` / `load_calibration` carry its result to the serving side.
 
 This module only marshals arguments and orders calls; every step of the
 path runs in the library's kernels.
