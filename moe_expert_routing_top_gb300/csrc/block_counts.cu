@@ -211,29 +211,30 @@ constexpr int AI_U = 4;                      // tokens per thread per item, load
 constexpr int AI_CHUNK = AI_THREADS * AI_U;  // tokens per work item
 
 // The tile's rows are E + 1 words apart, so the bank of D[a][b] depends on a
-// as well as b.
+// as well as b.  The pairs a < b go out a warp per row a, its lanes along b;
+// the diagonal a warp per expert, as the sum of its row and column of D (D[a][a]
+// is 0: a kept row's ids are distinct) over k - 1, by a warp reduction -- no
+// shared atomics, which a row's lanes would all aim at one counter.
 __device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* dst) {
+  (void)rsum;
   const int rs = E + 1;
-  for (int c = threadIdx.x; c < E * E; c += AI_THREADS) {
-    const int a = c / E, b = c - a * E;
-    if (a < b) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NW = AI_THREADS / 32;
+  for (int a = warp; a < E - 1; a += NW)
+    for (int b = a + 1 + lane; b < E; b += 32) {
       const int v = tile[a * rs + b] + tile[b * rs + a];
       if (v != 0) {
         atomicAdd(&dst[a * E + b], v);
         atomicAdd(&dst[b * E + a], v);
-        atomicAdd(&rsum[a], v);
-        atomicAdd(&rsum[b], v);
       }
     }
+  for (int a = warp; a < E; a += NW) {
+    int sum = 0;
+    for (int b = lane; b < E; b += 32) sum += tile[a * rs + b] + tile[b * rs + a];
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+    if (lane == 0 && sum != 0) atomicAdd(&dst[a * E + a], sum / (k - 1));
   }
-  __syncthreads();
-  for (int a = threadIdx.x; a < E; a += AI_THREADS) {
-    const int v = rsum[a];
-    if (v != 0) {
-      atomicAdd(&dst[a * E + a], v / (k - 1));
-      rsum[a] = 0;
-    }
-  }
+  __syncthreads();  // every read of the tile is done before it is cleared
   for (int c = threadIdx.x; c < E * rs; c += AI_THREADS) tile[c] = 0;
   __syncthreads();
 }

@@ -166,37 +166,39 @@ __device__ __forceinline__ void aff_add(uint32_t* aff, int a, int b) {
 // Co-activation is symmetric: A[a][b] = D[a][b] + D[b][a] for a != b, and,
 // every row holding k distinct experts, the diagonal (the expert's load) is
 // its off-diagonal row sum divided by k - 1.  Adds the tile to layer `layer`
-// of the global co-activation and clears it.  All consumer threads call this
-// (it holds a barrier); `skip` leaves the tile alone (a warp timed out).
+// of the global co-activation and clears it; the sums are formed by warp
+// reductions, with no shared atomics (a row's lanes would all hit one
+// counter).  All consumer threads call this (it holds a barrier); `skip`
+// leaves the tile alone (a warp timed out).
 template <int E, int K>
 __device__ void tpr_flush_aff(const K1Params& p, uint32_t* aff, int* rsum, int layer, bool skip) {
   using G = TprGeo<E>;
+  (void)rsum;
   int32_t* dst = p.affinity + (size_t)layer * E * E;
   if (!skip) {
-    for (int c = threadIdx.x; c < E * E; c += G::THREADS) {
-      const int a = c / E, b = c % E;
-      if (a < b) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the pairs a < b, a warp per row a and its lanes along b: A[a][b] = A[b][a] =
+    // D[a][b] + D[b][a]
+    for (int a = warp; a < E - 1; a += G::CW)
+      for (int b = a + 1 + lane; b < E; b += 32) {
         const int v = (int)(aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a));
         if (v != 0) {
           atomicAdd(&dst[a * E + b], v);
           atomicAdd(&dst[b * E + a], v);
-          atomicAdd(&rsum[a], v);
-          atomicAdd(&rsum[b], v);
         }
       }
+    // the diagonal, a warp per expert a: the sum of its row and column of D over
+    // all b (D[a][a] is 0: a row's k experts are distinct), divided by k - 1
+    for (int a = warp; a < E; a += G::CW) {
+      uint32_t sum = 0u;
+      for (int b = lane; b < E; b += 32) sum += aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a);
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+      if (lane == 0 && sum != 0u) atomicAdd(&dst[a * E + a], (int)(sum / (uint32_t)(K - 1)));
     }
   }
-  named_bar(1, G::THREADS);
-  if (!skip) {
-    for (int a = threadIdx.x; a < E; a += G::THREADS) {
-      const int v = rsum[a];
-      if (v != 0) {
-        atomicAdd(&dst[a * E + a], v / (K - 1));
-        rsum[a] = 0;
-      }
-    }
+  named_bar(1, G::THREADS);  // every read of the tile is done before it is cleared
+  if (!skip)
     for (int c = threadIdx.x; c < (int)G::AFF_WORDS; c += G::THREADS) aff[c] = 0u;
-  }
 }
 
 template <int E, int K>
