@@ -27,6 +27,9 @@ struct K1Params {
   // bytes between rows of the co-activation tile, at run time for the same
   // reason: each pair's shared address is then one multiply-add (FMA pipe)
   uint32_t aff_row_bytes;
+  // 1 when `affinity` is 8-byte aligned: the fold then adds two neighbouring
+  // counts of a row with one 64-bit red (no carry crosses: counts fit in int32)
+  int aff_pairs64;
   int16_t slot_of_layer[256];  // mask slot of each layer, -1 if not a mask layer
 };
 

@@ -268,6 +268,7 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
   p.key_hi_mul = 1u << 24;
   p.key_lo_mul = 1u << 8;
   p.aff_row_bytes = (uint32_t)(d->E + 1) * 4u;  // the 32-bit tile's row pitch (E + 1 words)
+  p.aff_pairs64 = (reinterpret_cast<uintptr_t>(affinity) & 7u) == 0 ? 1 : 0;
   for (int l = 0; l < 256; ++l) p.slot_of_layer[l] = -1;
   for (int i = 0; i < d->m; ++i) p.slot_of_layer[d->mask[i]] = (int16_t)i;
   const int grid = (int)min64(p.nitems, sms);

@@ -177,23 +177,44 @@ __device__ void tpr_flush_aff(const K1Params& p, uint32_t* aff, int* rsum, int l
   int32_t* dst = p.affinity + (size_t)layer * E * E;
   if (!skip) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // the pairs a < b, a warp per row a and its lanes along b: A[a][b] = A[b][a] =
-    // D[a][b] + D[b][a]
-    for (int a = warp; a < E - 1; a += G::CW)
-      for (int b = a + 1 + lane; b < E; b += 32) {
-        const int v = (int)(aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a));
-        if (v != 0) {
-          atomicAdd(&dst[a * E + b], v);
-          atomicAdd(&dst[b * E + a], v);
+    if (p.aff_pairs64) {
+      // a warp per row a: first the diagonal, the sum of the row and column of D
+      // over all b (D[a][a] is 0: a row's k experts are distinct) over k - 1; then
+      // the whole row A[a][b] = D[a][b] + D[b][a], two neighbouring counts per
+      // 64-bit red
+      for (int a = warp; a < E; a += G::CW) {
+        uint32_t sum = 0u;
+        for (int b = lane; b < E; b += 32) sum += aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a);
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+        const uint32_t diag = sum / (uint32_t)(K - 1);
+        for (int b = 2 * lane; b < E; b += 64) {
+          const uint32_t v0 = b == a ? diag : aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a);
+          const uint32_t v1 = b + 1 == a ? diag : aff_get<E>(aff, a, b + 1) + aff_get<E>(aff, b + 1, a);
+          if ((v0 | v1) != 0u) {
+            const unsigned long long v = ((unsigned long long)v1 << 32) | v0;
+            asm volatile("red.global.add.u64 [%0], %1;" ::"l"(dst + (size_t)a * E + b), "l"(v) : "memory");
+          }
         }
       }
-    // the diagonal, a warp per expert a: the sum of its row and column of D over
-    // all b (D[a][a] is 0: a row's k experts are distinct), divided by k - 1
-    for (int a = warp; a < E; a += G::CW) {
-      uint32_t sum = 0u;
-      for (int b = lane; b < E; b += 32) sum += aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a);
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
-      if (lane == 0 && sum != 0u) atomicAdd(&dst[a * E + a], (int)(sum / (uint32_t)(K - 1)));
+    } else {
+      // the pairs a < b, a warp per row a and its lanes along b: A[a][b] = A[b][a] =
+      // D[a][b] + D[b][a]
+      for (int a = warp; a < E - 1; a += G::CW)
+        for (int b = a + 1 + lane; b < E; b += 32) {
+          const int v = (int)(aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a));
+          if (v != 0) {
+            atomicAdd(&dst[a * E + b], v);
+            atomicAdd(&dst[b * E + a], v);
+          }
+        }
+      // the diagonal, a warp per expert a: the sum of its row and column of D over
+      // all b (D[a][a] is 0: a row's k experts are distinct), divided by k - 1
+      for (int a = warp; a < E; a += G::CW) {
+        uint32_t sum = 0u;
+        for (int b = lane; b < E; b += 32) sum += aff_get<E>(aff, a, b) + aff_get<E>(aff, b, a);
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+        if (lane == 0 && sum != 0u) atomicAdd(&dst[a * E + a], (int)(sum / (uint32_t)(K - 1)));
+      }
     }
   }
   named_bar(1, G::THREADS);  // every read of the tile is done before it is cleared
