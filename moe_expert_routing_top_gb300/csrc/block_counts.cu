@@ -211,28 +211,49 @@ constexpr int AI_U = 4;                      // tokens per thread per item, load
 constexpr int AI_CHUNK = AI_THREADS * AI_U;  // tokens per work item
 
 // The tile's rows are E + 1 words apart, so the bank of D[a][b] depends on a
-// as well as b.  The pairs a < b go out a warp per row a, its lanes along b;
-// the diagonal a warp per expert, as the sum of its row and column of D (D[a][a]
-// is 0: a kept row's ids are distinct) over k - 1, by a warp reduction -- no
-// shared atomics, which a row's lanes would all aim at one counter.
+// as well as b.  A warp per row a, by warp reductions -- no shared atomics,
+// which a row's lanes would all aim at one counter: the diagonal is the sum of
+// the row and column of D (D[a][a] is 0: a kept row's ids are distinct) over
+// k - 1, and A[a][b] = D[a][b] + D[b][a] goes out with 64-bit reds (two
+// neighbouring counts) when the output is 8-byte aligned, else pair by pair.
 __device__ void affinity_ids_flush(int* tile, int* rsum, int E, int k, int32_t* dst) {
   (void)rsum;
   const int rs = E + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int NW = AI_THREADS / 32;
-  for (int a = warp; a < E - 1; a += NW)
-    for (int b = a + 1 + lane; b < E; b += 32) {
-      const int v = tile[a * rs + b] + tile[b * rs + a];
-      if (v != 0) {
-        atomicAdd(&dst[a * E + b], v);
-        atomicAdd(&dst[b * E + a], v);
+  if ((reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+    // 8-byte aligned output: a warp adds its row's whole symmetric row, diagonal
+    // included, two neighbouring counts per 64-bit red (counts fit in int32, so no
+    // carry crosses into the upper count)
+    for (int a = warp; a < E; a += NW) {
+      int sum = 0;
+      for (int b = lane; b < E; b += 32) sum += tile[a * rs + b] + tile[b * rs + a];
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+      const uint32_t diag = (uint32_t)(sum / (k - 1));
+      for (int b = 2 * lane; b < E; b += 64) {
+        const uint32_t v0 = b == a ? diag : (uint32_t)(tile[a * rs + b] + tile[b * rs + a]);
+        const uint32_t v1 = b + 1 == a ? diag : (uint32_t)(tile[a * rs + b + 1] + tile[(b + 1) * rs + a]);
+        if ((v0 | v1) != 0u) {
+          const unsigned long long v = ((unsigned long long)v1 << 32) | v0;
+          asm volatile("red.global.add.u64 [%0], %1;" ::"l"(dst + (size_t)a * E + b), "l"(v) : "memory");
+        }
       }
     }
-  for (int a = warp; a < E; a += NW) {
-    int sum = 0;
-    for (int b = lane; b < E; b += 32) sum += tile[a * rs + b] + tile[b * rs + a];
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
-    if (lane == 0 && sum != 0) atomicAdd(&dst[a * E + a], sum / (k - 1));
+  } else {
+    for (int a = warp; a < E - 1; a += NW)
+      for (int b = a + 1 + lane; b < E; b += 32) {
+        const int v = tile[a * rs + b] + tile[b * rs + a];
+        if (v != 0) {
+          atomicAdd(&dst[a * E + b], v);
+          atomicAdd(&dst[b * E + a], v);
+        }
+      }
+    for (int a = warp; a < E; a += NW) {
+      int sum = 0;
+      for (int b = lane; b < E; b += 32) sum += tile[a * rs + b] + tile[b * rs + a];
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+      if (lane == 0 && sum != 0) atomicAdd(&dst[a * E + a], sum / (k - 1));
+    }
   }
   __syncthreads();  // every read of the tile is done before it is cleared
   for (int c = threadIdx.x; c < E * rs; c += AI_THREADS) tile[c] = 0;
