@@ -278,20 +278,21 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+// (barrier given by its shared::cta address)
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait for a phase whose arrivals may come from the other CTA.
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, uint32_t* status) {
   if (mbar_try_wait_cl(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
@@ -301,6 +302,9 @@ __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, uin
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  return mbar_wait_cl(smem_u32(bar), parity, status);
 }
 
 // Tiled 2-D copy into this CTA's shared memory, completing on a barrier that
@@ -328,13 +332,14 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t dt, uint32_t a_lo, uint3
 
 // Arrives on the barrier at this offset in both CTAs once every MMA issued so
 // far by this thread has completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
+          bar),
       "h"((uint16_t)3)
       : "memory");
 }
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) { umma_commit_pair(smem_u32(bar)); }
 
 template <int K>
 __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_constant__ GateParams p) {
@@ -450,44 +455,72 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gate_pair_kernel(const __grid_c
     if (lane == 0) {
       bool ok = true;
       if (leader) {
-        // stage s, its full-barrier parity, and stage 0's descriptors: a stage's
-        // descriptors differ from stage 0's only in the start address (low half)
-        int s = 0;
-        uint32_t ph = 0;
+        // The stage ring is unrolled, so each stage's barrier addresses are
+        // immediates and its operand descriptors (low halves: start address,
+        // per stage and K step) sit in registers: an MMA issue needs no
+        // arithmetic.  The issuing thread shares its SM sub-partition with an
+        // epilogue warp whose comparator networks keep the integer pipe busy,
+        // and any integer work here would queue behind them.
         const uint64_t d0 = umma_desc_sw128(smem_u32(gsm));
-        const uint32_t d0_lo = (uint32_t)d0, d_hi = (uint32_t)(d0 >> 32);
+        const uint32_t d_hi = (uint32_t)(d0 >> 32);
         constexpr uint32_t STAGE_STEP = GP_STAGE_BYTES >> 4, B_STEP = GP_A_BYTES >> 4;
-        for (int64_t j = 0; ok; ++j) {
+        uint32_t da[GP_STAGES][GP_BK / 16], db[GP_STAGES][GP_BK / 16];
+#pragma unroll
+        for (int st = 0; st < GP_STAGES; ++st)
+#pragma unroll
+          for (int kk = 0; kk < GP_BK / 16; ++kk) {  // K = 16 per instruction: 32 bytes along the row
+            da[st][kk] = (uint32_t)d0 + (uint32_t)st * STAGE_STEP + 2u * kk;
+            db[st][kk] = da[st][kk] + B_STEP;
+          }
+        const uint32_t full_a = smem_u32(full), empty_a = smem_u32(empty);
+        uint32_t ph = 0;  // parity of the full barriers in this round of the ring
+        int64_t j = 0;    // tiles begun
+        uint32_t dt = 0, tfull_a = 0;
+        int kb_left = 0;  // K blocks left in the current tile
+        // Starts tile j: its id, then a drained accumulator.  False at the end
+        // marker or when a wait expired (ok cleared).
+        auto begin_tile = [&]() -> bool {
           if (!mbar_wait_cl(&tid_full[j % GP_TRING], (uint32_t)((j / GP_TRING) & 1), p.status)) {
             ok = false;
-            break;
+            return false;
           }
-          if (tile_ring[j % GP_TRING] < 0) break;
+          if (tile_ring[j % GP_TRING] < 0) return false;
           const int a = (int)(j & 1);
           if (j >= 2 && !mbar_wait_cl(&tempty[a], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
             ok = false;
-            break;
+            return false;
           }
           tc_fence_after();
-          const uint32_t dt = tmem + (uint32_t)(a * GP_BN);
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait_cl(&full[s], ph, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_lo = d0_lo + (uint32_t)s * STAGE_STEP, b_lo = a_lo + B_STEP;
+          dt = tmem + (uint32_t)(a * GP_BN);
+          tfull_a = smem_u32(&tfull[a]);
+          kb_left = nkb;
+          return true;
+        };
+        if (begin_tile()) {
+          for (;;) {
 #pragma unroll
-            for (int kk = 0; kk < GP_BK / 16; ++kk)  // K = 16 per instruction: 32 bytes along the row
-              umma_bf16_pair(dt, a_lo + 2u * kk, b_lo + 2u * kk, d_hi, (kb | kk) ? 1u : 0u);
-            umma_commit_pair(&empty[s]);
-            if (++s == GP_STAGES) {
-              s = 0;
-              ph ^= 1u;
+            for (int st = 0; st < GP_STAGES; ++st) {
+              if (!mbar_wait_cl(full_a + 8u * st, ph, p.status)) {
+                ok = false;
+                goto mma_done;
+              }
+              tc_fence_after();
+              {
+                const uint32_t acc = kb_left != nkb ? 1u : 0u;  // a tile's first K block overwrites
+#pragma unroll
+                for (int kk = 0; kk < GP_BK / 16; ++kk) umma_bf16_pair(dt, da[st][kk], db[st][kk], d_hi, kk ? 1u : acc);
+              }
+              umma_commit_pair(empty_a + 8u * st);
+              if (--kb_left == 0) {
+                umma_commit_pair(tfull_a);
+                ++j;
+                if (!begin_tile()) goto mma_done;
+              }
             }
+            ph ^= 1u;
           }
-          if (ok) umma_commit_pair(&tfull[a]);
         }
+      mma_done:
         // every MMA issued has completed once this arrives (in both CTAs)
         umma_commit_pair(drain);
       }
