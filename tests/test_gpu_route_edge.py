@@ -149,3 +149,21 @@ def test_route_live_across_staging_buffers(env, D):
     gu.check_live_route(ch, odist, 0.1, loads0, och)
     assert np.array_equal(np.bincount(ch, minlength=D) + loads0, loads)
     assert loads.sum() == loads0.sum() + R
+
+
+@pytest.mark.parametrize("D,base", [(16, (1 << 25) - 300), (16, (1 << 25) - 100), (48, (1 << 24) - 300),
+                                    (48, (1 << 24) - 100), (16, (1 << 31) - 1000)])
+def test_route_live_large_loads(env, D, base):
+    """Live routing from large starting loads (around 2^24 and 2^25, and near the int32 limit,
+    where 200 requests raise no load past it) gives the oracle's picks and the oracle's final
+    loads: the pick compares the loads themselves, however large."""
+    orc = oracle.get()
+    R, m, E = 200, 2, 64
+    cnt, idf, cen = _inputs(31 + D, R, m, E, D)
+    loads0 = (base + np.random.RandomState(D).randint(0, 40, size=D)).astype(np.int32)
+    tau = 1e6 if base > (1 << 30) else 0.1                       # near int32: every decoder in the band
+    _, dist, ch, loads = _run(env, cnt, idf, cen, tau, loads0, True)
+    _, odist = orc.sig_dist(cnt, idf, cen)
+    och, oloads = orc.route(odist, tau, loads0, True)
+    gu.check_live_route(ch, odist, tau, loads0, och)
+    assert np.array_equal(np.bincount(ch, minlength=D).astype(np.int64) + loads0, loads.astype(np.int64))
