@@ -74,6 +74,9 @@ struct TprGeo {
   static constexpr int THREADS = CW * 32;
   static_assert(E % SW == 0 && Q >= 1, "whole slices per row");
   static_assert(R >= 2, "a warp needs a second slice buffer to overlap copy and compute");
+  // every tile starts in buffer 0, so a slice's buffer and the refill that
+  // follows it are fixed by its place q in the tile
+  static_assert(R <= Q && Q % R == 0, "whole rounds of the slice buffers per tile");
   static constexpr uint32_t SLICE_BYTES = (uint32_t)TT * SW * 4;
   static constexpr size_t OFF_ROWS = 0;
   static constexpr size_t OFF_AFF = OFF_ROWS + (size_t)CW * R * SLICE_BYTES;
@@ -246,40 +249,33 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   int64_t cur = epoch_of(i0);
   const int l0 = (int)((i0 + warp) / p.ntiles);
   const int t0 = (int)((i0 + warp) - (int64_t)l0 * p.ntiles);
-  // Copy side (lane 0): the warp's slices in order, slice j = (its tile j / Q,
-  // experts SW (j % Q) ...), slice j into buffer j % R.
-  const int64_t nsl = (N > warp ? (N - warp + G::CW - 1) / G::CW : 0) * Q;
-  int64_t js = 0;  // next slice to copy
-  int cq = 0, cl = l0, ct = t0;
-  auto fetch = [&](int buf) {
+  // Slice q of the warp's tile i (its tile n = warp + i CW) is its slice
+  // j = i Q + q: buffer j % R = q % R, use j / R of that buffer.  Lane 0
+  // copies the first R slices of the first tile, then, each time a slice is
+  // folded, refills its buffer with the slice R ahead -- slice q + R of the
+  // same tile, or slice q + R - Q of the warp's next tile.
+  const int64_t ntw = N > warp ? (N - warp + G::CW - 1) / G::CW : 0;  // tiles of this warp
+  auto copy = [&](int buf, int q, int tl, int ly) {
     mbar_arrive_expect_tx(&full[buf], G::SLICE_BYTES);
-    tma_load_3d(ring + (size_t)buf * SLICE_FLOATS, &p.tm_logits, cq * SW, ct * G::TT, cl, &full[buf]);
-    ++js;
-    if (++cq == Q) {
-      cq = 0;
-      ct += G::CW;
-      while (ct >= p.ntiles) {
-        ct -= p.ntiles;
-        ++cl;
-      }
-    }
+    tma_load_3d(ring + (size_t)buf * SLICE_FLOATS, &p.tm_logits, q * SW, tl * G::TT, ly, &full[buf]);
   };
-  if (lane == 0)
-    for (int r = 0; r < R && js < nsl; ++r) fetch(r);
-  // Fold side: slice jw is in buffer wb, phase parity wpar.
-  int64_t jw = 0;
-  int wb = 0;
-  uint32_t wpar = 0;
+  if (lane == 0 && ntw > 0)
+#pragma unroll
+    for (int r = 0; r < R; ++r) copy(r, r, t0, l0);
   bool dead = false;
-  int l = l0, tile = t0;
-  for (int64_t n = warp; n < N; n += G::CW) {
-    if (n > warp) {
-      tile += G::CW;
-      while (tile >= p.ntiles) {
-        tile -= p.ntiles;
-        ++l;
-      }
+  int64_t dead_j = 0;  // the slice whose wait expired
+  int l = l0, tile = t0, nl = l0, ntile = t0;
+  int64_t ti = 0;  // tiles of this warp begun
+  for (int64_t n = warp; n < N; n += G::CW, ++ti) {
+    l = nl;
+    tile = ntile;
+    // the warp's next tile
+    ntile = tile + G::CW;
+    while (ntile >= p.ntiles) {
+      ntile -= p.ntiles;
+      ++nl;
     }
+    const bool has_next = n + G::CW < N;
     const int64_t ep = (int64_t)l * epl + tile / G::FT;
     while (aff_on && cur < ep) {
       named_bar(1, G::THREADS);
@@ -295,25 +291,29 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     uint8_t* out = nullptr;
     if (p.ids != nullptr && (!p.ids_mask_only || slot >= 0))
       out = p.ids + ((size_t)(p.ids_mask_only ? slot : l) * p.T + tok0) * K;
+    // parity of the tile's first use of each buffer: (i Q / R) & 1
+    const uint32_t par0 = ((Q / R) & 1) ? (uint32_t)(ti & 1) : 0u;
     int Tk[8], L9;
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
-      if (!__all_sync(FULL, mbar_wait(&full[wb], wpar, p.status))) {
+      const int buf = q % R;
+      if (!__all_sync(FULL, mbar_wait(&full[buf], par0 ^ (uint32_t)((q / R) & 1), p.status))) {
         dead = true;
+        dead_j = ti * Q + q;
         break;
       }
-      const float* srow = ring + (size_t)wb * SLICE_FLOATS + lane * SW;
+      const float* srow = ring + (size_t)buf * SLICE_FLOATS + lane * SW;
       if (q == 0)
         slice_top8<SW, (K == 8), true>(srow, rot, 0, p.key_hi_mul, p.key_lo_mul, Tk, L9);
       else
         slice_top8<SW, (K == 8), false>(srow, rot, q * SW, p.key_hi_mul, p.key_lo_mul, Tk, L9);
       // every lane has read the buffer: refill it with the slice R ahead
       __syncwarp();
-      if (lane == 0 && js < nsl) fetch(wb);
-      ++jw;
-      if (++wb == R) {
-        wb = 0;
-        wpar ^= 1u;
+      if (lane == 0) {
+        if (q + R < Q)
+          copy(buf, q + R, tile, l);
+        else if (has_next)
+          copy(buf, q + R - Q, ntile, nl);
       }
     }
     if (dead) continue;
@@ -397,8 +397,10 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   }
   if (dead && lane == 0) {
     // a copy stopped answering: wait (bounded) for this warp's copies still in
-    // flight into shared memory before leaving
-    for (int64_t j = jw; j < js; ++j) mbar_wait(&full[j % R], (uint32_t)((j / R) & 1), nullptr);
+    // flight into shared memory before leaving -- slices dead_j .. (issued: R
+    // ahead of the slice that expired, within the warp's slices)
+    const int64_t js = min64(dead_j + R, ntw * Q);
+    for (int64_t j = dead_j; j < js; ++j) mbar_wait(&full[j % R], (uint32_t)((j / R) & 1), nullptr);
   }
   if (aff_on) {
     while (cur < ep_last) {
