@@ -17,6 +17,7 @@ struct K1Params {
   int ids_mask_only;     //   (when set) mask layers only, [m][T][k]
   int32_t* affinity;     // [L][E][E] accumulated, or NULL
   int ntiles;            // token tiles per layer
+  int tail_rows;         // tokens in the last tile of a layer (thread-per-row kernel)
   int64_t nitems;        // L * ntiles work items
   uint32_t* status;      // sticky workspace status word
   // 2^24 and 2^8, passed at run time so that the key builder's shift-and-

@@ -263,6 +263,7 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
   p.ids_mask_only = mask_only ? 1 : 0;
   p.affinity = affinity;
   p.ntiles = ntiles;
+  p.tail_rows = (int)(T - (int64_t)(ntiles - 1) * TT);
   p.nitems = (int64_t)d->L * ntiles;
   p.status = status;
   p.key_hi_mul = 1u << 24;
@@ -272,6 +273,8 @@ moer_status topk_signature_launch(const moer_dims* d, const float* logits, int64
   for (int l = 0; l < 256; ++l) p.slot_of_layer[l] = -1;
   for (int i = 0; i < d->m; ++i) p.slot_of_layer[d->mask[i]] = (int16_t)i;
   const int grid = (int)min64(p.nitems, sms);
+  // a CTA counts its work items in 32 bits
+  if (grid > 0 && (p.nitems + grid - 1) / grid >= (int64_t(1) << 31)) return MOER_ERANGE;
   cudaError_t e;
   if (tpr)
     e = tpr_run(E, k, p, grid, st);

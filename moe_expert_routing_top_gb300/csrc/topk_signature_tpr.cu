@@ -238,15 +238,16 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   int* rsum = reinterpret_cast<int*>(smem + G::OFF_RSUM);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR) + warp * R;
   const bool aff_on = p.affinity != nullptr;
-  const int64_t N = i1 - i0;
-  // fold epochs: (layer, tile / FT), numbered l * epl + tile / FT, monotone in the item
+  const int N = (int)(i1 - i0);  // this CTA's items (the host keeps them below 2^31)
+  // fold epochs: (layer, tile / FT), numbered l * epl + tile / FT, monotone in
+  // the item (below 2^24: fewer than 256 layers, epl <= 2^26 / FT)
   const int epl = (p.ntiles + G::FT - 1) / G::FT;
   auto epoch_of = [&](int64_t item) {
     const int li = (int)(item / p.ntiles);
-    return (int64_t)li * epl + (item - (int64_t)li * p.ntiles) / G::FT;
+    return li * epl + (int)(item - (int64_t)li * p.ntiles) / G::FT;
   };
-  const int64_t ep_last = epoch_of(i1 - 1);
-  int64_t cur = epoch_of(i0);
+  const int ep_last = epoch_of(i1 - 1);
+  int cur = epoch_of(i0);
   const int l0 = (int)((i0 + warp) / p.ntiles);
   const int t0 = (int)((i0 + warp) - (int64_t)l0 * p.ntiles);
   // Slice q of the warp's tile i (its tile n = warp + i CW) is its slice
@@ -254,7 +255,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
   // copies the first R slices of the first tile, then, each time a slice is
   // folded, refills its buffer with the slice R ahead -- slice q + R of the
   // same tile, or slice q + R - Q of the warp's next tile.
-  const int64_t ntw = N > warp ? (N - warp + G::CW - 1) / G::CW : 0;  // tiles of this warp
+  const int ntw = N > warp ? (N - warp + G::CW - 1) / G::CW : 0;  // tiles of this warp
   auto copy = [&](int buf, int q, int tl, int ly) {
     mbar_arrive_expect_tx(&full[buf], G::SLICE_BYTES);
     tma_load_3d(ring + (size_t)buf * SLICE_FLOATS, &p.tm_logits, q * SW, tl * G::TT, ly, &full[buf]);
@@ -263,10 +264,10 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
 #pragma unroll
     for (int r = 0; r < R; ++r) copy(r, r, t0, l0);
   bool dead = false;
-  int64_t dead_j = 0;  // the slice whose wait expired
+  int dead_j = 0;  // the slice whose wait expired
   int l = l0, tile = t0, nl = l0, ntile = t0;
-  int64_t ti = 0;  // tiles of this warp begun
-  for (int64_t n = warp; n < N; n += G::CW, ++ti) {
+  int ti = 0;  // tiles of this warp begun
+  for (int n = warp; n < N; n += G::CW, ++ti) {
     l = nl;
     tile = ntile;
     // the warp's next tile
@@ -276,7 +277,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
       ++nl;
     }
     const bool has_next = n + G::CW < N;
-    const int64_t ep = (int64_t)l * epl + tile / G::FT;
+    const int ep = l * epl + tile / G::FT;
     while (aff_on && cur < ep) {
       named_bar(1, G::THREADS);
       tpr_flush_aff<E, K>(p, aff, rsum, (int)(cur / epl), dead);
@@ -286,7 +287,7 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     cur = ep;
     if (dead) continue;
     const int64_t tok0 = (int64_t)tile * G::TT;
-    const int ntok = (int)min64(G::TT, p.T - tok0);
+    const int ntok = tile == p.ntiles - 1 ? p.tail_rows : G::TT;
     const int slot = p.slot_of_layer[l];
     uint8_t* out = nullptr;
     if (p.ids != nullptr && (!p.ids_mask_only || slot >= 0))
@@ -399,8 +400,8 @@ __device__ void tpr_consumer(const K1Params& p, char* smem, int64_t i0, int64_t 
     // a copy stopped answering: wait (bounded) for this warp's copies still in
     // flight into shared memory before leaving -- slices dead_j .. (issued: R
     // ahead of the slice that expired, within the warp's slices)
-    const int64_t js = min64(dead_j + R, ntw * Q);
-    for (int64_t j = dead_j; j < js; ++j) mbar_wait(&full[j % R], (uint32_t)((j / R) & 1), nullptr);
+    const int js = min(dead_j + R, ntw * Q);
+    for (int j = dead_j; j < js; ++j) mbar_wait(&full[j % R], (uint32_t)((j / R) & 1), nullptr);
   }
   if (aff_on) {
     while (cur < ep_last) {
