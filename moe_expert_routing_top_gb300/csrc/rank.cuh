@@ -81,31 +81,60 @@ __device__ __forceinline__ void clean8_desc(int (&m)[8]) {
   cas(m[0], m[1]); cas(m[2], m[3]); cas(m[4], m[5]); cas(m[6], m[7]);
 }
 
-// Folds the losers of a half-cleaner step (mins of T[i] and U[7 - i]) into
-// the running 9th key with 3-input maxima (one ALU op each).
-__device__ __forceinline__ int fold_losers(int L9, const int (&lo)[8]) {
-  const int a = __vimax3_s32(lo[0], lo[1], lo[2]);
-  const int b = __vimax3_s32(lo[3], lo[4], lo[5]);
-  const int c = __vimax3_s32(lo[6], lo[7], L9);
-  return __vimax3_s32(a, b, c);
-}
+// One comparator of a descending network whose min output is not needed.
+__device__ __forceinline__ void cmax(int& a, int b) { a = max(a, b); }
 
 // T <- top-8 of T and U (both sorted descending), sorted descending; with
 // WANT9, L9 <- max(L9, 9th key of T and U).
+// Without WANT9: the bitonic split (the maxima of T[i] and U[7 - i]) and a
+// half-cleaner network sort the eight winners, 8 + 24 operations.
+// With WANT9: Batcher's odd-even merge of the two lists (T on wires 0-7, U
+// on wires 8-15; a comparator (i, j) leaves the max on wire i and the min on
+// wire j) pruned to its nine leading outputs: comparators that feed none of
+// them are dropped and those whose min feeds none keep only the max.  Wires
+// 0-7 then hold the new T and wire 8 the 9th key, in 13 full and 7 one-sided
+// comparators: 33 operations, against 44 for the split, the cleaner and a
+// fold of the split's eight losers.
 template <bool WANT9>
 __device__ __forceinline__ void merge8(int (&T)[8], const int (&U)[8], int& L9) {
-  int mrg[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) mrg[i] = max(T[i], U[7 - i]);
   if constexpr (WANT9) {
-    int lo[8];
+    int w[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lo[i] = min(T[i], U[7 - i]);
-    L9 = fold_losers(L9, lo);
+    for (int i = 0; i < 8; ++i) {
+      w[i] = T[i];
+      w[8 + i] = U[i];
+    }
+    cas(w[0], w[8]);
+    cmax(w[4], w[12]);
+    cas(w[4], w[8]);
+    cas(w[2], w[10]);
+    cmax(w[6], w[14]);
+    cmax(w[6], w[10]);
+    cas(w[2], w[4]);
+    cas(w[6], w[8]);
+    cas(w[1], w[9]);
+    cmax(w[5], w[13]);
+    cas(w[5], w[9]);
+    cas(w[3], w[11]);
+    cmax(w[7], w[15]);
+    cmax(w[7], w[11]);
+    cas(w[3], w[5]);
+    cmax(w[7], w[9]);
+    cas(w[1], w[2]);
+    cas(w[3], w[4]);
+    cas(w[5], w[6]);
+    cas(w[7], w[8]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) T[i] = w[i];
+    L9 = max(L9, w[8]);
+  } else {
+    int mrg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mrg[i] = max(T[i], U[7 - i]);
+    clean8_desc(mrg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) T[i] = mrg[i];
   }
-  clean8_desc(mrg);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) T[i] = mrg[i];
 }
 
 // True when the truncated-key top-8 T (descending; L9 the best key outside
