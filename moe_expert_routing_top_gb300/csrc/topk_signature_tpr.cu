@@ -22,8 +22,9 @@
 //     in 16-byte units whose order is XOR-rotated by (lane & 7), which makes
 //     every LDS.128 conflict-free, and folds it 8 values at a time into a
 //     sorted top-8 held in registers: an optimal 19-comparator sorting network
-//     per chunk, then a bitonic split/merge with the running top-8 (the
-//     split's losers, folded with 3-input maxima, give the 9th-ranked key).
+//     per chunk, then a merge with the running top-8 that also yields the
+//     9th-ranked key (Batcher's odd-even merge pruned to its nine leading
+//     outputs, rank.cuh).
 //     Keys are the float's upper 24 bits (signed-int order equals value order
 //     for positive floats) with the value's position in the lane's read order
 //     in the low 8 bits, so keys are unique and min/max networks apply.
