@@ -11,7 +11,10 @@ g++ (qualifiers defined away, min/max from the standard library) and checks:
     maximum of the old one and that 9th;
   - merge8<false> (bitonic split and cleaner) gives the top 8 for the same
     inputs;
-  - both merges agree with a plain sort on random lists, ties included.
+  - both merges agree with a plain sort on random lists, ties included;
+  - trunc_top8_uncertain (7 index bits, as the gate's epilogue uses it) agrees
+    with its definition on random sorted keys, close values and negatives
+    included.
 """
 import os
 import shutil
@@ -22,7 +25,7 @@ import pytest
 HERE = os.path.dirname(os.path.abspath(__file__))
 RANK = os.path.join(os.path.dirname(HERE), "moe_expert_routing_top_gb300", "csrc", "rank.cuh")
 BEGIN = "// ---------------------------------------------------- comparator networks"
-END = "// True when the truncated-key top-8 T"
+END = "// ------------------------------------------------------ exact warp path"
 
 PRE = r"""
 #include <algorithm>
@@ -34,6 +37,7 @@ PRE = r"""
 #define __forceinline__ inline
 using std::max;
 using std::min;
+static inline uint32_t __vimin3_u32(uint32_t a, uint32_t b, uint32_t c) { return std::min(a, std::min(b, c)); }
 """
 
 DRIVER = r"""
@@ -98,6 +102,32 @@ int main() {
     merge8<false>(Tb, U, Lb);
     for (int i = 0; i < 8; ++i) CHECK(T9[i] == all[i] && Tb[i] == all[i]);
     CHECK(L9 == std::max(l9, all[8]));
+  }
+  // certification against its definition (a leading key not a positive finite
+  // float, or a key at or above its predecessor's value bits)
+  for (int it = 0; it < 400000; ++it) {
+    int v[16];
+    const int mode = it % 4;
+    for (int i = 0; i < 16; ++i) {
+      const int base = mode == 0 ? (int)rng() : (mode == 1 ? 0x3F800000 + (int)(rng() % 4096) : (int)(rng() % 1024) - 256);
+      v[i] = base;
+    }
+    // distinct keys: the low 7 bits carry a position
+    for (int i = 0; i < 16; ++i) v[i] = (int)(((uint32_t)v[i] & ~127u) | (uint32_t)i);
+    sorted_desc(v, 16);
+    int T[8];
+    std::copy(v, v + 8, T);
+    const int L9 = v[8];
+    for (int K : {6, 8}) {
+      const int nxt = K == 8 ? L9 : T[K];
+      bool ref = (T[K - 1] < (1 << 7)) || (T[0] >= 0x7F800000);
+      for (int i = 0; i < K; ++i) {
+        const int b = i + 1 < K ? T[i + 1] : nxt;
+        ref = ref || (b >= (int)((uint32_t)T[i] & ~127u));
+      }
+      const bool got = K == 8 ? trunc_top8_uncertain<8, 7>(T, L9) : trunc_top8_uncertain<6, 7>(T, L9);
+      CHECK(got == ref);
+    }
   }
   std::printf("OK\n");
   return 0;
